@@ -1,0 +1,383 @@
+// Decode indexer: block scores of one new query per sequence against the
+// cached block keys, and the exact selection of the (budget-1) best past
+// blocks plus the current block (Qwen3.8-Flash-Next launch post, "Model
+// Architecture / Attention: GDN + QSA"; budget from the model card, "Model
+// Overview / Qwen Sparse Attention").
+//
+// The scan streams the block-key cache once (256 B per block; at 1M tokens
+// 64 MiB per sequence), so it is bound by HBM bandwidth:
+//   * scan kernel: one CTA per (sequence, chunk of blocks); each warp takes
+//     16 blocks at a time with 16-byte loads straight into the warp-MMA
+//     operand registers (the contraction order inside a 32-dim slice is
+//     permuted identically on both operands, which leaves the dot products
+//     unchanged), forms s = sum_h w_h max(0, qi_h . kblk) and keeps the chunk's
+//     scores in shared memory; a CTA-wide radix select then writes the chunk's
+//     exact top-(budget-1) (score desc, block asc) as candidates;
+//   * merge kernel: one CTA per sequence selects the final (budget-1) among
+//     the chunks' candidates, sorts them by block and appends the current
+//     block.
+#include "qsa_common.cuh"
+#include "qsa_kernels.h"
+
+namespace qsa {
+namespace dx {
+
+constexpr int SCAN_THREADS = 256;
+constexpr int MAX_CHUNK = 16384;
+constexpr int MAX_NCHUNK = 47;
+constexpr int MERGE_THREADS = 1024;
+constexpr int MAX_SEL = kMaxBudget - 1;
+
+__device__ __forceinline__ unsigned long long composite(float s, uint32_t b) {
+    return (static_cast<unsigned long long>(f2key(s)) << 32) |
+           static_cast<unsigned long long>(0xFFFFFFFFu - b);
+}
+
+// CTA-wide exact selection over n items given by get(i) -> composite.
+// Returns T with exactly k items >= T.  hist: 256 uint32 in smem;
+// ctl: 4 ints in smem.  All threads must call.
+template <int NT, typename Get>
+__device__ unsigned long long cta_kth(int n, int k, Get get, uint32_t *hist, int *ctl) {
+    unsigned long long prefix = 0;
+    int krem = k;
+    const int tid = threadIdx.x;
+    for (int pass = 0; pass < 8; ++pass) {
+        const int shift = 56 - 8 * pass;
+        for (int i = tid; i < 256; i += NT) hist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < n; i += NT) {
+            const unsigned long long C = get(i);
+            const bool match = (pass == 0) || ((C >> (shift + 8)) == (prefix >> (shift + 8)));
+            if (match) atomicAdd(&hist[(C >> shift) & 255], 1u);
+        }
+        __syncthreads();
+        if (tid < 32) {
+            const int lane = tid;
+            uint32_t cnt[8];
+            uint32_t sum = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                cnt[i] = hist[255 - (lane * 8 + i)];
+                sum += cnt[i];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            const uint32_t excl = incl - sum;
+            if (excl < static_cast<uint32_t>(krem) && static_cast<uint32_t>(krem) <= incl) {
+                uint32_t acc = excl;
+                for (int i = 0; i < 8; ++i) {
+                    if (acc + cnt[i] >= static_cast<uint32_t>(krem)) {
+                        ctl[0] = 255 - (lane * 8 + i);
+                        ctl[1] = static_cast<int>(acc);
+                        ctl[2] = static_cast<int>(cnt[i]);
+                        break;
+                    }
+                    acc += cnt[i];
+                }
+            }
+        }
+        __syncthreads();
+        const int digit = ctl[0];
+        krem -= ctl[1];
+        const int eq = ctl[2];
+        prefix |= static_cast<unsigned long long>(digit) << shift;
+        __syncthreads();
+        if (eq == krem) break;
+    }
+    return prefix;
+}
+
+struct ScanParams {
+    const uint16_t *qi;        // [B, 4, 128]
+    const uint16_t *w;         // [B, 4]
+    const uint16_t *kblk;      // [B, max_ctx/4, 128]
+    const int32_t *seq_lens;   // [B]
+    int64_t max_ctx;
+    int64_t chunk;
+    int nchunk;
+    int k_sel;
+    uint2 *cand;               // [B, nchunk, k_sel]
+    int32_t *cnt;              // [B, nchunk]
+    int32_t *status;
+};
+
+__global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    float *sc = reinterpret_cast<float *>(smem);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.chunk * 4);  // dynamic size: chunk*4 + 256*4 + 16
+    int *ctl = reinterpret_cast<int *>(hist + 256);
+
+    const int s = blockIdx.y;
+    const int ch = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t T = p.seq_lens[s];
+    int32_t *cnt_out = p.cnt + static_cast<int64_t>(s) * p.nchunk + ch;
+    if (T < 1 || T > p.max_ctx) {
+        if (threadIdx.x == 0) {
+            report(p.status, QSA_ERR_DEVICE_CHECK);
+            *cnt_out = 0;
+        }
+        return;
+    }
+    const int64_t c = (T - 1) / kBlock;  // past blocks 0..c-1
+    const int64_t b0 = static_cast<int64_t>(ch) * p.chunk;
+    int64_t b1 = b0 + p.chunk;
+    if (b1 > c) b1 = c;
+    if (b0 >= b1) {
+        if (threadIdx.x == 0) *cnt_out = 0;
+        return;
+    }
+    const int n = static_cast<int>(b1 - b0);
+
+    // B operand: qi^T, columns = heads (4 live of 8), loaded once
+    const int qd = lane & 3, hr = lane >> 2;
+    uint4 bq[4];
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+        bq[kk] = hr < kHI ? *reinterpret_cast<const uint4 *>(
+                                p.qi + (static_cast<int64_t>(s) * kHI + hr) * kDI + kk * 32 + qd * 8)
+                          : make_uint4(0, 0, 0, 0);
+    float w0 = 0.f, w1 = 0.f;
+    if (qd < 2) {
+        w0 = __uint_as_float(static_cast<uint32_t>(p.w[s * kHI + 2 * qd]) << 16);
+        w1 = __uint_as_float(static_cast<uint32_t>(p.w[s * kHI + 2 * qd + 1]) << 16);
+    }
+    const uint16_t *kb = p.kblk + static_cast<int64_t>(s) * (p.max_ctx / kBlock) * kDI;
+
+    for (int mt = warp; mt * 16 < n; mt += SCAN_THREADS / 32) {
+        const int64_t ra = b0 + mt * 16 + hr;
+        const int64_t rb = ra + 8;
+        const int64_t la = ra < b1 ? ra : b1 - 1;
+        const int64_t lb = rb < b1 ? rb : b1 - 1;
+        uint4 ua[4], ub[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            ua[kk] = __ldcs(reinterpret_cast<const uint4 *>(kb + la * kDI + kk * 32 + qd * 8));
+            ub[kk] = __ldcs(reinterpret_cast<const uint4 *>(kb + lb * kDI + kk * 32 + qd * 8));
+        }
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+            mma_bf16_16816(acc, ua[kk].x, ub[kk].x, ua[kk].y, ub[kk].y, bq[kk].x, bq[kk].y);
+            mma_bf16_16816(acc, ua[kk].z, ub[kk].z, ua[kk].w, ub[kk].w, bq[kk].z, bq[kk].w);
+        }
+        float pa = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);  // row hr
+        float pb = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);  // row hr + 8
+        pa += __shfl_xor_sync(0xFFFFFFFFu, pa, 1);
+        pb += __shfl_xor_sync(0xFFFFFFFFu, pb, 1);
+        if (qd == 0) {
+            if (ra < b1) sc[ra - b0] = pa + 0.0f;
+            if (rb < b1) sc[rb - b0] = pb + 0.0f;
+        }
+    }
+    __syncthreads();
+
+    uint2 *out = p.cand + (static_cast<int64_t>(s) * p.nchunk + ch) * p.k_sel;
+    if (n <= p.k_sel) {
+        for (int i = threadIdx.x; i < n; i += SCAN_THREADS)
+            out[i] = make_uint2(__float_as_uint(sc[i]), static_cast<uint32_t>(b0 + i));
+        if (threadIdx.x == 0) *cnt_out = n;
+        return;
+    }
+    auto get = [&](int i) { return composite(sc[i], static_cast<uint32_t>(b0 + i)); };
+    const unsigned long long T_ = cta_kth<SCAN_THREADS>(n, p.k_sel, get, hist, ctl);
+    if (threadIdx.x == 0) ctl[3] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += SCAN_THREADS) {
+        if (get(i) >= T_) {
+            const int pos = atomicAdd(&ctl[3], 1);
+            if (pos < p.k_sel)
+                out[pos] = make_uint2(__float_as_uint(sc[i]), static_cast<uint32_t>(b0 + i));
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (ctl[3] != p.k_sel) report(p.status, QSA_ERR_DEVICE_CHECK);
+        *cnt_out = min(ctl[3], p.k_sel);
+    }
+}
+
+struct MergeParams {
+    const int32_t *seq_lens;
+    int64_t max_ctx;
+    int nchunk;
+    int k_sel;
+    int budget;
+    const uint2 *cand;
+    const int32_t *cnt;
+    int32_t *idx;   // [B, budget]
+    int32_t *status;
+};
+
+__global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint2 *items = reinterpret_cast<uint2 *>(smem);
+    const int cap = MAX_NCHUNK * MAX_SEL;
+    unsigned long long *sortb = reinterpret_cast<unsigned long long *>(items + cap);
+    uint32_t *hist = reinterpret_cast<uint32_t *>(sortb + kMaxBudget);
+    int *ctl = reinterpret_cast<int *>(hist + 256);
+    int *offs = ctl + 8;  // [MAX_NCHUNK + 1]
+
+    const int s = blockIdx.x;
+    const int64_t T = p.seq_lens[s];
+    int32_t *row = p.idx + static_cast<int64_t>(s) * p.budget;
+    if (T < 1 || T > p.max_ctx) {
+        if (threadIdx.x == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
+        for (int i = threadIdx.x; i < p.budget; i += MERGE_THREADS) row[i] = -1;
+        return;
+    }
+    const int64_t c = (T - 1) / kBlock;
+    if (threadIdx.x == 0) {
+        int o = 0;
+        for (int ch = 0; ch < p.nchunk; ++ch) {
+            offs[ch] = o;
+            o += p.k_sel > 0 ? p.cnt[static_cast<int64_t>(s) * p.nchunk + ch] : 0;
+        }
+        offs[p.nchunk] = o;
+    }
+    __syncthreads();
+    const int n = offs[p.nchunk];
+    for (int ch = 0; ch < p.nchunk; ++ch) {
+        const int m = offs[ch + 1] - offs[ch];
+        const uint2 *src = p.cand + (static_cast<int64_t>(s) * p.nchunk + ch) * p.k_sel;
+        for (int i = threadIdx.x; i < m; i += MERGE_THREADS) items[offs[ch] + i] = src[i];
+    }
+    __syncthreads();
+    int m = n;
+    unsigned long long T_ = 0;
+    auto get = [&](int i) { return composite(__uint_as_float(items[i].x), items[i].y); };
+    if (n > p.k_sel) {
+        T_ = cta_kth<MERGE_THREADS>(n, p.k_sel, get, hist, ctl);
+        m = p.k_sel;
+    }
+    if (threadIdx.x == 0) ctl[3] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += MERGE_THREADS) {
+        if (n <= p.k_sel || get(i) >= T_) {
+            const int pos = atomicAdd(&ctl[3], 1);
+            if (pos < kMaxBudget) sortb[pos] = (static_cast<unsigned long long>(items[i].y) << 32) | items[i].x;
+        }
+    }
+    __syncthreads();
+    int P2 = 32;
+    while (P2 < m) P2 <<= 1;
+    for (int i = m + threadIdx.x; i < P2; i += MERGE_THREADS) sortb[i] = ~0ull;
+    __syncthreads();
+    for (int kb = 2; kb <= P2; kb <<= 1) {
+        for (int jb = kb >> 1; jb > 0; jb >>= 1) {
+            for (int i = threadIdx.x; i < P2; i += MERGE_THREADS) {
+                const int ix = i ^ jb;
+                if (ix > i) {
+                    const unsigned long long a = sortb[i], b = sortb[ix];
+                    const bool up = (i & kb) == 0;
+                    if ((a > b) == up) {
+                        sortb[i] = b;
+                        sortb[ix] = a;
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+    for (int i = threadIdx.x; i < p.budget; i += MERGE_THREADS) {
+        int32_t v;
+        if (i < m) v = static_cast<int32_t>(sortb[i] >> 32);
+        else if (i == m) v = static_cast<int32_t>(c);
+        else v = -1;
+        row[i] = v;
+    }
+}
+
+}  // namespace dx
+
+DecodePlan decode_plan(int batch, int64_t max_ctx, int sms) {
+    DecodePlan pl;
+    const int64_t cmax = (max_ctx - 1) / kBlock;
+    int64_t target = (static_cast<int64_t>(batch) * cmax + static_cast<int64_t>(sms) * 4 - 1) /
+                     (static_cast<int64_t>(sms) * 4);
+    int64_t ch = ((target + 255) / 256) * 256;
+    if (ch < 1024) ch = 1024;
+    if (ch > dx::MAX_CHUNK) ch = dx::MAX_CHUNK;
+    int64_t nchunk = cmax > 0 ? (cmax + ch - 1) / ch : 1;
+    if (nchunk > dx::MAX_NCHUNK) {
+        ch = (((cmax + dx::MAX_NCHUNK - 1) / dx::MAX_NCHUNK + 255) / 256) * 256;
+        nchunk = (cmax + ch - 1) / ch;
+    }
+    pl.chunk = ch;
+    pl.nchunk = static_cast<int>(nchunk < 1 ? 1 : nchunk);
+    int nsplit = (2 * sms + batch - 1) / batch;
+    if (nsplit > 16) nsplit = 16;
+    if (nsplit < 1) nsplit = 1;
+    pl.nsplit = nsplit;
+    return pl;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+size_t decode_ws_bytes(int batch, int64_t max_ctx, int budget, int sms) {
+    const DecodePlan pl = decode_plan(batch, max_ctx, sms);
+    const int k_sel = budget - 1 > 0 ? budget - 1 : 1;
+    size_t b = 0;
+    b += align256(static_cast<size_t>(batch) * pl.nchunk * k_sel * sizeof(uint2));   // cand
+    b += align256(static_cast<size_t>(batch) * pl.nchunk * sizeof(int32_t));         // cnt
+    b += align256(static_cast<size_t>(batch) * budget * sizeof(int32_t));            // idx
+    b += align256(static_cast<size_t>(batch) * pl.nsplit * kHQ * kD * sizeof(float)); // part_o
+    b += align256(static_cast<size_t>(batch) * pl.nsplit * kHQ * sizeof(float));      // part_lse
+    return b;
+}
+
+cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &plan,
+                                const uint16_t *qi, const uint16_t *w, const uint16_t *kblk,
+                                const int32_t *seq_lens, int budget, void *ws, int32_t *idx_out,
+                                int32_t *status, cudaStream_t stream) {
+    const int k_sel = budget - 1;
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    const int k_alloc = k_sel > 0 ? k_sel : 1;
+    uint2 *cand = reinterpret_cast<uint2 *>(base);
+    base += align256(static_cast<size_t>(batch) * plan.nchunk * k_alloc * sizeof(uint2));
+    int32_t *cnt = reinterpret_cast<int32_t *>(base);
+    cudaError_t e;
+    if (k_sel > 0) {
+        dx::ScanParams sp;
+        sp.qi = qi;
+        sp.w = w;
+        sp.kblk = kblk;
+        sp.seq_lens = seq_lens;
+        sp.max_ctx = max_ctx;
+        sp.chunk = plan.chunk;
+        sp.nchunk = plan.nchunk;
+        sp.k_sel = k_sel;
+        sp.cand = cand;
+        sp.cnt = cnt;
+        sp.status = status;
+        const int smem = static_cast<int>(plan.chunk * 4 + 256 * 4 + 16);
+        e = cudaFuncSetAttribute(dx::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        dim3 grid(plan.nchunk, batch);
+        dx::scan_kernel<<<grid, dx::SCAN_THREADS, smem, stream>>>(sp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    dx::MergeParams mp;
+    mp.seq_lens = seq_lens;
+    mp.max_ctx = max_ctx;
+    mp.nchunk = plan.nchunk;
+    mp.k_sel = k_sel;
+    mp.budget = budget;
+    mp.cand = cand;
+    mp.cnt = cnt;
+    mp.idx = idx_out;
+    mp.status = status;
+    const int smem = dx::MAX_NCHUNK * dx::MAX_SEL * 8 + kMaxBudget * 8 + 256 * 4 + 8 * 4 +
+                     (dx::MAX_NCHUNK + 1) * 4;
+    e = cudaFuncSetAttribute(dx::merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dx::merge_kernel<<<batch, dx::MERGE_THREADS, smem, stream>>>(mp);
+    return cudaGetLastError();
+}
+
+}  // namespace qsa

@@ -1,0 +1,386 @@
+// The extern "C" boundary of libqsa.so: argument validation, workspace
+// carving, TMA tensor maps, and the launch sequence of each entry point.
+// Declarations and their documentation are in include/qsa.h.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "qsa_common.cuh"
+#include "qsa_kernels.h"
+
+namespace {
+
+thread_local std::string g_detail = "no error";
+
+qsa_status fail(qsa_status s, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+qsa_status fail(qsa_status s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_detail = buf;
+    return s;
+}
+
+qsa_status cuda_fail(cudaError_t e, const char *where) {
+    return fail(QSA_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+qsa_status ok() {
+    g_detail = "no error";
+    return QSA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// per-device SM count, cached
+int sm_count() {
+    static std::mutex mu;
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    std::lock_guard<std::mutex> lk(mu);
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            n = 148;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, inner] row-major, 128-byte swizzled boxes of
+// [box_rows, 64] (out-of-range rows read as zero).
+qsa_status make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t rows,
+                    uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {inner * 2};
+    cuuint32_t box[2] = {64, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return QSA_OK;
+}
+
+qsa_status check_cfg(const qsa_config *cfg) {
+    if (!cfg) return fail(QSA_ERR_INVALID_ARG, "cfg is NULL");
+    if (cfg->block_size != qsa::kBlock || cfg->n_q_heads != qsa::kHQ ||
+        cfg->n_kv_heads != qsa::kHKV || cfg->head_dim != qsa::kD || cfg->rope_dim != qsa::kRD ||
+        cfg->n_idx_heads != qsa::kHI || cfg->idx_dim != qsa::kDI)
+        return fail(QSA_ERR_UNSUPPORTED,
+                    "only block 4, 24/2 heads of dim 256, rope dim 64, indexer 4 x 128 are compiled in");
+    if (cfg->budget_blocks < 1) return fail(QSA_ERR_INVALID_ARG, "budget_blocks must be >= 1");
+    if (cfg->budget_blocks > qsa::kMaxBudget)
+        return fail(QSA_ERR_UNSUPPORTED, "budget_blocks > %d", qsa::kMaxBudget);
+    if (!(cfg->rope_theta > 0.0) || !std::isfinite(cfg->rope_theta))
+        return fail(QSA_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
+    if (!std::isfinite(cfg->softmax_scale))
+        return fail(QSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+    return QSA_OK;
+}
+
+qsa::RopeFreqs freqs_of(const qsa_config *cfg) {
+    qsa::RopeFreqs f;
+    for (int i = 0; i < 32; ++i) f.inv_freq[i] = std::pow(cfg->rope_theta, -2.0 * i / qsa::kRD);
+    return f;
+}
+
+float scale_log2_of(const qsa_config *cfg) {
+    const double sc = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0 / std::sqrt(double(qsa::kD));
+    return static_cast<float>(sc * 1.4426950408889634);
+}
+
+#define REQ_PTR(p)                                                                       \
+    do {                                                                                 \
+        if (!(p)) return fail(QSA_ERR_INVALID_ARG, "%s is NULL", #p);                    \
+        if (!aligned16(p)) return fail(QSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p); \
+    } while (0)
+#define OPT_PTR(p)                                                                       \
+    do {                                                                                 \
+        if ((p) && !aligned16(p))                                                        \
+            return fail(QSA_ERR_INVALID_ARG, "%s is not 16-byte aligned", #p);           \
+    } while (0)
+
+constexpr int64_t kMaxL = int64_t(1) << 24;           // tokens per prefill call
+constexpr int64_t kMaxScoresL = 65536;
+constexpr int64_t kMaxDecodeCtx = int64_t(47) * 16384 * 4;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t index_ws(int64_t L) {
+    const size_t kblk = align_up(static_cast<size_t>(L / qsa::kBlock) * qsa::kDI * 2 + 16, 1024);
+    return kblk + qsa::index_cand_bytes(L, sm_count());
+}
+
+}  // namespace
+
+extern "C" {
+
+void qsa_default_config(qsa_config *cfg) {
+    if (!cfg) return;
+    cfg->block_size = qsa::kBlock;
+    cfg->budget_blocks = qsa::kMaxBudget;
+    cfg->n_q_heads = qsa::kHQ;
+    cfg->n_kv_heads = qsa::kHKV;
+    cfg->head_dim = qsa::kD;
+    cfg->rope_dim = qsa::kRD;
+    cfg->n_idx_heads = qsa::kHI;
+    cfg->idx_dim = qsa::kDI;
+    cfg->rope_theta = 1.0e7;
+    cfg->softmax_scale = 1.0f / 16.0f;
+}
+
+const char *qsa_status_string(qsa_status s) {
+    switch (s) {
+        case QSA_OK: return "QSA_OK";
+        case QSA_ERR_INVALID_ARG: return "QSA_ERR_INVALID_ARG";
+        case QSA_ERR_UNSUPPORTED: return "QSA_ERR_UNSUPPORTED";
+        case QSA_ERR_WORKSPACE: return "QSA_ERR_WORKSPACE";
+        case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+        case QSA_ERR_TIMEOUT: return "QSA_ERR_TIMEOUT";
+        case QSA_ERR_DEVICE_CHECK: return "QSA_ERR_DEVICE_CHECK";
+    }
+    return "QSA_ERR_UNKNOWN";
+}
+
+const char *qsa_last_error_detail(void) { return g_detail.c_str(); }
+
+qsa_status qsa_kprep(const qsa_config *cfg, int batch, int64_t L, int64_t max_ctx,
+                     const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot, qsa_bf16 *kblk,
+                     void *stream) {
+    qsa_status st = check_cfg(cfg);
+    if (st != QSA_OK) return st;
+    if (batch < 1) return fail(QSA_ERR_INVALID_ARG, "batch must be >= 1");
+    if (L < 1 || max_ctx < L) return fail(QSA_ERR_INVALID_ARG, "need 1 <= L <= max_ctx");
+    if (max_ctx > (int64_t(1) << 40) / batch) return fail(QSA_ERR_UNSUPPORTED, "too many tokens");
+    REQ_PTR(ki);
+    REQ_PTR(kblk);
+    if ((k == nullptr) != (k_rot == nullptr))
+        return fail(QSA_ERR_INVALID_ARG, "k and k_rot must both be given or both be NULL");
+    OPT_PTR(k);
+    OPT_PTR(k_rot);
+    if (batch > 1 && (max_ctx % qsa::kBlock) != 0 && L / qsa::kBlock > 0)
+        return fail(QSA_ERR_INVALID_ARG, "max_ctx must be a multiple of 4 for batch > 1");
+    cudaError_t e = qsa::launch_kprep(batch, L, max_ctx, ki, k, k_rot, kblk, freqs_of(cfg), sm_count(),
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kprep launch");
+    return ok();
+}
+
+size_t qsa_index_topk_workspace_bytes(const qsa_config *cfg, int64_t L) {
+    if (check_cfg(cfg) != QSA_OK || L < 1 || L > kMaxL) return 0;
+    return index_ws(L);
+}
+
+static qsa_status index_common(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                               const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot, int64_t L,
+                               int32_t *idx, float *score, float *dense, void *ws,
+                               size_t ws_bytes, int32_t *dev_status, void *stream) {
+    qsa_status st = check_cfg(cfg);
+    if (st != QSA_OK) return st;
+    if (L < 1) return fail(QSA_ERR_INVALID_ARG, "L must be >= 1");
+    if (L > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "L > %lld", static_cast<long long>(kMaxL));
+    REQ_PTR(qi);
+    REQ_PTR(w);
+    REQ_PTR(ki);
+    REQ_PTR(dev_status);
+    if ((k == nullptr) != (k_rot == nullptr))
+        return fail(QSA_ERR_INVALID_ARG, "k and k_rot must both be given or both be NULL");
+    OPT_PTR(k);
+    OPT_PTR(k_rot);
+    if (dense) {
+        REQ_PTR(dense);
+    } else {
+        REQ_PTR(idx);
+        OPT_PTR(score);
+    }
+    const size_t need = index_ws(L);
+    if (!ws || ws_bytes < need)
+        return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int sms = sm_count();
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    // TMA needs a 16-byte aligned base; round the block-key region up to 1 KiB
+    uint16_t *kblk = reinterpret_cast<uint16_t *>(align_up(reinterpret_cast<uintptr_t>(wsb), 16));
+    const size_t kblk_bytes = align_up(static_cast<size_t>(L / qsa::kBlock) * qsa::kDI * 2 + 16, 1024);
+    void *cand = wsb + kblk_bytes;
+
+    cudaError_t e = qsa::launch_kprep(1, L, L, ki, k, k_rot, kblk, freqs_of(cfg), sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "kprep launch");
+    if (!dense && cfg->budget_blocks == 1) {
+        e = qsa::launch_fill_current_only(L, 1, idx, score, s);
+        if (e != cudaSuccess) return cuda_fail(e, "selection launch");
+        return ok();
+    }
+    CUtensorMap map_q, map_k;
+    st = make_map(&map_q, qi, qsa::kDI, static_cast<uint64_t>(L) * qsa::kHI, 256);
+    if (st != QSA_OK) return st;
+    const int64_t nbk = L / qsa::kBlock;
+    st = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
+    if (st != QSA_OK) return st;
+    e = qsa::launch_index(map_q, map_k, L, cfg->budget_blocks, w, idx, score, dense, cand,
+                          dev_status, sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+    return ok();
+}
+
+qsa_status qsa_index_topk(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                          const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot, int64_t L,
+                          int32_t *idx, float *score, void *ws, size_t ws_bytes,
+                          int32_t *dev_status, void *stream) {
+    return index_common(cfg, qi, w, ki, k, k_rot, L, idx, score, nullptr, ws, ws_bytes,
+                        dev_status, stream);
+}
+
+qsa_status qsa_index_scores(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                            const qsa_bf16 *ki, int64_t L, float *scores, void *ws,
+                            size_t ws_bytes, int32_t *dev_status, void *stream) {
+    if (L > kMaxScoresL) return fail(QSA_ERR_UNSUPPORTED, "dense scores need L <= %lld",
+                                     static_cast<long long>(kMaxScoresL));
+    if (!scores) return fail(QSA_ERR_INVALID_ARG, "scores is NULL");
+    return index_common(cfg, qi, w, ki, nullptr, nullptr, L, nullptr, nullptr, scores, ws, ws_bytes,
+                        dev_status, stream);
+}
+
+qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
+                                   const qsa_bf16 *k_rot, const qsa_bf16 *v, const int32_t *idx,
+                                   int64_t L, qsa_bf16 *out, float *lse, int32_t *dev_status,
+                                   void *stream) {
+    qsa_status st = check_cfg(cfg);
+    if (st != QSA_OK) return st;
+    if (L < 1) return fail(QSA_ERR_INVALID_ARG, "L must be >= 1");
+    if (L > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "L > %lld", static_cast<long long>(kMaxL));
+    REQ_PTR(q);
+    REQ_PTR(k_rot);
+    REQ_PTR(v);
+    REQ_PTR(idx);
+    REQ_PTR(out);
+    OPT_PTR(lse);
+    REQ_PTR(dev_status);
+    qsa::AttnArgs a{};
+    a.q = q;
+    a.k = k_rot;
+    a.v = v;
+    a.seq_stride = 0;
+    a.idx = idx;
+    a.budget = cfg->budget_blocks;
+    a.seq_lens = nullptr;
+    a.L = L;
+    a.out = out;
+    a.lse = lse;
+    a.nsplit = 1;
+    a.scale_log2 = scale_log2_of(cfg);
+    a.status = dev_status;
+    cudaError_t e = qsa::launch_attn_prefill(a, freqs_of(cfg), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    return ok();
+}
+
+size_t qsa_decode_workspace_bytes(const qsa_config *cfg, int batch, int64_t max_ctx) {
+    if (check_cfg(cfg) != QSA_OK || batch < 1 || max_ctx < 1 || max_ctx > kMaxDecodeCtx) return 0;
+    return qsa::decode_ws_bytes(batch, max_ctx, cfg->budget_blocks, sm_count());
+}
+
+qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf16 *q,
+                                  const qsa_bf16 *qi, const qsa_bf16 *w,
+                                  const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                  const qsa_bf16 *kblk_cache, int64_t max_ctx,
+                                  const int32_t *seq_lens, qsa_bf16 *out, float *lse,
+                                  int32_t *idx_out, void *ws, size_t ws_bytes,
+                                  int32_t *dev_status, void *stream) {
+    qsa_status st = check_cfg(cfg);
+    if (st != QSA_OK) return st;
+    if (batch < 1 || batch > 65535) return fail(QSA_ERR_INVALID_ARG, "need 1 <= batch <= 65535");
+    if (max_ctx < 1) return fail(QSA_ERR_INVALID_ARG, "max_ctx must be >= 1");
+    if (max_ctx > kMaxDecodeCtx)
+        return fail(QSA_ERR_UNSUPPORTED, "max_ctx > %lld", static_cast<long long>(kMaxDecodeCtx));
+    if (max_ctx % qsa::kBlock) return fail(QSA_ERR_INVALID_ARG, "max_ctx must be a multiple of 4");
+    REQ_PTR(q);
+    REQ_PTR(qi);
+    REQ_PTR(w);
+    REQ_PTR(k_cache);
+    REQ_PTR(v_cache);
+    REQ_PTR(kblk_cache);
+    REQ_PTR(seq_lens);
+    REQ_PTR(out);
+    OPT_PTR(lse);
+    OPT_PTR(idx_out);
+    REQ_PTR(dev_status);
+    const int sms = sm_count();
+    const size_t need = qsa::decode_ws_bytes(batch, max_ctx, cfg->budget_blocks, sms);
+    if (!ws || ws_bytes < need)
+        return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const qsa::DecodePlan plan = qsa::decode_plan(batch, max_ctx, sms);
+    const int budget = cfg->budget_blocks;
+    const int k_alloc = budget - 1 > 0 ? budget - 1 : 1;
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    auto take = [&](size_t bytes) {
+        uint8_t *r = p;
+        p += align_up(bytes, 256);
+        return r;
+    };
+    uint8_t *cand_region = take(static_cast<size_t>(batch) * plan.nchunk * k_alloc * 8);
+    take(static_cast<size_t>(batch) * plan.nchunk * 4);
+    int32_t *idx_ws = reinterpret_cast<int32_t *>(take(static_cast<size_t>(batch) * budget * 4));
+    float *part_o = reinterpret_cast<float *>(take(static_cast<size_t>(batch) * plan.nsplit * qsa::kHQ * qsa::kD * 4));
+    float *part_lse = reinterpret_cast<float *>(take(static_cast<size_t>(batch) * plan.nsplit * qsa::kHQ * 4));
+    int32_t *idx = idx_out ? idx_out : idx_ws;
+
+    cudaError_t e = qsa::launch_decode_index(batch, max_ctx, plan, qi, w, kblk_cache, seq_lens,
+                                             budget, cand_region, idx, dev_status, s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode indexer launch");
+    qsa::AttnArgs a{};
+    a.q = q;
+    a.k = k_cache;
+    a.v = v_cache;
+    a.seq_stride = max_ctx;
+    a.idx = idx;
+    a.budget = budget;
+    a.seq_lens = seq_lens;
+    a.L = 0;
+    a.out = out;
+    a.lse = lse;
+    a.part_o = part_o;
+    a.part_lse = part_lse;
+    a.nsplit = plan.nsplit;
+    a.scale_log2 = scale_log2_of(cfg);
+    a.status = dev_status;
+    e = qsa::launch_attn_decode(a, batch, freqs_of(cfg), s);
+    if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
+    if (plan.nsplit > 1) {
+        e = qsa::launch_attn_combine(part_o, part_lse, batch, plan.nsplit, out, lse, s);
+        if (e != cudaSuccess) return cuda_fail(e, "decode combine launch");
+    }
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Host-side launchers of the QSA kernels (internal to libqsa.so).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda.h>
+#include <stdint.h>
+
+namespace qsa {
+
+// inv_freq[i] = theta^(-2i/64), computed on the host in double.
+struct RopeFreqs {
+    double inv_freq[32];
+};
+
+cudaError_t launch_kprep(int batch, int64_t L, int64_t max_ctx, const uint16_t *ki,
+                         const uint16_t *k, uint16_t *k_rot, uint16_t *kblk,
+                         const RopeFreqs &freqs, int sms, cudaStream_t stream);
+
+// ---- prefill indexer + selection (tcgen05) ----
+int index_grid(int64_t L, int sms);
+size_t index_cand_bytes(int64_t L, int sms);
+cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t L,
+                         int budget, const uint16_t *w, int32_t *idx, float *score,
+                         float *dense, void *cand_ws, int32_t *status, int sms,
+                         cudaStream_t stream);
+cudaError_t launch_fill_current_only(int64_t L, int budget, int32_t *idx, float *score,
+                                     cudaStream_t stream);
+
+// ---- block-sparse attention (prefill and decode splits) ----
+struct AttnArgs {
+    const uint16_t *q;       // [items, 24, 256] pre-RoPE
+    const uint16_t *k;       // key rows (post-RoPE), sequence s starts at s * seq_stride rows
+    const uint16_t *v;
+    int64_t seq_stride;      // rows between sequences (decode: max_ctx; prefill: 0)
+    const int32_t *idx;      // [items, budget]
+    int budget;
+    const int32_t *seq_lens; // decode: [B] device; prefill: null
+    int64_t L;               // prefill length (prefill only)
+    uint16_t *out;           // final output (nsplit == 1)
+    float *lse;              // final lse or null
+    float *part_o;           // [B, nsplit, 24, 256] (nsplit > 1)
+    float *part_lse;         // [B, nsplit, 24]
+    int nsplit;
+    float scale_log2;        // softmax scale * log2(e)
+    int32_t *status;
+};
+cudaError_t launch_attn_prefill(const AttnArgs &a, const RopeFreqs &f, cudaStream_t stream);
+cudaError_t launch_attn_decode(const AttnArgs &a, int batch, const RopeFreqs &f,
+                               cudaStream_t stream);
+cudaError_t launch_attn_combine(const float *part_o, const float *part_lse, int batch,
+                                int nsplit, uint16_t *out, float *lse, cudaStream_t stream);
+
+// ---- decode indexer ----
+struct DecodePlan {
+    int64_t chunk;    // blocks per scan CTA
+    int nchunk;       // scan CTAs per sequence
+    int nsplit;       // attention splits per sequence
+};
+DecodePlan decode_plan(int batch, int64_t max_ctx, int sms);
+size_t decode_ws_bytes(int batch, int64_t max_ctx, int budget, int sms);
+cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &plan,
+                                const uint16_t *qi, const uint16_t *w, const uint16_t *kblk,
+                                const int32_t *seq_lens, int budget, void *ws, int32_t *idx_out,
+                                int32_t *status, cudaStream_t stream);
+
+}  // namespace qsa

