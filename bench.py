@@ -1,0 +1,454 @@
+"""Benchmark of the QSA hot path on one B300 (or N replicas under torchrun).
+
+One step = one pass of the whole QSA layer over one batch of synthetic input:
+  prefill of L tokens (K-prep, tensor-core indexer + exact top-k selection,
+  block-sparse attention) followed by one decode step for B sequences of T
+  cached tokens (block-key scan + selection, split attention, combine).
+Default workload: L = 1,048,576 (budget 512 blocks) and decode 8 x 1,048,576.
+
+Prints ONE JSON line.  `value` = tokens processed per second of device time
+(prefill tokens + decode tokens), inputs resident in HBM; `e2e` = the same
+through the C ABI with the step's inputs copied from pinned host memory and
+the attention output copied back, inside the timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle on the same workload
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from block_sparse_long_19_b300 import qsa as Q  # noqa: E402
+from block_sparse_long_19_b300 import workloads as W  # noqa: E402
+
+METRIC = "QSA prefill tokens/s and decode µs/token at 128K–1M ctx; % of roofline"
+WORKLOADS = {
+    # name: (prefill L, budget, prefill seed, decode batch, decode ctx, decode seed)
+    "qsa_1m": (1 << 20, 512, 4, 8, 1 << 20, 4),
+    "qsa_128k": (131072, 512, 2, 64, 262144, 3),
+    "qsa_small": (32768, 512, 1, 4, 65536, 5),
+    # profiling case: K/V (268 MB) larger than L2, a few GB on the device
+    "prof_128k": (131072, 512, 2, 1, 65536, 3),
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        smax = [num(r[2]) for r in rows if num(r[2]) is not None]
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- workload --
+
+class Workload:
+    def __init__(self, name: str, dev: str):
+        L, budget, pseed, B, T, dseed = WORKLOADS[name]
+        self.name, self.L, self.budget, self.B, self.T = name, L, budget, B, T
+        self.dev = dev
+        self.cfg = Q.default_config(budget=budget)
+        log(f"[bench] generating {name}: prefill L={L}, decode {B}x{T}")
+        self.p = W.prefill_inputs(L, pseed, dev)
+        d = W.decode_inputs(B, T, dseed, dev)
+        # fill the decode caches once (RoPE'd keys in place, block keys); this
+        # is cache state, not part of a step
+        self.kblk_cache, _ = Q.kprep(self.cfg, d["ki"], d["k"], k_rot=d["k"])
+        del d["ki"]
+        self.d = d
+        torch.cuda.synchronize()
+        # outputs and workspaces, allocated once
+        self.ws_pre = torch.empty(Q.index_topk_workspace_bytes(self.cfg, L), dtype=torch.uint8, device=dev)
+        self.ws_dec = torch.empty(Q.decode_workspace_bytes(self.cfg, B, T), dtype=torch.uint8, device=dev)
+        self.idx = torch.empty((L, budget), dtype=torch.int32, device=dev)
+        self.k_rot = torch.empty_like(self.p["k"])
+        self.out = torch.empty((L, 24, 256), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((L, 24), dtype=torch.float32, device=dev)
+        self.dout = torch.empty((B, 24, 256), dtype=torch.bfloat16, device=dev)
+        self.dlse = torch.empty((B, 24), dtype=torch.float32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.ev = None
+
+    def step(self, events=None):
+        """One pass of the hot path.  events: optional list of 5 CUDA events
+        recorded at: start, after indexer, after attention, after decode."""
+        cfg, p, d = self.cfg, self.p, self.d
+        if events:
+            events[0].record()
+        Q.index_topk(cfg, p["qi"], p["w"], p["ki"], k=p["k"], k_rot=self.k_rot, idx=self.idx,
+                     score=None, ws=self.ws_pre, status=self.status, want_score=False)
+        if events:
+            events[1].record()
+        Q.sparse_attn_prefill(cfg, p["q"], self.k_rot, p["v"], self.idx, out=self.out, lse=self.lse,
+                              status=self.status)
+        if events:
+            events[2].record()
+        Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], d["k"], d["v"], self.kblk_cache,
+                             d["seq_lens"], out=self.dout, lse=self.dlse, idx_out=None,
+                             ws=self.ws_dec, status=self.status, want_idx=False)
+        if events:
+            events[3].record()
+
+    def launches_per_step(self) -> int:
+        plan_split = 1  # combine kernel launched when the decode splits > 1
+        n = 2 + 1 + 1   # kprep blocks + kprep rope, indexer, attention
+        n += 2 + 1 + plan_split  # decode scan + merge, attention, combine
+        return n
+
+    def attn_bytes(self) -> int:
+        """Algorithmic bytes of one prefill attention launch: per query the
+        gathered K and V rows of both KV heads (2048 B per attended key), the
+        query and output rows (2 x 12288 B), the index row and the LSE row."""
+        L, B = self.L, self.budget
+        t = np.arange(L, dtype=np.int64)
+        c = t // 4
+        past = np.minimum(c, B - 1)
+        keys = past * 4 + (t % 4) + 1
+        return int((keys * 2048).sum() + L * (2 * 24 * 256 * 2 + B * 4 + 24 * 4))
+
+    def index_flops(self) -> float:
+        """Algorithmic flops of the indexer: 2 * 4 heads * 128 per (query, past block)."""
+        t = np.arange(self.L, dtype=np.int64)
+        return float((t // 4).sum() * 1024)
+
+    def decode_bytes(self) -> int:
+        """Algorithmic bytes of one decode step: the block-key scan
+        (256 B per past block) plus 2048 B per attended key, per sequence."""
+        c = (self.T - 1) // 4
+        keys = min(c, self.budget - 1) * 4 + ((self.T - 1) % 4) + 1
+        return self.B * (c * 256 + keys * 2048 + 2 * 24 * 256 * 2)
+
+
+# ----------------------------------------------------------------- e2e --
+
+def run_e2e(wl: Workload, steps: int) -> dict:
+    """Step through the public API from pinned host buffers: H2D of every
+    prefill input and of the decode query inputs, compute, D2H of both
+    attention outputs; all inside the timed region."""
+    p, d = wl.p, wl.d
+    names = ["q", "k", "v", "qi", "w", "ki"]
+    host = {n: torch.empty(p[n].shape, dtype=p[n].dtype, pin_memory=True) for n in names}
+    for n in names:
+        host[n].copy_(p[n])
+        host[n] = host[n]
+    dn = ["q", "qi", "w", "seq_lens"]
+    dhost = {n: torch.empty(d[n].shape, dtype=d[n].dtype, pin_memory=True) for n in dn}
+    for n in dn:
+        dhost[n].copy_(d[n])
+    out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+    dout_h = torch.empty(wl.dout.shape, dtype=wl.dout.dtype, pin_memory=True)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names) + \
+        sum(dhost[n].numel() * dhost[n].element_size() for n in dn)
+    d2h = out_h.numel() * out_h.element_size() + dout_h.numel() * dout_h.element_size()
+
+    def one():
+        for n in names:
+            p[n].copy_(host[n], non_blocking=True)
+        for n in dn:
+            d[n].copy_(dhost[n], non_blocking=True)
+        wl.step()
+        out_h.copy_(wl.out, non_blocking=True)
+        dout_h.copy_(wl.dout, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    del host, dhost, out_h, dout_h
+    return {"value": (wl.L + wl.B) / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+# ---------------------------------------------------------- CPU baseline --
+
+def oracle_sample(wl_name: str, target_s: float = 12.0, host_inputs=None) -> dict:
+    """The oracle as it stands, on the host cores, on a bounded sample of the
+    workload's prefill query rows (all steps of the layer per row)."""
+    import oracle as O
+
+    L, budget, pseed, B, T, dseed = WORKLOADS[wl_name]
+    if host_inputs is None:
+        t = W.prefill_inputs(L, pseed, "cuda" if torch.cuda.is_available() else "cpu")
+    else:
+        t = host_inputs
+    rng = np.random.default_rng(12345)
+    # rows from the part of the sequence where the budget binds (c >= 511)
+    lo = min(2048, L - 1)
+    pool = rng.permutation(np.arange(lo, L))
+    hb = {}
+    for n in ("k", "v", "ki"):
+        hb[n] = W.to_bits(t[n])
+    hb["q"] = np.zeros((L, 24, 256), np.uint16)   # only sampled rows are filled
+    hb["qi"] = np.zeros((L, 4, 128), np.uint16)
+    hb["w"] = W.to_bits(t["w"])
+
+    def fill(rows):
+        ri = torch.as_tensor(rows, device=t["q"].device)
+        hb["q"][rows] = W.to_bits(t["q"][ri])
+        hb["qi"][rows] = W.to_bits(t["qi"][ri])
+
+    cores = O.max_threads()
+    n0 = max(2, cores)
+    rows0 = np.sort(pool[:n0])
+    fill(rows0)
+    t0 = time.perf_counter()
+    O.prefill_rows(hb, rows0, budget)
+    dt0 = time.perf_counter() - t0
+    n1 = int(max(n0, min(len(pool), n0 * max(1.0, target_s / max(dt0, 1e-3)))))
+    rows1 = np.sort(pool[n0:n0 + n1]) if n0 + n1 <= len(pool) else np.sort(pool[:n1])
+    fill(rows1)
+    t1 = time.perf_counter()
+    O.prefill_rows(hb, rows1, budget)
+    dt1 = time.perf_counter() - t1
+    return {"value": len(rows1) / dt1, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"{len(rows1)} uniformly drawn query rows (positions >= {lo}) of the "
+                      f"L={L} prefill, full layer per row (scores over every past block, "
+                      f"selection, RoPE, attention), fp64, {dt1:.1f} s"}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed as it stands on this host."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl_name = args.workload
+    L = WORKLOADS[wl_name][0]
+    import oracle as O
+
+    cores = O.max_threads()
+    # each step: a bounded sample sized so the whole run ends within minutes
+    budget_s = 150.0 / max(1, args.steps + args.warmup)
+    vals = []
+    res = None
+    t = W.prefill_inputs(L, WORKLOADS[wl_name][2], "cuda" if torch.cuda.is_available() else "cpu")
+    for i in range(args.warmup + args.steps):
+        res = oracle_sample(wl_name, target_s=min(budget_s, 12.0), host_inputs=t)
+        if i >= args.warmup:
+            vals.append(res["value"])
+    v = statistics.median(vals)
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / v if v else None,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl_name, "L": L},
+        "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": res["sample"] if res else ""},
+        "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------ main --
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qsa_1m", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.warmup < 3:
+        log("[bench] raising warmup to 3")
+        args.warmup = 3
+    torch.cuda.set_device(local)
+    dev = f"cuda:{local}"
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+        pg = dist
+
+    Q.load()
+    wl = Workload(args.workload, dev)
+    peaks = {}
+    pk_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(pk_path):
+        peaks = json.load(open(pk_path))
+
+    for _ in range(args.warmup):
+        wl.step()
+    torch.cuda.synchronize()
+    Q.check_status(wl.status, "warm-up")
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    e_start.record()
+    for i in range(K):
+        wl.step(evs[i])
+    e_end.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if pg:
+        pg.barrier()
+    Q.check_status(wl.status, "timed steps")
+    ms = e_start.elapsed_time(e_end) / K
+    idx_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(K))
+    attn_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(K))
+    dec_ms = statistics.mean(evs[i][2].elapsed_time(evs[i][3]) for i in range(K))
+    if pg:
+        t = torch.tensor([ms], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+
+    tokens = (wl.L + wl.B) * world
+    value = tokens / (ms / 1e3)
+
+    hbm = peaks.get("hbm_gbs")
+    tc = peaks.get("bf16_tflops")
+    peak_src = "measured" if hbm else "fallback"
+    hbm = hbm or 6400.0
+    tc = tc or 1800.0
+    attn_bytes = wl.attn_bytes()
+    attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9
+    idx_tflops = wl.index_flops() / (idx_ms / 1e3) / 1e12
+    dec_gbs = wl.decode_bytes() / (dec_ms / 1e3) / 1e9
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", "attn_prefill_traffic.json")
+    if os.path.exists(prof):
+        try:
+            pj = json.load(open(prof))
+            if pj.get("L") and pj.get("bytes_per_query"):
+                traffic = int(pj["bytes_per_query"] * wl.L)
+        except Exception:
+            traffic = None
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "prefill_L": wl.L, "budget_blocks": wl.budget,
+                   "decode_batch": wl.B, "decode_ctx": wl.T,
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "prefill_tokens_per_s": wl.L / ((idx_ms + attn_ms) / 1e3),
+        "decode_us_per_token": dec_ms * 1e3,
+        "decode_us_per_step": dec_ms * 1e3,
+        "stage_ms": {"indexer_topk": idx_ms, "sparse_attn_prefill": attn_ms, "decode_step": dec_ms},
+        "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": attn_gbs / hbm, "traffic": traffic,
+                     "kernel": "sparse_attn_prefill", "peak_source": peak_src + " hbm_gbs",
+                     "bytes_per_launch": attn_bytes},
+        "stage_roofline": {
+            "indexer_topk": {"bound": "tensor", "achieved": idx_tflops, "peak": tc, "unit": "TFLOP/s",
+                             "frac": idx_tflops / tc, "peak_source": peak_src + " bf16_tflops"},
+            "decode_step": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
+                            "frac": dec_gbs / hbm},
+        },
+        "gpu_launches": wl.launches_per_step() * K,
+        "clocks": clk,
+    }
+    if not args.no_e2e:
+        try:
+            line["e2e"] = run_e2e(wl, max(1, min(K, 3)))
+            line["e2e"]["value"] = line["e2e"]["value"] * world
+        except Exception as ex:  # report, never fake
+            line["e2e"] = {"value": None, "unit": "tokens/s", "error": str(ex)[:200]}
+    if rank == 0 and not args.no_cpu_baseline:
+        try:
+            line["cpu_baseline"] = oracle_sample(args.workload, host_inputs=wl.p)
+        except Exception as ex:
+            line["cpu_baseline"] = {"value": None, "error": str(ex)[:200]}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -37,6 +37,22 @@ def oracle_compare_prefill(t, hb, res, rows, budget, check_attn=True):
 
 # ------------------------------------------------------------------ K-prep --
 
+def check_rope(got_bits, ref_bits, x_bits):
+    """RoPE'd keys: the GPU rotates in fp32 (angle reduced in fp64), the
+    oracle in fp64, both then round to bf16.  Allowed: one bf16 ulp of the
+    result (2^-7 relative) plus the fp32 rounding error of the rotation, which
+    dominates when x1 cos a and x2 sin a nearly cancel."""
+    g = \
+        torch.from_numpy(got_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
+    r = torch.from_numpy(ref_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
+    x = torch.from_numpy(x_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
+    mag = np.abs(x[..., :32]) + np.abs(x[..., 32:])
+    mag = np.concatenate([mag, mag], axis=-1)
+    bound = 2.0 ** -7 * np.abs(r) + 2.0 ** -20 * mag
+    assert np.all(np.abs(g - r) <= bound), float(np.max(np.abs(g - r) - bound))
+    assert np.mean(got_bits[..., :64] != ref_bits[..., :64]) < 1e-3
+
+
 @pytest.mark.parametrize("L", [5, 1003, 4096])
 def test_kprep_block_keys_bit_exact_and_rope(L):
     t = W.prefill_inputs(L, 21, DEV)
@@ -48,10 +64,7 @@ def test_kprep_block_keys_bit_exact_and_rope(L):
     ref = O.rope_keys(hb["k"])
     got = W.to_bits(k_rot)
     assert np.array_equal(got[:, :, 64:], hb["k"][:, :, 64:])
-    diff = np.abs(got[:, :, :64].astype(np.int32) - ref[:, :, :64].astype(np.int32))
-    # fp32 rotation vs fp64 may land on the other side of a bf16 rounding boundary
-    assert diff.max() <= 1
-    assert (diff != 0).mean() < 1e-3
+    check_rope(got, ref, hb["k"])
 
 
 def test_kprep_batched_in_place():
@@ -63,8 +76,7 @@ def test_kprep_batched_in_place():
     torch.cuda.synchronize()
     for s in range(B):
         assert np.array_equal(W.to_bits(kblk[s]), O.block_keys(hd["ki"][s]))
-        diff = np.abs(W.to_bits(k_rot[s]).astype(np.int32) - O.rope_keys(hd["k"][s]).astype(np.int32))
-        assert diff.max() <= 1
+        check_rope(W.to_bits(k_rot[s]), O.rope_keys(hd["k"][s]), hd["k"][s])
 
 
 # ------------------------------------------------------------ block scores --
