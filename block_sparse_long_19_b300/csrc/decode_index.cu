@@ -18,6 +18,7 @@
 //     block.
 #include "qsa_common.cuh"
 #include "qsa_kernels.h"
+#include "qsa_select.cuh"
 
 namespace qsa {
 namespace dx {
@@ -28,67 +29,140 @@ constexpr int MAX_NCHUNK = 47;
 constexpr int MERGE_THREADS = 1024;
 constexpr int MAX_SEL = kMaxBudget - 1;
 
-__device__ __forceinline__ unsigned long long composite(float s, uint32_t b) {
-    return (static_cast<unsigned long long>(f2key(s)) << 32) |
-           static_cast<unsigned long long>(0xFFFFFFFFu - b);
-}
-
-// CTA-wide exact selection over n items given by get(i) -> composite.
-// Returns T with exactly k items >= T.  hist: 256 uint32 in smem;
-// ctl: 4 ints in smem.  All threads must call.
-template <int NT, typename Get>
-__device__ unsigned long long cta_kth(int n, int k, Get get, uint32_t *hist, int *ctl) {
-    unsigned long long prefix = 0;
-    int krem = k;
-    const int tid = threadIdx.x;
-    for (int pass = 0; pass < 8; ++pass) {
-        const int shift = 56 - 8 * pass;
-        for (int i = tid; i < 256; i += NT) hist[i] = 0;
+// CTA-wide radix step over n items: value(i) -> uint32, pred(i) -> bool.
+// Finds a bucket [thr, thr + 2^lo) holding the k-th largest value, looking
+// only at the bits below the prefix every valid value shares (candidate
+// scores agree on their top bits).  Same contract as the warp version in
+// qsa_select.cuh.  ctl: 8 ints of shared memory; all threads must call.
+template <int NT, typename Val, typename Pred>
+__device__ RadixOut cta_radix(int n, int k, Val value, Pred pred, uint32_t *hist, int *ctl) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+    int nv = 0;
+    for (int i = tid; i < n; i += NT)
+        if (pred(i)) {
+            const uint32_t v = value(i);
+            mx = max(mx, v);
+            mn = min(mn, v);
+            ++nv;
+        }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+    nv = __reduce_add_sync(0xFFFFFFFFu, nv);
+    if (tid < 3) ctl[tid] = tid == 1 ? static_cast<int>(0xFFFFFFFFu) : 0;
+    __syncthreads();
+    if (lane == 0) {
+        atomicMax(reinterpret_cast<unsigned *>(&ctl[0]), mx);
+        atomicMin(reinterpret_cast<unsigned *>(&ctl[1]), mn);
+        atomicAdd(&ctl[2], nv);
+    }
+    __syncthreads();
+    mx = static_cast<uint32_t>(ctl[0]);
+    mn = static_cast<uint32_t>(ctl[1]);
+    nv = ctl[2];
+    (void)warp;
+    RadixOut r;
+    r.krem = k;
+    __syncthreads();
+    if (mx == mn) {
+        r.thr = mx;
+        r.eq = nv;
+        r.lo = 0;
+        return r;
+    }
+    const int hi = 32 - __clz(mx ^ mn);
+    unsigned long long prefix = hi >= 32 ? 0ull : (static_cast<unsigned long long>(mx >> hi) << hi);
+    int lo = hi;
+    int eq = nv;
+    while (lo > 0) {
+        const int w = lo >= 8 ? 8 : lo;
+        lo -= w;
+        const uint32_t dmask = (1u << w) - 1u;
+        for (int i = tid; i < 256; i += NT) hist[i] = 0u;
         __syncthreads();
+        const unsigned long long want = prefix >> (lo + w);
         for (int i = tid; i < n; i += NT) {
-            const unsigned long long C = get(i);
-            const bool match = (pass == 0) || ((C >> (shift + 8)) == (prefix >> (shift + 8)));
-            if (match) atomicAdd(&hist[(C >> shift) & 255], 1u);
+            if (!pred(i)) continue;
+            const uint32_t v = value(i);
+            if ((static_cast<unsigned long long>(v) >> (lo + w)) == want)
+                atomicAdd(&hist[(v >> lo) & dmask], 1u);
         }
         __syncthreads();
         if (tid < 32) {
-            const int lane = tid;
             uint32_t cnt[8];
             uint32_t sum = 0;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                cnt[i] = hist[255 - (lane * 8 + i)];
-                sum += cnt[i];
+            for (int b = 0; b < 8; ++b) {
+                cnt[b] = hist[255 - (lane * 8 + b)];
+                sum += cnt[b];
             }
             uint32_t incl = sum;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += v;
+                const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += t;
             }
             const uint32_t excl = incl - sum;
-            if (excl < static_cast<uint32_t>(krem) && static_cast<uint32_t>(krem) <= incl) {
+            if (excl < static_cast<uint32_t>(r.krem) && static_cast<uint32_t>(r.krem) <= incl) {
                 uint32_t acc = excl;
-                for (int i = 0; i < 8; ++i) {
-                    if (acc + cnt[i] >= static_cast<uint32_t>(krem)) {
-                        ctl[0] = 255 - (lane * 8 + i);
-                        ctl[1] = static_cast<int>(acc);
-                        ctl[2] = static_cast<int>(cnt[i]);
+                for (int b = 0; b < 8; ++b) {
+                    if (acc + cnt[b] >= static_cast<uint32_t>(r.krem)) {
+                        ctl[4] = 255 - (lane * 8 + b);
+                        ctl[5] = static_cast<int>(acc);
+                        ctl[6] = static_cast<int>(cnt[b]);
                         break;
                     }
-                    acc += cnt[i];
+                    acc += cnt[b];
                 }
             }
         }
         __syncthreads();
-        const int digit = ctl[0];
-        krem -= ctl[1];
-        const int eq = ctl[2];
-        prefix |= static_cast<unsigned long long>(digit) << shift;
+        const int digit = ctl[4];
+        r.krem -= ctl[5];
+        eq = ctl[6];
+        prefix |= static_cast<unsigned long long>(digit) << lo;
         __syncthreads();
-        if (eq == krem) break;
+        if (eq == r.krem) break;
     }
-    return prefix;
+    r.thr = static_cast<uint32_t>(prefix);
+    r.eq = eq;
+    r.lo = lo;
+    return r;
+}
+
+// Exact selection of the k best (score desc, block asc) among n items
+// given as score(i) (float) and block(i).  Returns the rule: item i is
+// selected iff key > t.thr_key, or key == thr_key and ~block >= t.thr_blk
+// (thr_blk = 0 selects every item of the bucket when it is exact).
+struct SelectRule {
+    uint32_t thr_key;
+    uint32_t thr_nblk;
+    int exact_bucket;  // 1: select key >= thr_key
+};
+template <int NT, typename Score, typename Block>
+__device__ SelectRule cta_select(int n, int k, Score score, Block block, uint32_t *hist, int *ctl) {
+    auto kv = [&](int i) { return f2key(score(i)); };
+    auto all = [&](int) { return true; };
+    const RadixOut r = cta_radix<NT>(n, k, kv, all, hist, ctl);
+    SelectRule rule;
+    rule.thr_key = r.thr;
+    if (r.eq == r.krem) {
+        rule.exact_bucket = 1;
+        rule.thr_nblk = 0;
+        return rule;
+    }
+    auto nb = [&](int i) { return ~block(i); };
+    auto tie = [&](int i) { return kv(i) == r.thr; };
+    const RadixOut r2 = cta_radix<NT>(n, r.krem, nb, tie, hist, ctl);
+    rule.exact_bucket = 0;
+    rule.thr_nblk = r2.thr;
+    return rule;
+}
+
+__device__ __forceinline__ bool selected(const SelectRule &r, float s, uint32_t b) {
+    const uint32_t key = f2key(s);
+    if (r.exact_bucket) return key >= r.thr_key;
+    return key > r.thr_key || (key == r.thr_key && ~b >= r.thr_nblk);
 }
 
 struct ScanParams {
@@ -108,7 +182,7 @@ struct ScanParams {
 __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     float *sc = reinterpret_cast<float *>(smem);
-    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.chunk * 4);  // dynamic size: chunk*4 + 256*4 + 16
+    uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.chunk * 4);  // dynamic size: chunk*4 + 256*4 + 32
     int *ctl = reinterpret_cast<int *>(hist + 256);
 
     const int s = blockIdx.y;
@@ -183,12 +257,13 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
         if (threadIdx.x == 0) *cnt_out = n;
         return;
     }
-    auto get = [&](int i) { return composite(sc[i], static_cast<uint32_t>(b0 + i)); };
-    const unsigned long long T_ = cta_kth<SCAN_THREADS>(n, p.k_sel, get, hist, ctl);
+    const SelectRule rule = cta_select<SCAN_THREADS>(
+        n, p.k_sel, [&](int i) { return sc[i]; },
+        [&](int i) { return static_cast<uint32_t>(b0 + i); }, hist, ctl);
     if (threadIdx.x == 0) ctl[3] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += SCAN_THREADS) {
-        if (get(i) >= T_) {
+        if (selected(rule, sc[i], static_cast<uint32_t>(b0 + i))) {
             const int pos = atomicAdd(&ctl[3], 1);
             if (pos < p.k_sel)
                 out[pos] = make_uint2(__float_as_uint(sc[i]), static_cast<uint32_t>(b0 + i));
@@ -220,7 +295,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
     unsigned long long *sortb = reinterpret_cast<unsigned long long *>(items + cap);
     uint32_t *hist = reinterpret_cast<uint32_t *>(sortb + kMaxBudget);
     int *ctl = reinterpret_cast<int *>(hist + 256);
-    int *offs = ctl + 8;  // [MAX_NCHUNK + 1]
+    int *offs = ctl + 8;  // [MAX_NCHUNK + 1]; ctl uses 8 ints
 
     const int s = blockIdx.x;
     const int64_t T = p.seq_lens[s];
@@ -248,16 +323,17 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
     }
     __syncthreads();
     int m = n;
-    unsigned long long T_ = 0;
-    auto get = [&](int i) { return composite(__uint_as_float(items[i].x), items[i].y); };
+    SelectRule rule{0u, 0u, 1};
     if (n > p.k_sel) {
-        T_ = cta_kth<MERGE_THREADS>(n, p.k_sel, get, hist, ctl);
+        rule = cta_select<MERGE_THREADS>(
+            n, p.k_sel, [&](int i) { return __uint_as_float(items[i].x); },
+            [&](int i) { return items[i].y; }, hist, ctl);
         m = p.k_sel;
     }
     if (threadIdx.x == 0) ctl[3] = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < n; i += MERGE_THREADS) {
-        if (n <= p.k_sel || get(i) >= T_) {
+        if (n <= p.k_sel || selected(rule, __uint_as_float(items[i].x), items[i].y)) {
             const int pos = atomicAdd(&ctl[3], 1);
             if (pos < kMaxBudget) sortb[pos] = (static_cast<unsigned long long>(items[i].y) << 32) | items[i].x;
         }
@@ -354,7 +430,7 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
         sp.cand = cand;
         sp.cnt = cnt;
         sp.status = status;
-        const int smem = static_cast<int>(plan.chunk * 4 + 256 * 4 + 16);
+        const int smem = static_cast<int>(plan.chunk * 4 + 256 * 4 + 32);
         e = cudaFuncSetAttribute(dx::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
         dim3 grid(plan.nchunk, batch);

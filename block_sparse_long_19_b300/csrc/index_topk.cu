@@ -29,6 +29,7 @@
 //     them by block index and writes the row.
 #include "qsa_common.cuh"
 #include "qsa_kernels.h"
+#include "qsa_select.cuh"
 
 namespace qsa {
 namespace ix {
@@ -37,7 +38,7 @@ constexpr int TQ = 64;               // query tokens per tile
 constexpr int NCOL = TQ * kHI;       // 256 MMA columns (token-major, head-minor)
 constexpr int TB = 128;              // block keys per block tile (MMA M)
 constexpr int NSTAGE = 3;            // kblk tile ring
-constexpr int CAP = 2048;            // candidate slots per token
+constexpr int CAP = 1024;            // candidate slots per token (32 per lane)
 constexpr int KSTEPS = kDI / 16;     // 8 MMAs of K = 16
 constexpr int NEPI = 8;              // epilogue warps
 constexpr int THREADS = (4 + NEPI) * 32;
@@ -84,91 +85,43 @@ __device__ __forceinline__ int num_btiles(int64_t L, int q) {
     return static_cast<int>((cmax + TB - 1) / TB);
 }
 
-__device__ __forceinline__ unsigned long long composite(uint2 it) {
-    // larger = better: score descending, then block index ascending
-    return (static_cast<unsigned long long>(f2key(__uint_as_float(it.x))) << 32) |
-           static_cast<unsigned long long>(0xFFFFFFFFu - it.y);
-}
+// Candidate lists hold (score bits, block); loaded into registers as
+// (order-preserving key, block), item i of a lane = list entry i*32 + lane.
+constexpr int NI = CAP / 32;
+constexpr int KEEP_MAX = CAP - 2 * TB;  // a lower-bound compaction must keep at most this many
 
-// Warp-wide exact selection: returns T such that exactly k of the n items
-// have composite >= T (1 <= k <= n).  hist: 256 ints of this warp.
-__device__ unsigned long long warp_kth(const uint2 *items, int n, int k, uint32_t *hist,
-                                       int lane) {
-    unsigned long long prefix = 0;
-    int krem = k;
-    for (int pass = 0; pass < 8; ++pass) {
-        const int shift = 56 - 8 * pass;
+__device__ __forceinline__ uint32_t load_items(const uint2 *src, int n, uint32_t (&key)[NI],
+                                               uint32_t (&blk)[NI], int lane) {
+    uint32_t vm = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0;
-        __syncwarp();
-        for (int i = lane; i < n; i += 32) {
-            const unsigned long long C = composite(items[i]);
-            const bool match = (pass == 0) || ((C >> (shift + 8)) == (prefix >> (shift + 8)));
-            if (match) atomicAdd(&hist[(C >> shift) & 255], 1u);
+    for (int i = 0; i < NI; ++i) {
+        const int j = i * 32 + lane;
+        uint2 it = make_uint2(0u, 0u);
+        if (j < n) {
+            it = src[j];
+            vm |= 1u << i;
         }
-        __syncwarp();
-        // lane l owns digits 255-8l .. 248-8l (descending)
-        uint32_t cnt[8];
-        uint32_t sum = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            cnt[i] = hist[255 - (lane * 8 + i)];
-            sum += cnt[i];
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        const uint32_t excl = incl - sum;
-        const bool mine = excl < static_cast<uint32_t>(krem) && static_cast<uint32_t>(krem) <= incl;
-        int digit = 0;
-        uint32_t above = 0, eq = 0;
-        if (mine) {
-            uint32_t acc = excl;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                if (acc + cnt[i] >= static_cast<uint32_t>(krem)) {
-                    digit = 255 - (lane * 8 + i);
-                    above = acc;
-                    eq = cnt[i];
-                    break;
-                }
-                acc += cnt[i];
-            }
-        }
-        const unsigned ball = __ballot_sync(0xFFFFFFFFu, mine);
-        const int src = __ffs(ball) - 1;
-        digit = __shfl_sync(0xFFFFFFFFu, digit, src);
-        above = __shfl_sync(0xFFFFFFFFu, above, src);
-        eq = __shfl_sync(0xFFFFFFFFu, eq, src);
-        krem -= static_cast<int>(above);
-        prefix |= static_cast<unsigned long long>(digit) << shift;
-        __syncwarp();
-        if (eq == static_cast<uint32_t>(krem)) break;  // every item with this prefix is in
+        key[i] = f2key(__uint_as_float(it.x));
+        blk[i] = it.y;
     }
-    return prefix;
+    return vm;
 }
 
-// Keep exactly the k best of the n items (in place, order not kept).
-__device__ void warp_compact(uint2 *items, int n, int k, unsigned long long T, int lane) {
+// Write the items whose bit is set in `sel` to the front of the list (all
+// reads happened in load_items, so overwriting in place is safe).
+__device__ __forceinline__ int store_items(uint2 *dst, const uint32_t (&key)[NI],
+                                           const uint32_t (&blk)[NI], uint32_t sel, int lane) {
     int out = 0;
-    for (int base = 0; base < n; base += 32) {
-        const int i = base + lane;
-        uint2 it = make_uint2(0, 0);
-        bool keep = false;
-        if (i < n) {
-            it = items[i];
-            keep = composite(it) >= T;
-        }
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+        const bool keep = (sel >> i) & 1u;
         const unsigned ball = __ballot_sync(0xFFFFFFFFu, keep);
-        __syncwarp();
-        if (keep) items[out + __popc(ball & ((1u << lane) - 1))] = it;
+        if (keep)
+            dst[out + __popc(ball & ((1u << lane) - 1u))] =
+                make_uint2(__float_as_uint(key2f(key[i])), blk[i]);
         out += __popc(ball);
-        __syncwarp();
     }
-    (void)k;
+    return out;
 }
 
 template <bool DENSE>
@@ -331,12 +284,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tc_fence_after();
                 const int64_t b = static_cast<int64_t>(j) * TB + quarter * 32 + lane;
                 const bool masked = !(tile_all_in && (static_cast<int64_t>(j) * TB + TB <= c_min));
-#pragma unroll 1
+                const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       buf * NCOL + half * 128;
+                uint32_t ra[32], rb[32];
+                tmem_ld32(tbase, ra);
+                tmem_wait32(ra);
+#pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
-                    float v[32];
-                    tmem_ld32(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + buf * NCOL +
-                                  half * 128 + ch * 32,
-                              v);
+                    uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
+                    uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
+                    if (ch < 3) tmem_ld32(tbase + (ch + 1) * 32, nxt);  // overlaps the math below
                     const int tl0 = half * 32 + ch * 8;
                     float th[8];
                     *reinterpret_cast<float4 *>(&th[0]) = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
@@ -345,10 +302,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int tk = 0; tk < 8; ++tk) {
                         const int tl = tl0 + tk;
                         const float4 wv = *reinterpret_cast<const float4 *>(&sW[tl * 4]);
-                        float s = wv.x * fmaxf(v[4 * tk + 0], 0.f);
-                        s = fmaf(wv.y, fmaxf(v[4 * tk + 1], 0.f), s);
-                        s = fmaf(wv.z, fmaxf(v[4 * tk + 2], 0.f), s);
-                        s = fmaf(wv.w, fmaxf(v[4 * tk + 3], 0.f), s);
+                        float s = wv.x * fmaxf(__uint_as_float(cur[4 * tk + 0]), 0.f);
+                        s = fmaf(wv.y, fmaxf(__uint_as_float(cur[4 * tk + 1]), 0.f), s);
+                        s = fmaf(wv.z, fmaxf(__uint_as_float(cur[4 * tk + 2]), 0.f), s);
+                        s = fmaf(wv.w, fmaxf(__uint_as_float(cur[4 * tk + 3]), 0.f), s);
                         s = s + 0.0f;  // no negative zero: float order == key order
                         const int64_t t = t0 + tl;
                         bool valid = true;
@@ -356,33 +313,58 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if constexpr (DENSE) {
                             if (valid) p.dense[t * p.dense_ld + b] = s;
                         } else {
-                            if (valid && s > th[tk]) {
-                                const int pos = atomicAdd(&sCnt[tl], 1);
-                                if (pos < CAP)
-                                    p.cand[(static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP + pos] =
-                                        make_uint2(__float_as_uint(s), static_cast<uint32_t>(b));
-                                else
-                                    report(p.status, QSA_ERR_DEVICE_CHECK);
+                            // a block enters the token's list when s >= its threshold;
+                            // one shared-memory atomic per warp and token
+                            const bool pass = valid && (s >= th[tk]);
+                            if (__any_sync(0xFFFFFFFFu, pass)) {
+                                const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
+                                const int leader = __ffs(m) - 1;
+                                int base = 0;
+                                if (lane == leader) base = atomicAdd(&sCnt[tl], __popc(m));
+                                base = __shfl_sync(0xFFFFFFFFu, base, leader);
+                                if (pass) {
+                                    const int pos = base + __popc(m & ((1u << lane) - 1u));
+                                    if (pos < CAP)
+                                        p.cand[(static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP + pos] =
+                                            make_uint2(__float_as_uint(s), static_cast<uint32_t>(b));
+                                    else
+                                        report(p.status, QSA_ERR_DEVICE_CHECK);
+                                }
                             }
                         }
                     }
+                    if (ch < 3) tmem_wait32(nxt);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 ++acc;
                 if constexpr (!DENSE) {
+                    // lists that might overflow on the next tile are cut back
                     named_bar(1 + half, 128);
                     for (int i = 0; i < 8; ++i) {
                         const int tl = half * 32 + quarter + 4 * i;
                         const int n = sCnt[tl];
                         if (n > CAP - TB) {
                             uint2 *items = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
-                            const unsigned long long T = warp_kth(items, n, p.k_sel, hist, lane);
-                            warp_compact(items, n, p.k_sel, T, lane);
+                            uint32_t key[NI], blk[NI];
+                            const uint32_t vm = load_items(items, n, key, blk, lane);
+                            // cheap pass: a bucket bound 16 bits below the shared prefix
+                            const RadixOut r = warp_radix<NI>(key, vm, p.k_sel, 2, hist, lane);
+                            uint32_t sel = 0;
+                            float th;
+                            if ((p.k_sel - r.krem) + r.eq <= KEEP_MAX) {
+#pragma unroll
+                                for (int q2 = 0; q2 < NI; ++q2)
+                                    if (((vm >> q2) & 1u) && key[q2] >= r.thr) sel |= 1u << q2;
+                                th = r.lo == 0 ? nextafterf(key2f(r.thr), INFINITY) : key2f(r.thr);
+                            } else {
+                                sel = warp_select_exact<NI>(key, blk, vm, p.k_sel, hist, lane, &th);
+                            }
+                            const int kept = store_items(items, key, blk, sel, lane);
                             if (lane == 0) {
-                                sCnt[tl] = p.k_sel;
-                                sTheta[tl] = key2f(static_cast<uint32_t>(T >> 32));
+                                sCnt[tl] = kept;
+                                sTheta[tl] = th;
                             }
                             __syncwarp();
                         }
@@ -401,32 +383,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int64_t c = t / kBlock;
                     const int n = sCnt[tl];
                     uint2 *items = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
-                    int m = n;
-                    unsigned long long T = 0;
+                    uint32_t key[NI], blk[NI];
+                    const uint32_t vm = load_items(items, n, key, blk, lane);
+                    uint32_t sel = vm;
                     if (n > p.k_sel) {
-                        T = warp_kth(items, n, p.k_sel, hist, lane);
-                        m = p.k_sel;
+                        float th;
+                        sel = warp_select_exact<NI>(key, blk, vm, p.k_sel, hist, lane, &th);
                     }
-                    // gather the kept items as (block << 32 | score bits)
-                    int outn = 0;
-                    for (int base = 0; base < n; base += 32) {
-                        const int ii = base + lane;
-                        uint2 it = make_uint2(0, 0);
-                        bool keep = false;
-                        if (ii < n) {
-                            it = items[ii];
-                            keep = (n <= p.k_sel) || composite(it) >= T;
-                        }
+                    // the kept items as (block << 32 | score bits), sorted by block
+                    int m = 0;
+#pragma unroll
+                    for (int q2 = 0; q2 < NI; ++q2) {
+                        const bool keep = (sel >> q2) & 1u;
                         const unsigned ball = __ballot_sync(0xFFFFFFFFu, keep);
                         if (keep) {
-                            const int pos = outn + __popc(ball & ((1u << lane) - 1));
+                            const int pos = m + __popc(ball & ((1u << lane) - 1u));
                             if (pos < SORTN)
-                                sortb[pos] = (static_cast<unsigned long long>(it.y) << 32) | it.x;
+                                sortb[pos] = (static_cast<unsigned long long>(blk[q2]) << 32) |
+                                             __float_as_uint(key2f(key[q2]));
                         }
-                        outn += __popc(ball);
+                        m += __popc(ball);
                     }
-                    if (outn > SORTN) { report(p.status, QSA_ERR_DEVICE_CHECK); outn = SORTN; }
-                    m = outn < m ? outn : m;
+                    if (m > SORTN) { report(p.status, QSA_ERR_DEVICE_CHECK); m = SORTN; }
                     int P2 = 32;
                     while (P2 < m) P2 <<= 1;
                     for (int ii = m + lane; ii < P2; ii += 32) sortb[ii] = ~0ull;
