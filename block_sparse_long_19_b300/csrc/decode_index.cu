@@ -306,21 +306,38 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
         return;
     }
     const int64_t c = (T - 1) / kBlock;
-    if (threadIdx.x == 0) {
-        int o = 0;
-        for (int ch = 0; ch < p.nchunk; ++ch) {
-            offs[ch] = o;
-            o += p.k_sel > 0 ? p.cnt[static_cast<int64_t>(s) * p.nchunk + ch] : 0;
+    // chunk counts in parallel, then every candidate slot of every chunk
+    // flattened over the threads (order does not matter: the selection is
+    // order-free and the output is sorted by block)
+    for (int ch = threadIdx.x; ch < p.nchunk; ch += MERGE_THREADS)
+        offs[ch] = p.k_sel > 0 ? p.cnt[static_cast<int64_t>(s) * p.nchunk + ch] : 0;
+    if (threadIdx.x == 0) ctl[3] = 0;
+    __syncthreads();
+    const int slots = p.nchunk * p.k_sel;
+    const uint2 *src = p.cand + static_cast<int64_t>(s) * p.nchunk * p.k_sel;
+    constexpr int U = 8;
+    for (int base = threadIdx.x; base < slots; base += MERGE_THREADS * U) {
+        uint2 it[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = base + u * MERGE_THREADS;
+            ok[u] = false;
+            if (j < slots) {
+                const int ch = j / p.k_sel;
+                ok[u] = (j - ch * p.k_sel) < offs[ch];
+                if (ok[u]) it[u] = src[j];
+            }
         }
-        offs[p.nchunk] = o;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (ok[u]) {
+                const int pos = atomicAdd(&ctl[3], 1);
+                if (pos < cap) items[pos] = it[u];
+            }
     }
     __syncthreads();
-    const int n = offs[p.nchunk];
-    for (int ch = 0; ch < p.nchunk; ++ch) {
-        const int m = offs[ch + 1] - offs[ch];
-        const uint2 *src = p.cand + (static_cast<int64_t>(s) * p.nchunk + ch) * p.k_sel;
-        for (int i = threadIdx.x; i < m; i += MERGE_THREADS) items[offs[ch] + i] = src[i];
-    }
+    const int n = min(ctl[3], cap);
     __syncthreads();
     int m = n;
     SelectRule rule{0u, 0u, 1};

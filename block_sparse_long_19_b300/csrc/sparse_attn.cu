@@ -14,12 +14,18 @@
 // the tensor cores.  The design therefore spends its effort on the data path:
 //   * one CTA per query (all 24 heads: each gathered row serves both KV heads'
 //     12 query heads);
-//   * a producer warp issues one 1 KiB cp.async.bulk per key row (both KV
-//     heads) into a ring of stages; rows land at a 1040-byte pitch so the
-//     tensor-core operand loads (ldmatrix) are free of bank conflicts;
-//   * four consumer warps (KV head x stage parity) run QK^T and PV with the
-//     warp-level MMA (m16n8k16, bf16 in, fp32 out) and an fp32 online softmax
-//     in the log2 domain with a lazy rescale; the two parities merge at the end.
+//   * a producer warp issues one 4 KiB cp.async.bulk per selected block for K
+//     and one for V (a block's 4 key rows of both KV heads are contiguous in
+//     HBM) into a ring of 64 KiB stages of 8 blocks; block slots are skewed by
+//     16 bytes so the tensor-core operand loads (ldmatrix) are free of bank
+//     conflicts.  4 KiB copies matter: with 1 KiB copies one producer warp
+//     per SM could not keep enough bytes in flight;
+//   * four consumer warps (KV head x key half of every stage) run QK^T and PV
+//     with the warp-level MMA (m16n8k16, bf16 in, fp32 out) and an fp32 online
+//     softmax in the log2 domain with a lazy rescale; the two halves merge at
+//     the end.  Every consumer waits on every stage: with an odd ring depth,
+//     consumers that skipped stages could wait on a slot two fills ahead,
+//     which a one-bit phase parity cannot tell apart.
 // Decode runs the same kernel over a slice of the selected blocks per CTA
 // (split-KV) and a second kernel merges the slices by log-sum-exp.
 #include "qsa_common.cuh"
@@ -28,9 +34,15 @@
 namespace qsa {
 namespace at {
 
-constexpr int SKEYS = 16;                 // keys per stage = 4 blocks
-constexpr int ROWB = kHKV * kD * 2 + 16;  // 1040 B per key row in smem
-constexpr int STAGE_BYTES = 2 * SKEYS * ROWB;
+// A stage holds 8 selected blocks (32 keys).  Each block's 4 key rows (both
+// KV heads, 1 KiB per row) arrive as one 4 KiB bulk copy into a "slot"; slots
+// sit 4096 + 16 bytes apart, so the 8 rows an 8x8 ldmatrix reads (the same
+// token of 8 different blocks) fall into 8 different bank groups.
+constexpr int SBLK = 8;                   // blocks per stage
+constexpr int ROWB = kHKV * kD * 2;       // 1024 B per key row
+constexpr int SLOTB = kBlock * ROWB + 16; // 4112 B per block slot
+constexpr int KV_BYTES = SBLK * SLOTB;    // K (or V) part of a stage
+constexpr int STAGE_BYTES = 2 * KV_BYTES;
 constexpr int QROW = kD * 2 + 16;         // 528 B per query row in smem
 constexpr int Q_BYTES = kHKV * 16 * QROW;
 constexpr int NCONS = 4;
@@ -48,7 +60,7 @@ constexpr int smem_bytes() {
 // combine buffer (reuses the stage ring after the main loop): per KV head
 // 32 lanes x (32 dim tiles x 4 + 4) floats
 constexpr int COMB_FLOATS = 32 * (32 * 4 + 4);
-static_assert(kHKV * COMB_FLOATS * 4 <= 2 * STAGE_BYTES, "combine buffer must fit in two stages");
+static_assert(kHKV * COMB_FLOATS * 4 <= STAGE_BYTES, "combine buffer must fit in one stage");
 
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -99,7 +111,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 2);
+            mbar_init(&empty[i], NCONS);
         }
         fence_barrier_init();
     }
@@ -151,7 +163,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     __syncthreads();
 
     const int nslot = sMisc[0];
-    const int total_st = (nslot + 3) / 4;
+    const int total_st = (nslot + SBLK - 1) / SBLK;
     int st_begin = 0, st_end = total_st;
     if constexpr (DECODE) {
         const int per = (total_st + a.nsplit - 1) / a.nsplit;
@@ -162,8 +174,13 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
 
     if (warp == 0) {
         // ------------------------------------------------- producer --
-        const int r = lane & 15;
-        const int isv = lane >> 4;
+        // lanes 0..7: K of slot `lane`, lanes 8..15: V of slot `lane - 8`.
+        // A past block (b < c, all rows <= t) is one 4 KiB copy.  The current
+        // block and padding slots are copied row by row; a row that must not
+        // be attended (j > t, or no block) fetches the query's own row t, so
+        // every byte read is inside the tensor and finite.
+        const int sl = lane & 7;
+        const int isv = (lane >> 3) & 1;
         const uint64_t pol = policy_evict_first();
         bool ok = true;
         for (int st = st_begin; st < st_end; ++st) {
@@ -173,17 +190,36 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
             if (lane == 0) ok = mbar_wait(&empty[slot], ph ^ 1);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], 2 * SKEYS * 1024);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], STAGE_BYTES - 2 * SBLK * 16);
             __syncwarp();
-            const int si = st * 4 + (r >> 2);
-            const int b = si < a.budget ? sIdx[si] : -1;
-            const int64_t j = static_cast<int64_t>(b) * kBlock + (r & 3);
-            const bool valid = b >= 0 && j <= t;
-            const int64_t row = valid ? j : t;  // masked rows fetch the query's own row
-            const uint16_t *src = (isv ? vbase : kbase) + row * (kHKV * kD);
-            uint8_t *dst = sSt + slot * STAGE_BYTES + isv * SKEYS * ROWB + r * ROWB;
-            bulk_g2s_hint(dst, src, 1024, &full[slot], pol);
+            if (lane < 16) {
+                const int si = st * SBLK + sl;
+                const int b = si < a.budget ? sIdx[si] : -1;
+                const uint16_t *base = isv ? vbase : kbase;
+                uint8_t *dst = sSt + slot * STAGE_BYTES + isv * KV_BYTES + sl * SLOTB;
+                if (b >= 0 && b < c) {
+                    bulk_g2s_hint(dst, base + static_cast<int64_t>(b) * kBlock * (kHKV * kD),
+                                  kBlock * ROWB, &full[slot], pol);
+                } else {
+#pragma unroll
+                    for (int r = 0; r < kBlock; ++r) {
+                        const int64_t j = static_cast<int64_t>(b) * kBlock + r;
+                        const int64_t row = (b >= 0 && j <= t) ? j : t;
+                        bulk_g2s_hint(dst + r * ROWB, base + row * (kHKV * kD), ROWB, &full[slot], pol);
+                    }
+                }
+            }
         }
+        // the CTA must not finish while its copies can still land: wait for the
+        // stages issued last (normal runs find them complete already)
+        if (lane == 0) {
+            const int first = max(st_begin, st_end - NST);
+            for (int st = first; st < st_end; ++st) {
+                const int local = st - st_begin;
+                if (!mbar_wait(&full[local % NST], (local / NST) & 1)) ok = false;
+            }
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
         if (!ok && lane == 0) {
             report(a.status, QSA_ERR_TIMEOUT);
             sMisc[1] = 1;
@@ -192,9 +228,14 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     }
 
     // ------------------------------------------------------ consumers --
+    // Every consumer warp takes part in every stage (so no warp can ever wait
+    // on a ring slot more than one fill ahead): warp (g, kh) handles KV head g
+    // and the key half kh of each stage, i.e. tokens 2kh and 2kh+1 of the 8
+    // blocks, and keeps its own online-softmax state; the two key halves are
+    // merged at the end.
     const int cw = warp - 1;
     const int g = cw & 1;
-    const int par = cw >> 1;
+    const int kh = cw >> 1;
     const int qd = lane & 3;     // column pair within an 8-wide tile
     const int r0 = lane >> 2;    // fragment rows r0 and r0 + 8 (= query heads g*12 + r)
     float O[32][4];
@@ -205,55 +246,62 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
 
     const uint32_t q_addr = smem_u32(sQ) + g * 16 * QROW +
                             ((lane & 7) + ((lane >> 3) & 1) * 8) * QROW + (lane >> 4) * 16;
-    const int krow_l = (lane & 7) + (lane >> 4) * 8;
-    const int kcol_l = ((lane >> 3) & 1) * 16;
-    const int vrow_l = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const int vcol_l = (lane >> 4) * 16;
+    // key k of a stage = (token-in-block k / 8, slot k % 8)
+    // QK^T B operand (keys x dims): lanes 0-7 / 16-23 -> token 2kh / 2kh+1 of slots 0-7,
+    // lanes 8-15 / 24-31 -> dims +8
+    const uint32_t k_lane = (lane & 7) * SLOTB + (2 * kh + (lane >> 4)) * ROWB + ((lane >> 3) & 1) * 16;
+    // PV B operand via ldmatrix.trans (keys x dims): lanes 0-7 / 8-15 -> token 2kh / 2kh+1
+    // of slots 0-7, lanes 16-31 -> dims +8
+    const uint32_t v_lane = (lane & 7) * SLOTB + (2 * kh + ((lane >> 3) & 1)) * ROWB + (lane >> 4) * 16;
     bool ok = true;
 
-    for (int st = st_begin + par; st < st_end; st += 2) {
+    for (int st = st_begin; st < st_end; ++st) {
         const int local = st - st_begin;
         const int slot = local % NST;
         const uint32_t ph = (local / NST) & 1;
         if (!mbar_wait(&full[slot], ph)) { ok = false; break; }
         const uint32_t kb = smem_u32(sSt + slot * STAGE_BYTES) + g * (kD * 2);
-        const uint32_t vb = kb + SKEYS * ROWB;
+        const uint32_t vb = kb + KV_BYTES;
 
-        float S0[4] = {0.f, 0.f, 0.f, 0.f}, S1[4] = {0.f, 0.f, 0.f, 0.f};
+        // S[n][4]: n-tile n = token 2kh + n of the 8 slots
+        float S[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) S[n][0] = S[n][1] = S[n][2] = S[n][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
             uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
             ldsm_x4(q_addr + kk * 32, a0, a1, a2, a3);
-            ldsm_x4(kb + krow_l * ROWB + kk * 32 + kcol_l, b0, b1, b2, b3);
-            mma_bf16_16816(S0, a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(S1, a0, a1, a2, a3, b2, b3);
+            ldsm_x4(kb + k_lane + kk * 32, b0, b1, b2, b3);
+            mma_bf16_16816(S[0], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(S[1], a0, a1, a2, a3, b2, b3);
         }
-        // log2-domain logits; mask keys outside the selection or after t
-        float z[8] = {S0[0], S0[1], S1[0], S1[1], S0[2], S0[3], S1[2], S1[3]};
         bool need_mask = false;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int si = st * 4 + e;
+        for (int e = 0; e < SBLK; ++e) {
+            const int si = st * SBLK + e;
             const int b = si < a.budget ? sIdx[si] : -1;
             need_mask |= (b < 0) || (b == c);
         }
+        // S[n][0..1]: row r0, S[n][2..3]: row r0+8; columns = slots 2qd, 2qd+1
 #pragma unroll
-        for (int e = 0; e < 8; ++e) z[e] *= a.scale_log2;
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) S[n][e] *= a.scale_log2;
         if (need_mask) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int key = (e & 2 ? 8 : 0) + 2 * qd + (e & 1);  // key within the stage
-                const int si = st * 4 + (key >> 2);
-                const int b = si < a.budget ? sIdx[si] : -1;
-                const int64_t j = static_cast<int64_t>(b) * kBlock + (key & 3);
-                if (b < 0 || j > t) z[e] = -INFINITY;
-            }
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int si = st * SBLK + 2 * qd + (e & 1);
+                    const int b = si < a.budget ? sIdx[si] : -1;
+                    const int64_t j = static_cast<int64_t>(b) * kBlock + 2 * kh + n;
+                    if (b < 0 || j > t) S[n][e] = -INFINITY;
+                }
         }
-        // z[0..3]: row r0 ; z[4..7]: row r0 + 8
-        float p[8];
+        float pv[2][4];
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-            float mx = fmaxf(fmaxf(z[4 * rr], z[4 * rr + 1]), fmaxf(z[4 * rr + 2], z[4 * rr + 3]));
+            float mx = fmaxf(fmaxf(S[0][2 * rr], S[0][2 * rr + 1]), fmaxf(S[1][2 * rr], S[1][2 * rr + 1]));
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
             if (mx > m_r[rr] + 8.f) {
@@ -268,19 +316,24 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
             }
             const bool dead = m_r[rr] == -INFINITY;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                p[4 * rr + e] = dead ? 0.f : exp2f(z[4 * rr + e] - m_r[rr]);
-                l_r[rr] += p[4 * rr + e];
-            }
+            for (int n = 0; n < 2; ++n)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float pe = dead ? 0.f : exp2f(S[n][2 * rr + e] - m_r[rr]);
+                    pv[n][2 * rr + e] = pe;
+                    l_r[rr] += pe;
+                }
         }
-        const uint32_t pa0 = pack_bf16(p[0], p[1]);  // row r0,   keys 2qd..   (n-tile 0)
-        const uint32_t pa1 = pack_bf16(p[4], p[5]);  // row r0+8, keys 2qd..
-        const uint32_t pa2 = pack_bf16(p[2], p[3]);  // row r0,   keys 8+2qd.. (n-tile 1)
-        const uint32_t pa3 = pack_bf16(p[6], p[7]);  // row r0+8, keys 8+2qd..
+        // one k-step of 16 keys: token 2kh (n-tile 0) then token 2kh+1 (n-tile 1)
+        const uint32_t pa0 = pack_bf16(pv[0][0], pv[0][1]);
+        const uint32_t pa1 = pack_bf16(pv[0][2], pv[0][3]);
+        const uint32_t pa2 = pack_bf16(pv[1][0], pv[1][1]);
+        const uint32_t pa3 = pack_bf16(pv[1][2], pv[1][3]);
+        const uint32_t vks = vb + v_lane;
 #pragma unroll
         for (int dt = 0; dt < 16; ++dt) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vb + vrow_l * ROWB + dt * 32 + vcol_l, b0, b1, b2, b3);
+            ldsm_x4_t(vks + dt * 32, b0, b1, b2, b3);
             mma_bf16_16816(O[2 * dt], pa0, pa1, pa2, pa3, b0, b1);
             mma_bf16_16816(O[2 * dt + 1], pa0, pa1, pa2, pa3, b2, b3);
         }
@@ -299,10 +352,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
         l_r[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_r[rr], 2);
     }
 
-    // ------------------------------------------- merge the two parities --
+    // ------------------------------------------ merge the two key halves --
     named_bar(1, NCONS * 32);  // every consumer is done reading the ring
     float *comb = reinterpret_cast<float *>(sSt) + g * COMB_FLOATS;
-    if (par == 1) {
+    if (kh == 1) {
 #pragma unroll
         for (int i = 0; i < 32; ++i)
             *reinterpret_cast<float4 *>(&comb[(i * 32 + lane) * 4]) =
@@ -311,7 +364,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
             make_float4(m_r[0], m_r[1], l_r[0], l_r[1]);
     }
     named_bar(1, NCONS * 32);
-    if (par == 1) return;
+    if (kh == 1) return;
     const float4 ml = *reinterpret_cast<const float4 *>(&comb[32 * 32 * 4 + lane * 4]);
     const float m1[2] = {ml.x, ml.y}, l1[2] = {ml.z, ml.w};
     float fa[2], fb[2], lt[2], mt[2];
@@ -404,7 +457,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
 
 }  // namespace at
 
-constexpr int kPrefillStages = 6;
+constexpr int kPrefillStages = 3;
 constexpr int kDecodeStages = 3;
 
 cudaError_t launch_attn_prefill(const AttnArgs &a, const RopeFreqs &f, cudaStream_t stream) {
