@@ -138,6 +138,12 @@ size_t index_ws(int64_t L) {
 
 }  // namespace
 
+namespace qsa {
+// Lets other translation units of the library set the message returned by
+// qsa_last_error_detail().
+void set_error_detail(const char *msg) { g_detail = msg; }
+}  // namespace qsa
+
 extern "C" {
 
 void qsa_default_config(qsa_config *cfg) {

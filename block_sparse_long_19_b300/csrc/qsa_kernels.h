@@ -7,6 +7,9 @@
 
 namespace qsa {
 
+// Message for qsa_last_error_detail() on this host thread.
+void set_error_detail(const char *msg);
+
 // inv_freq[i] = theta^(-2i/64), computed on the host in double.
 struct RopeFreqs {
     double inv_freq[32];

@@ -30,6 +30,7 @@ EXPORTED = [
     "qsa_default_config", "qsa_status_string", "qsa_last_error_detail", "qsa_kprep",
     "qsa_index_topk_workspace_bytes", "qsa_index_topk", "qsa_index_scores",
     "qsa_sparse_attn_prefill", "qsa_decode_workspace_bytes", "qsa_sparse_attn_decode",
+    "qsa_sparse_attn_decode_noalloc",
 ]
 
 
@@ -85,6 +86,9 @@ def load(path: str = LIB_PATH):
     L.qsa_sparse_attn_decode.argtypes = [cfgp, c.c_int, P, P, P, P, P, P, c.c_int64, P, P, P, P,
                                          P, c.c_size_t, P, P]
     L.qsa_sparse_attn_decode.restype = c.c_int
+    L.qsa_sparse_attn_decode_noalloc.argtypes = [cfgp, c.c_int, P, P, P, P, P, P, c.c_int64, P, P,
+                                                 P, P, P, P]
+    L.qsa_sparse_attn_decode_noalloc.restype = c.c_int
     _lib = L
     return L
 
@@ -263,6 +267,36 @@ def sparse_attn_decode(cfg: Config, q, qi, w, k_cache, v_cache, kblk_cache, seq_
         ctypes.byref(cfg), B, _ptr(q), _ptr(qi), _ptr(w), _ptr(k_cache), _ptr(v_cache),
         _ptr(kblk_cache), Tmax, _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(ws),
         ws.numel(), _ptr(status), _stream(stream)), "qsa_sparse_attn_decode")
+    return out, lse, idx_out, status
+
+
+def sparse_attn_decode_noalloc(cfg: Config, q, qi, w, k_cache, v_cache, kblk_cache, seq_lens,
+                               out=None, lse=None, idx_out=None, status=None, want_idx: bool = True,
+                               want_lse: bool = True, stream=None):
+    """Decode through qsa_sparse_attn_decode_noalloc: no workspace argument,
+    the library's built-in 16 MiB device scratch is used instead (for callers
+    that cannot allocate device memory; see include/qsa.h)."""
+    B, Tmax = k_cache.shape[0], k_cache.shape[1]
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (B, 24, 256))
+    _need(qi, "qi", torch.bfloat16, (B, 4, 128))
+    _need(w, "w", torch.bfloat16, (B, 4))
+    _need(k_cache, "k_cache", torch.bfloat16, (B, Tmax, 2, 256))
+    _need(v_cache, "v_cache", torch.bfloat16, (B, Tmax, 2, 256))
+    _need(kblk_cache, "kblk_cache", torch.bfloat16, (B, Tmax // 4, 128))
+    _need(seq_lens, "seq_lens", torch.int32, (B,))
+    if out is None:
+        out = torch.empty((B, 24, 256), dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((B, 24), dtype=torch.float32, device=dev)
+    if idx_out is None and want_idx:
+        idx_out = torch.empty((B, cfg.budget_blocks), dtype=torch.int32, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_sparse_attn_decode_noalloc(
+        ctypes.byref(cfg), B, _ptr(q), _ptr(qi), _ptr(w), _ptr(k_cache), _ptr(v_cache),
+        _ptr(kblk_cache), Tmax, _ptr(seq_lens), _ptr(out), _ptr(lse), _ptr(idx_out), _ptr(status),
+        _stream(stream)), "qsa_sparse_attn_decode_noalloc")
     return out, lse, idx_out, status
 
 

@@ -32,7 +32,8 @@
  *   - The caller owns every buffer, workspaces included.  The library never
  *     allocates or frees device memory and keeps no state between calls
  *     other than a cached per-device property query and a resolved driver
- *     entry point.
+ *     entry point (qsa_sparse_attn_decode_noalloc, at the end, is the one
+ *     call that uses a built-in scratch array instead of a workspace).
  *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and return without synchronising.
  *   - Argument errors are reported synchronously by the return value, and
@@ -187,6 +188,34 @@ qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf
                                   const int32_t *seq_lens, qsa_bf16 *out, float *lse,
                                   int32_t *idx_out, void *ws, size_t ws_bytes,
                                   int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Decode without a workspace argument: the same computation as
+ * qsa_sparse_attn_decode (same arguments minus ws / ws_bytes), for callers
+ * that cannot allocate device memory when they run a decode step -- a C host
+ * embedded in a process whose device memory is owned by another runtime, or
+ * a serving loop that must not call cudaMalloc/cudaFree (they can
+ * synchronise the device and fail under memory pressure mid-request).
+ * The pages have no counterpart of this call; it is a property of this
+ * library's interface only.
+ *   - Scratch is a statically sized device array inside libqsa.so, 16 MiB,
+ *     present on every GPU that loads the library until it is unloaded.
+ *     batch x max_ctx combinations whose workspace
+ *     (qsa_decode_workspace_bytes) exceeds it return QSA_ERR_UNSUPPORTED and
+ *     launch nothing (8 x 1,048,576 and 64 x 262,144 fit).
+ *   - The first call on each device (that device current) resolves the
+ *     array's device address; make that first call before any stream
+ *     capture.
+ *   - All calls share the array: calls whose GPU work overlaps (other
+ *     streams, unordered host threads) race.  Nothing in it needs zeroing.
+ *   - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).
+ * ---------------------------------------------------------------------- */
+qsa_status qsa_sparse_attn_decode_noalloc(const qsa_config *cfg, int batch, const qsa_bf16 *q,
+                                          const qsa_bf16 *qi, const qsa_bf16 *w,
+                                          const qsa_bf16 *k_cache, const qsa_bf16 *v_cache,
+                                          const qsa_bf16 *kblk_cache, int64_t max_ctx,
+                                          const int32_t *seq_lens, qsa_bf16 *out, float *lse,
+                                          int32_t *idx_out, int32_t *dev_status, void *stream);
 
 #ifdef __cplusplus
 }
