@@ -39,6 +39,7 @@ constexpr int NCOL = TQ * kHI;       // 256 MMA columns (token-major, head-minor
 constexpr int TB = 128;              // block keys per block tile (MMA M)
 constexpr int NSTAGE = 3;            // kblk tile ring
 constexpr int CAP = 1024;            // candidate slots per token (32 per lane)
+constexpr int SUB = CAP / 4;         // per-warp sub-list of a token (one per TMEM lane quarter)
 constexpr int KSTEPS = kDI / 16;     // 8 MMAs of K = 16
 constexpr int NEPI = 8;              // epilogue warps
 constexpr int THREADS = (4 + NEPI) * 32;
@@ -54,8 +55,8 @@ constexpr int OFF_SORT = OFF_K + NSTAGE * SK_BYTES;
 constexpr int OFF_HIST = OFF_SORT + NEPI * SORTN * 8;
 constexpr int OFF_W = OFF_HIST + NEPI * 256 * 4;
 constexpr int OFF_THETA = OFF_W + TQ * 4 * 4;
-constexpr int OFF_CNT = OFF_THETA + TQ * 4;
-constexpr int OFF_BAR = OFF_CNT + TQ * 4;
+constexpr int OFF_CNT = OFF_THETA + TQ * 4;  // [4 quarters][TQ] sub-list counts
+constexpr int OFF_BAR = OFF_CNT + 4 * TQ * 4;
 constexpr int NBAR = 2 * NSTAGE + 2 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -85,40 +86,47 @@ __device__ __forceinline__ int num_btiles(int64_t L, int q) {
     return static_cast<int>((cmax + TB - 1) / TB);
 }
 
-// Candidate lists hold (score bits, block); loaded into registers as
-// (order-preserving key, block), item i of a lane = list entry i*32 + lane.
+// A token's candidate list is 4 sub-lists of SUB entries, one per epilogue
+// warp of its half (the warp that owns TMEM lane quarter q appends to
+// sub-list q with a warp-private count, so appending needs neither atomics
+// nor shuffles).  Entries are (score bits, block).  For selection the union
+// is loaded into registers as (order-preserving key, block): item i of a
+// lane is entry (i % 8) * 32 + lane of sub-list i / 8.
 constexpr int NI = CAP / 32;
 constexpr int KEEP_MAX = CAP - 2 * TB;  // a lower-bound compaction must keep at most this many
 
-__device__ __forceinline__ uint32_t load_items(const uint2 *src, int n, uint32_t (&key)[NI],
-                                               uint32_t (&blk)[NI], int lane) {
+__device__ __forceinline__ uint32_t load_union(const uint2 *lst, const int (&n)[4],
+                                               uint32_t (&key)[NI], uint32_t (&blk)[NI], int lane) {
     uint32_t vm = 0;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
-        const int j = i * 32 + lane;
+        const int q = i >> 3;
+        const int e = (i & 7) * 32 + lane;
         uint2 it = make_uint2(0u, 0u);
-        if (j < n) {
-            it = src[j];
+        if (e < n[q]) {
+            it = lst[q * SUB + e];
             vm |= 1u << i;
         }
         key[i] = f2key(__uint_as_float(it.x));
         blk[i] = it.y;
     }
+    __syncwarp();  // every lane's reads are done before anyone rewrites the list
     return vm;
 }
 
-// Write the items whose bit is set in `sel` to the front of the list (all
-// reads happened in load_items, so overwriting in place is safe).
-__device__ __forceinline__ int store_items(uint2 *dst, const uint32_t (&key)[NI],
+// Write the items whose bit is set in `sel` back, dealt round-robin over the
+// 4 sub-lists; returns the total kept (sub-list q then holds (kept+3-q)/4).
+__device__ __forceinline__ int store_union(uint2 *lst, const uint32_t (&key)[NI],
                                            const uint32_t (&blk)[NI], uint32_t sel, int lane) {
     int out = 0;
 #pragma unroll
     for (int i = 0; i < NI; ++i) {
         const bool keep = (sel >> i) & 1u;
         const unsigned ball = __ballot_sync(0xFFFFFFFFu, keep);
-        if (keep)
-            dst[out + __popc(ball & ((1u << lane) - 1u))] =
-                make_uint2(__float_as_uint(key2f(key[i])), blk[i]);
+        if (keep) {
+            const int r = out + __popc(ball & ((1u << lane) - 1u));
+            lst[(r & 3) * SUB + (r >> 2)] = make_uint2(__float_as_uint(key2f(key[i])), blk[i]);
+        }
         out += __popc(ball);
     }
     return out;
@@ -137,7 +145,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t *sHist = reinterpret_cast<uint32_t *>(smem + OFF_HIST);
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sTheta = reinterpret_cast<float *>(smem + OFF_THETA);
-    int *sCnt = reinterpret_cast<int *>(smem + OFF_CNT);
+    int *sCnt = reinterpret_cast<int *>(smem + OFF_CNT);  // sCnt[q * TQ + tl]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *full = bars;
     uint64_t *empty = bars + NSTAGE;
@@ -255,6 +263,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int tid_h = quarter * 32 + lane;
         uint32_t *hist = sHist + e * 256;
         unsigned long long *sortb = sSort + e * SORTN;
+        const unsigned ltmask = (1u << lane) - 1u;
+        // this warp's sub-lists: token tl's at sub[tl * CAP]
+        uint2 *sub = p.cand + static_cast<int64_t>(blockIdx.x) * TQ * CAP + quarter * SUB;
         uint32_t acc = 0;
         bool ok = true;
         for (int kk = blockIdx.x; kk < p.nq && ok; kk += gridDim.x) {
@@ -265,7 +276,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (tid_h < 32) {
                 const int tl = half * 32 + tid_h;
                 const int64_t t = t0 + tl;
-                sCnt[tl] = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) sCnt[q * TQ + tl] = 0;
                 sTheta[tl] = -INFINITY;
 #pragma unroll
                 for (int h = 0; h < kHI; ++h) {
@@ -298,40 +310,40 @@ __global__ void __launch_bounds__(THREADS, 1)
                     float th[8];
                     *reinterpret_cast<float4 *>(&th[0]) = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
                     *reinterpret_cast<float4 *>(&th[4]) = *reinterpret_cast<const float4 *>(&sTheta[tl0 + 4]);
+                    int cnt8[8];
+                    if constexpr (!DENSE) {
+                        *reinterpret_cast<int4 *>(&cnt8[0]) = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0]);
+                        *reinterpret_cast<int4 *>(&cnt8[4]) = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0 + 4]);
+                    }
 #pragma unroll
                     for (int tk = 0; tk < 8; ++tk) {
                         const int tl = tl0 + tk;
                         const float4 wv = *reinterpret_cast<const float4 *>(&sW[tl * 4]);
-                        float s = wv.x * fmaxf(__uint_as_float(cur[4 * tk + 0]), 0.f);
+                        // the first product is added to +0 so the sum is never -0
+                        float s = fmaf(wv.x, fmaxf(__uint_as_float(cur[4 * tk + 0]), 0.f), 0.0f);
                         s = fmaf(wv.y, fmaxf(__uint_as_float(cur[4 * tk + 1]), 0.f), s);
                         s = fmaf(wv.z, fmaxf(__uint_as_float(cur[4 * tk + 2]), 0.f), s);
                         s = fmaf(wv.w, fmaxf(__uint_as_float(cur[4 * tk + 3]), 0.f), s);
-                        s = s + 0.0f;  // no negative zero: float order == key order
                         const int64_t t = t0 + tl;
                         bool valid = true;
                         if (masked) valid = (t < p.L) && (b < t / kBlock);
                         if constexpr (DENSE) {
                             if (valid) p.dense[t * p.dense_ld + b] = s;
                         } else {
-                            // a block enters the token's list when s >= its threshold;
-                            // one shared-memory atomic per warp and token
+                            // a block enters the token's list when s >= its threshold:
+                            // position from a ballot, no branch, no atomic
                             const bool pass = valid && (s >= th[tk]);
-                            if (__any_sync(0xFFFFFFFFu, pass)) {
-                                const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
-                                const int leader = __ffs(m) - 1;
-                                int base = 0;
-                                if (lane == leader) base = atomicAdd(&sCnt[tl], __popc(m));
-                                base = __shfl_sync(0xFFFFFFFFu, base, leader);
-                                if (pass) {
-                                    const int pos = base + __popc(m & ((1u << lane) - 1u));
-                                    if (pos < CAP)
-                                        p.cand[(static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP + pos] =
-                                            make_uint2(__float_as_uint(s), static_cast<uint32_t>(b));
-                                    else
-                                        report(p.status, QSA_ERR_DEVICE_CHECK);
-                                }
-                            }
+                            const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
+                            const int pos = cnt8[tk] + __popc(m & ltmask);
+                            if (pass && pos < SUB)
+                                sub[static_cast<int64_t>(tl) * CAP + pos] =
+                                    make_uint2(__float_as_uint(s), static_cast<uint32_t>(b));
+                            cnt8[tk] += __popc(m);
                         }
+                    }
+                    if constexpr (!DENSE) {
+                        *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0]) = *reinterpret_cast<const int4 *>(&cnt8[0]);
+                        *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0 + 4]) = *reinterpret_cast<const int4 *>(&cnt8[4]);
                     }
                     if (ch < 3) tmem_wait32(nxt);
                 }
@@ -344,11 +356,17 @@ __global__ void __launch_bounds__(THREADS, 1)
                     named_bar(1 + half, 128);
                     for (int i = 0; i < 8; ++i) {
                         const int tl = half * 32 + quarter + 4 * i;
-                        const int n = sCnt[tl];
-                        if (n > CAP - TB) {
-                            uint2 *items = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
+                        int n[4];
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) n[q] = sCnt[q * TQ + tl];
+                        const int nmax = max(max(n[0], n[1]), max(n[2], n[3]));
+                        if (nmax > SUB) report(p.status, QSA_ERR_DEVICE_CHECK);
+                        if (nmax > SUB - 32) {
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) n[q] = min(n[q], SUB);
+                            uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
                             uint32_t key[NI], blk[NI];
-                            const uint32_t vm = load_items(items, n, key, blk, lane);
+                            const uint32_t vm = load_union(lst, n, key, blk, lane);
                             // cheap pass: a bucket bound 16 bits below the shared prefix
                             const RadixOut r = warp_radix<NI>(key, vm, p.k_sel, 2, hist, lane);
                             uint32_t sel = 0;
@@ -361,11 +379,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                             } else {
                                 sel = warp_select_exact<NI>(key, blk, vm, p.k_sel, hist, lane, &th);
                             }
-                            const int kept = store_items(items, key, blk, sel, lane);
-                            if (lane == 0) {
-                                sCnt[tl] = kept;
-                                sTheta[tl] = th;
-                            }
+                            const int kept = store_union(lst, key, blk, sel, lane);
+                            if (lane < 4) sCnt[lane * TQ + tl] = (kept + 3 - lane) / 4;
+                            if (lane == 0) sTheta[tl] = th;
                             __syncwarp();
                         }
                     }
@@ -381,10 +397,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int64_t t = t0 + tl;
                     if (t >= p.L) continue;
                     const int64_t c = t / kBlock;
-                    const int n = sCnt[tl];
-                    uint2 *items = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
+                    int nq4[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) nq4[q] = min(sCnt[q * TQ + tl], SUB);
+                    const int n = nq4[0] + nq4[1] + nq4[2] + nq4[3];
+                    const uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
                     uint32_t key[NI], blk[NI];
-                    const uint32_t vm = load_items(items, n, key, blk, lane);
+                    const uint32_t vm = load_union(lst, nq4, key, blk, lane);
                     uint32_t sel = vm;
                     if (n > p.k_sel) {
                         float th;
