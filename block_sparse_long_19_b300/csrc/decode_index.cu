@@ -176,6 +176,7 @@ struct ScanParams {
     int k_sel;
     uint2 *cand;               // [B, nchunk, k_sel]
     int32_t *cnt;              // [B, nchunk]
+    uint32_t *thr;             // [B] running max of the chunks' (budget-1)-th best key
     int32_t *status;
 };
 
@@ -260,10 +261,18 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     const SelectRule rule = cta_select<SCAN_THREADS>(
         n, p.k_sel, [&](int i) { return sc[i]; },
         [&](int i) { return static_cast<uint32_t>(b0 + i); }, hist, ctl);
-    if (threadIdx.x == 0) ctl[3] = 0;
+    // This chunk holds budget-1 blocks whose keys are >= rule.thr_key, so the
+    // sequence's (budget-1)-th best key is >= it too: publish it.  Candidates
+    // below the largest bound published so far can never be selected.
+    if (threadIdx.x == 0) {
+        const uint32_t old = atomicMax(&p.thr[s], rule.thr_key);
+        ctl[7] = static_cast<int>(max(old, rule.thr_key));
+        ctl[3] = 0;
+    }
     __syncthreads();
+    const uint32_t bound = static_cast<uint32_t>(ctl[7]);
     for (int i = threadIdx.x; i < n; i += SCAN_THREADS) {
-        if (selected(rule, sc[i], static_cast<uint32_t>(b0 + i))) {
+        if (selected(rule, sc[i], static_cast<uint32_t>(b0 + i)) && f2key(sc[i]) >= bound) {
             const int pos = atomicAdd(&ctl[3], 1);
             if (pos < p.k_sel)
                 out[pos] = make_uint2(__float_as_uint(sc[i]), static_cast<uint32_t>(b0 + i));
@@ -271,7 +280,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-        if (ctl[3] != p.k_sel) report(p.status, QSA_ERR_DEVICE_CHECK);
+        if (ctl[3] > p.k_sel) report(p.status, QSA_ERR_DEVICE_CHECK);
         *cnt_out = min(ctl[3], p.k_sel);
     }
 }
@@ -284,6 +293,7 @@ struct MergeParams {
     int budget;
     const uint2 *cand;
     const int32_t *cnt;
+    const uint32_t *thr;  // [B] lower bound of the (budget-1)-th best key (null: none)
     int32_t *idx;   // [B, budget]
     int32_t *status;
 };
@@ -315,6 +325,7 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
     __syncthreads();
     const int slots = p.nchunk * p.k_sel;
     const uint2 *src = p.cand + static_cast<int64_t>(s) * p.nchunk * p.k_sel;
+    const uint32_t bound = p.thr ? p.thr[s] : 0u;
     constexpr int U = 8;
     for (int base = threadIdx.x; base < slots; base += MERGE_THREADS * U) {
         uint2 it[U];
@@ -326,7 +337,10 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
             if (j < slots) {
                 const int ch = j / p.k_sel;
                 ok[u] = (j - ch * p.k_sel) < offs[ch];
-                if (ok[u]) it[u] = src[j];
+                if (ok[u]) {
+                    it[u] = src[j];
+                    ok[u] = f2key(__uint_as_float(it[u].x)) >= bound;
+                }
             }
         }
 #pragma unroll
@@ -417,6 +431,7 @@ size_t decode_ws_bytes(int batch, int64_t max_ctx, int budget, int sms) {
     size_t b = 0;
     b += align256(static_cast<size_t>(batch) * pl.nchunk * k_sel * sizeof(uint2));   // cand
     b += align256(static_cast<size_t>(batch) * pl.nchunk * sizeof(int32_t));         // cnt
+    b += align256(static_cast<size_t>(batch) * sizeof(uint32_t));                    // thr
     b += align256(static_cast<size_t>(batch) * budget * sizeof(int32_t));            // idx
     b += align256(static_cast<size_t>(batch) * pl.nsplit * kHQ * kD * sizeof(float)); // part_o
     b += align256(static_cast<size_t>(batch) * pl.nsplit * kHQ * sizeof(float));      // part_lse
@@ -433,8 +448,12 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
     uint2 *cand = reinterpret_cast<uint2 *>(base);
     base += align256(static_cast<size_t>(batch) * plan.nchunk * k_alloc * sizeof(uint2));
     int32_t *cnt = reinterpret_cast<int32_t *>(base);
+    base += align256(static_cast<size_t>(batch) * plan.nchunk * sizeof(int32_t));
+    uint32_t *thr = reinterpret_cast<uint32_t *>(base);
     cudaError_t e;
     if (k_sel > 0) {
+        e = cudaMemsetAsync(thr, 0, static_cast<size_t>(batch) * sizeof(uint32_t), stream);
+        if (e != cudaSuccess) return e;
         dx::ScanParams sp;
         sp.qi = qi;
         sp.w = w;
@@ -446,6 +465,7 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
         sp.k_sel = k_sel;
         sp.cand = cand;
         sp.cnt = cnt;
+        sp.thr = thr;
         sp.status = status;
         const int smem = static_cast<int>(plan.chunk * 4 + 256 * 4 + 32);
         e = cudaFuncSetAttribute(dx::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -463,6 +483,7 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
     mp.budget = budget;
     mp.cand = cand;
     mp.cnt = cnt;
+    mp.thr = k_sel > 0 ? thr : nullptr;
     mp.idx = idx_out;
     mp.status = status;
     const int smem = dx::MAX_NCHUNK * dx::MAX_SEL * 8 + kMaxBudget * 8 + 256 * 4 + 8 * 4 +

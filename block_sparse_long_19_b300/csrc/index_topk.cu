@@ -37,13 +37,12 @@ namespace ix {
 constexpr int TQ = 64;               // query tokens per tile
 constexpr int NCOL = TQ * kHI;       // 256 MMA columns (token-major, head-minor)
 constexpr int TB = 128;              // block keys per block tile (MMA M)
-constexpr int NSTAGE = 3;            // kblk tile ring
+constexpr int NSTAGE = 2;            // kblk tile ring
 constexpr int CAP = 1024;            // candidate slots per token (32 per lane)
 constexpr int SUB = CAP / 4;         // per-warp sub-list of a token (one per TMEM lane quarter)
 constexpr int KSTEPS = kDI / 16;     // 8 MMAs of K = 16
 constexpr int NEPI = 8;              // epilogue warps
 constexpr int THREADS = (4 + NEPI) * 32;
-constexpr int SORTN = 512;           // sort buffer per epilogue warp (>= budget-1)
 
 constexpr uint32_t IDESC = idesc_bf16_f32(TB, NCOL);
 
@@ -51,12 +50,13 @@ constexpr int SQ_BYTES = 2 * NCOL * 128;     // two 64-wide K halves, 128-B rows
 constexpr int SK_BYTES = 2 * TB * 128;
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + SQ_BYTES;
-constexpr int OFF_SORT = OFF_K + NSTAGE * SK_BYTES;
-constexpr int OFF_HIST = OFF_SORT + NEPI * SORTN * 8;
+constexpr int OFF_STAGE = OFF_K + NSTAGE * SK_BYTES;   // per epilogue warp: one candidate union
+constexpr int OFF_HIST = OFF_STAGE + NEPI * CAP * 8;
 constexpr int OFF_W = OFF_HIST + NEPI * 256 * 4;
 constexpr int OFF_THETA = OFF_W + TQ * 4 * 4;
 constexpr int OFF_CNT = OFF_THETA + TQ * 4;  // [4 quarters][TQ] sub-list counts
-constexpr int OFF_BAR = OFF_CNT + 4 * TQ * 4;
+constexpr int OFF_FLAG = OFF_CNT + 4 * TQ * 4;  // [2 halves][2 parities] token masks
+constexpr int OFF_BAR = OFF_FLAG + 16;
 constexpr int NBAR = 2 * NSTAGE + 2 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -75,8 +75,19 @@ struct Params {
     int32_t *status;
 };
 
-__device__ __forceinline__ void named_bar(int id, int n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+// Barrier among the 4 epilogue warps of one token half that is also a vote:
+// every thread gets the OR of all `fail` flags, so the warps of a half always
+// leave together (a warp that left alone would strand the others at the
+// next barrier; every wait before a barrier is bounded).
+__device__ __forceinline__ bool group_sync_fail(int id, bool fail) {
+    int r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.b32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, 128, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(fail ? 1 : 0), "r"(id)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ int num_btiles(int64_t L, int q) {
@@ -89,47 +100,270 @@ __device__ __forceinline__ int num_btiles(int64_t L, int q) {
 // A token's candidate list is 4 sub-lists of SUB entries, one per epilogue
 // warp of its half (the warp that owns TMEM lane quarter q appends to
 // sub-list q with a warp-private count, so appending needs neither atomics
-// nor shuffles).  Entries are (score bits, block).  For selection the union
-// is loaded into registers as (order-preserving key, block): item i of a
-// lane is entry (i % 8) * 32 + lane of sub-list i / 8.
-constexpr int NI = CAP / 32;
+// nor shuffles).  Entries are (score bits, block).  For selection a warp
+// copies the union into its shared-memory staging buffer (as order keys) and
+// works from there; staged entry i belongs to sub-list i / SUB.
 constexpr int KEEP_MAX = CAP - 2 * TB;  // a lower-bound compaction must keep at most this many
 
-__device__ __forceinline__ uint32_t load_union(const uint2 *lst, const int (&n)[4],
-                                               uint32_t (&key)[NI], uint32_t (&blk)[NI], int lane) {
-    uint32_t vm = 0;
+// Visit every staged slot: f(i, valid) with i = q*SUB + e, the loop fully
+// unrolled so q is a compile-time constant (n[q] stays in a register).
+template <typename F>
+__device__ __forceinline__ void for_staged(const int (&n)[4], int lane, F f) {
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-        const int q = i >> 3;
-        const int e = (i & 7) * 32 + lane;
-        uint2 it = make_uint2(0u, 0u);
-        if (e < n[q]) {
-            it = lst[q * SUB + e];
-            vm |= 1u << i;
-        }
-        key[i] = f2key(__uint_as_float(it.x));
-        blk[i] = it.y;
+    for (int c = 0; c < CAP / 32; ++c) {
+        const int q = c / (SUB / 32);
+        const int e = (c % (SUB / 32)) * 32 + lane;
+        f(q * SUB + e, e < n[q]);
     }
-    __syncwarp();  // every lane's reads are done before anyone rewrites the list
-    return vm;
 }
 
-// Write the items whose bit is set in `sel` back, dealt round-robin over the
-// 4 sub-lists; returns the total kept (sub-list q then holds (kept+3-q)/4).
-__device__ __forceinline__ int store_union(uint2 *lst, const uint32_t (&key)[NI],
-                                           const uint32_t (&blk)[NI], uint32_t sel, int lane) {
-    int out = 0;
+// Copy a token's 4 sub-lists into this warp's staging buffer with plain
+// loads (all independent, so they overlap), converting scores to keys.
+__device__ __forceinline__ void fetch_union(const uint2 *__restrict__ lst, const int (&n)[4],
+                                            uint2 *__restrict__ stage, int lane) {
+    // 8 loads in flight before any of them is stored
 #pragma unroll
-    for (int i = 0; i < NI; ++i) {
-        const bool keep = (sel >> i) & 1u;
-        const unsigned ball = __ballot_sync(0xFFFFFFFFu, keep);
-        if (keep) {
+    for (int g = 0; g < CAP / 256; ++g) {
+        uint2 it[8];
+        bool v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = g * 8 + u;
+            const int q = c / (SUB / 32);
+            const int e = (c % (SUB / 32)) * 32 + lane;
+            v[u] = e < n[q];
+            it[u] = v[u] ? __ldcg(lst + q * SUB + e) : make_uint2(0u, 0u);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int c = g * 8 + u;
+            const int q = c / (SUB / 32);
+            const int e = (c % (SUB / 32)) * 32 + lane;
+            if (v[u]) stage[q * SUB + e] = make_uint2(f2key(__uint_as_float(it[u].x)), it[u].y);
+        }
+    }
+    __syncwarp();
+}
+
+// After a fetch: score bits -> order-preserving keys, in place (x field).
+__device__ __forceinline__ void stage_to_keys(uint2 *stage, const int (&n)[4], int lane) {
+    for_staged(n, lane, [&](int i, bool v) {
+        if (v) stage[i].x = f2key(__uint_as_float(stage[i].x));
+    });
+    __syncwarp();
+}
+
+// Warp radix over the staged items (same contract as warp_radix in
+// qsa_select.cuh).  NEG ranks ~block instead of the key; `tie` restricts the
+// items to those whose key equals tie_key.
+template <bool NEG, bool TIE>
+__device__ __forceinline__ RadixOut warp_radix_staged(const uint2 *stage, const int (&n)[4], uint32_t tie_key,
+                                                      int k, int max_passes, uint32_t *hist, int lane) {
+    auto val = [&](int i) { return NEG ? ~stage[i].y : stage[i].x; };
+    auto use = [&](int i, bool v) { return v && (!TIE || stage[i].x == tie_key); };
+    uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+    int nv = 0;
+    for_staged(n, lane, [&](int i, bool v) {
+        if (use(i, v)) {
+            const uint32_t x = val(i);
+            mx = max(mx, x);
+            mn = min(mn, x);
+            ++nv;
+        }
+    });
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+    nv = __reduce_add_sync(0xFFFFFFFFu, nv);
+    RadixOut r;
+    r.krem = k;
+    if (mx == mn) {
+        r.thr = mx;
+        r.eq = nv;
+        r.lo = 0;
+        return r;
+    }
+    const int hi = 32 - __clz(mx ^ mn);
+    unsigned long long prefix = hi >= 32 ? 0ull : (static_cast<unsigned long long>(mx >> hi) << hi);
+    int lo = hi;
+    int eq = nv;
+    for (int pass = 0; pass < max_passes && lo > 0; ++pass) {
+        const int w = lo >= 8 ? 8 : lo;
+        lo -= w;
+        const uint32_t dmask = (1u << w) - 1u;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) hist[lane * 8 + b] = 0u;
+        __syncwarp();
+        const unsigned long long want = prefix >> (lo + w);
+        for_staged(n, lane, [&](int i, bool v) {
+            if (use(i, v)) {
+                const uint32_t x = val(i);
+                if ((static_cast<unsigned long long>(x) >> (lo + w)) == want) atomicAdd(&hist[(x >> lo) & dmask], 1u);
+            }
+        });
+        __syncwarp();
+        uint32_t cnt[8];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            cnt[b] = hist[255 - (lane * 8 + b)];
+            sum += cnt[b];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        const uint32_t excl = incl - sum;
+        const bool mine = excl < static_cast<uint32_t>(r.krem) && static_cast<uint32_t>(r.krem) <= incl;
+        int digit = 0;
+        uint32_t above = 0, e = 0;
+        if (mine) {
+            uint32_t acc = excl;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) {
+                if (acc + cnt[b] >= static_cast<uint32_t>(r.krem)) {
+                    digit = 255 - (lane * 8 + b);
+                    above = acc;
+                    e = cnt[b];
+                    break;
+                }
+                acc += cnt[b];
+            }
+        }
+        const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1;
+        digit = __shfl_sync(0xFFFFFFFFu, digit, src);
+        above = __shfl_sync(0xFFFFFFFFu, above, src);
+        e = __shfl_sync(0xFFFFFFFFu, e, src);
+        r.krem -= static_cast<int>(above);
+        eq = static_cast<int>(e);
+        prefix |= static_cast<unsigned long long>(digit) << lo;
+        __syncwarp();
+        if (eq == r.krem) break;
+    }
+    r.thr = static_cast<uint32_t>(prefix);
+    r.eq = eq;
+    r.lo = lo;
+    return r;
+}
+
+struct StagedRule {
+    uint32_t thr_key;
+    uint32_t thr_nblk;
+    int by_bucket;  // 1: keep key >= thr_key
+};
+
+// staged items hold (key, block) after stage_to_keys
+__device__ __forceinline__ bool staged_keep(const StagedRule &r, uint2 it) {
+    if (r.by_bucket) return it.x >= r.thr_key;
+    return it.x > r.thr_key || (it.x == r.thr_key && ~it.y >= r.thr_nblk);
+}
+
+// Exact k best (key desc, block asc) of the staged union, plus the streaming
+// threshold a later (higher-index) block must reach: s >= *theta.
+__device__ __forceinline__ StagedRule staged_select_exact(const uint2 *stage, const int (&n)[4], int k,
+                                                          uint32_t *hist, int lane, float *theta) {
+    const RadixOut r = warp_radix_staged<false, false>(stage, n, 0u, k, 8, hist, lane);
+    StagedRule rule;
+    rule.thr_key = r.thr;
+    rule.thr_nblk = 0;
+    rule.by_bucket = 1;
+    if (r.eq == r.krem) {
+        *theta = r.lo == 0 ? nextafterf(key2f(r.thr), INFINITY) : key2f(r.thr);
+        return rule;
+    }
+    // the k-th key is exactly r.thr; take the r.krem ties with the lowest blocks
+    const RadixOut r2 = warp_radix_staged<true, true>(stage, n, r.thr, r.krem, 8, hist, lane);
+    rule.by_bucket = 0;
+    rule.thr_nblk = r2.thr;
+    *theta = nextafterf(key2f(r.thr), INFINITY);
+    return rule;
+}
+
+// Write the staged items that the rule keeps back to the global list (keys
+// turned back into score bits), dealt round-robin over the 4 sub-lists;
+// returns the number kept.
+__device__ __forceinline__ int restore_union(uint2 *lst, const uint2 *stage, const int (&n)[4],
+                                             const StagedRule &rule, int lane) {
+    int out = 0;
+    for_staged(n, lane, [&](int i, bool v) {
+        const uint2 it = stage[i];
+        const bool kp = v && staged_keep(rule, it);
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, kp);
+        if (kp) {
             const int r = out + __popc(ball & ((1u << lane) - 1u));
-            lst[(r & 3) * SUB + (r >> 2)] = make_uint2(__float_as_uint(key2f(key[i])), blk[i]);
+            lst[(r & 3) * SUB + (r >> 2)] = make_uint2(__float_as_uint(key2f(it.x)), it.y);
         }
         out += __popc(ball);
-    }
+    });
     return out;
+}
+
+// Stable LSD radix sort (warp) of m <= 512 64-bit items by their high word
+// (the block index, < 2^(8*passes)); a and b are two 512-entry buffers, the
+// result ends in a.  hist: 256 words of this warp.
+__device__ __forceinline__ void warp_sort_by_block(unsigned long long *a, unsigned long long *b, int m,
+                                                   int passes, uint32_t *hist, int lane) {
+    for (int pass = 0; pass < passes; ++pass) {
+        const int shift = 32 + 8 * pass;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) hist[lane * 8 + d] = 0u;
+        __syncwarp();
+        for (int i = lane; i < m; i += 32) atomicAdd(&hist[(a[i] >> shift) & 255], 1u);
+        __syncwarp();
+        // exclusive scan of the 256 counts (lane owns 8 consecutive digits)
+        uint32_t c8[8], sum = 0;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            c8[d] = hist[lane * 8 + d];
+            sum += c8[d];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += t;
+        }
+        uint32_t run = incl - sum;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            hist[lane * 8 + d] = run;
+            run += c8[d];
+        }
+        __syncwarp();
+        // stable scatter, 32 items at a time in order
+        for (int i0 = 0; i0 < m; i0 += 32) {
+            const int i = i0 + lane;
+            const bool v = i < m;
+            const unsigned long long x = v ? a[i] : 0ull;
+            const unsigned d = v ? static_cast<unsigned>((x >> shift) & 255) : 256u + lane;
+            const unsigned peers = __match_any_sync(0xFFFFFFFFu, d);
+            const uint32_t base = v ? hist[d] : 0u;
+            __syncwarp();
+            if (v) {
+                b[base + __popc(peers & ((1u << lane) - 1u))] = x;
+                if ((peers & ((1u << lane) - 1u)) == 0u) hist[d] = base + __popc(peers);
+            }
+            __syncwarp();
+        }
+        unsigned long long *t = a;
+        a = b;
+        b = t;
+    }
+    if (passes & 1) {  // result is in the second buffer: copy back
+        for (int i = lane; i < m; i += 32) b[i] = a[i];
+        __syncwarp();
+    }
+}
+
+// Store only where pred holds, as a predicated instruction (no branch).  No
+// "memory" clobber: the compiler may move other loads across it (ordering
+// against the list readers comes from the proxy fence and group barrier).
+__device__ __forceinline__ void st_global_pred(uint2 *addr, uint2 v, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.v2.b32 [%1], {%2, %3};\n\t}" ::"r"(
+            pred ? 1 : 0),
+        "l"(addr), "r"(v.x), "r"(v.y));
 }
 
 template <bool DENSE>
@@ -141,11 +375,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = smem + OFF_Q;
     uint8_t *sK = smem + OFF_K;
-    unsigned long long *sSort = reinterpret_cast<unsigned long long *>(smem + OFF_SORT);
+    uint2 *sStage = reinterpret_cast<uint2 *>(smem + OFF_STAGE);
     uint32_t *sHist = reinterpret_cast<uint32_t *>(smem + OFF_HIST);
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sTheta = reinterpret_cast<float *>(smem + OFF_THETA);
     int *sCnt = reinterpret_cast<int *>(smem + OFF_CNT);  // sCnt[q * TQ + tl]
+    unsigned *sFlag = reinterpret_cast<unsigned *>(smem + OFF_FLAG);  // sFlag[half * 2 + parity]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *full = bars;
     uint64_t *empty = bars + NSTAGE;
@@ -171,6 +406,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[i], NEPI);
         }
         sMisc[1] = 0;
+        for (int i = 0; i < 4; ++i) sFlag[i] = 0u;
         fence_barrier_init();
     }
     if (warp == 2) {
@@ -262,17 +498,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int half = e >> 2;       // token half: columns [half*128, half*128+128)
         const int tid_h = quarter * 32 + lane;
         uint32_t *hist = sHist + e * 256;
-        unsigned long long *sortb = sSort + e * SORTN;
+        uint2 *stage = sStage + e * CAP;
+        const int gbar = 1 + half;  // hardware barrier id of this half
         const unsigned ltmask = (1u << lane) - 1u;
         // this warp's sub-lists: token tl's at sub[tl * CAP]
         uint2 *sub = p.cand + static_cast<int64_t>(blockIdx.x) * TQ * CAP + quarter * SUB;
         uint32_t acc = 0;
         bool ok = true;
-        for (int kk = blockIdx.x; kk < p.nq && ok; kk += gridDim.x) {
+        for (int kk = blockIdx.x; kk < p.nq; kk += gridDim.x) {
             const int q = p.nq - 1 - kk;
             const int64_t t0 = static_cast<int64_t>(q) * TQ;
             const int nbt = num_btiles(p.L, q);
-            named_bar(1 + half, 128);
+            if (group_sync_fail(gbar, !ok || sMisc[1] != 0)) { ok = false; break; }
             if (tid_h < 32) {
                 const int tl = half * 32 + tid_h;
                 const int64_t t = t0 + tl;
@@ -286,66 +523,81 @@ __global__ void __launch_bounds__(THREADS, 1)
                     sW[tl * 4 + h] = wv;
                 }
             }
-            named_bar(1 + half, 128);
+            if (group_sync_fail(gbar, false)) { ok = false; break; }
             const bool tile_all_in = (t0 + TQ <= p.L);
             const int64_t c_min = t0 / kBlock;
             for (int j = 0; j < nbt; ++j) {
                 const uint32_t buf = acc & 1;
                 const uint32_t use = acc >> 1;
-                if (!mbar_wait(&tfull[buf], use & 1)) { ok = false; break; }
+                if (ok && !mbar_wait(&tfull[buf], use & 1)) ok = false;
+                if (!ok) {  // skip the work, keep taking part in the barriers
+                    ++acc;
+                    if constexpr (!DENSE) {
+                        if (group_sync_fail(gbar, true)) break;
+                    }
+                    continue;
+                }
                 tc_fence_after();
                 const int64_t b = static_cast<int64_t>(j) * TB + quarter * 32 + lane;
                 const bool masked = !(tile_all_in && (static_cast<int64_t>(j) * TB + TB <= c_min));
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        buf * NCOL + half * 128;
-                uint32_t ra[32], rb[32];
-                tmem_ld32(tbase, ra);
-                tmem_wait32(ra);
+                // 8 chunks of 4 tokens (16 columns), the load of chunk ch+1 in
+                // flight while chunk ch is scored
+                uint32_t ra[16], rb[16];
+                tmem_ld16(tbase, ra);
+                tmem_wait16(ra);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t(&cur)[32] = (ch & 1) ? rb : ra;
-                    uint32_t(&nxt)[32] = (ch & 1) ? ra : rb;
-                    if (ch < 3) tmem_ld32(tbase + (ch + 1) * 32, nxt);  // overlaps the math below
-                    const int tl0 = half * 32 + ch * 8;
-                    float th[8];
-                    *reinterpret_cast<float4 *>(&th[0]) = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
-                    *reinterpret_cast<float4 *>(&th[4]) = *reinterpret_cast<const float4 *>(&sTheta[tl0 + 4]);
-                    int cnt8[8];
-                    if constexpr (!DENSE) {
-                        *reinterpret_cast<int4 *>(&cnt8[0]) = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0]);
-                        *reinterpret_cast<int4 *>(&cnt8[4]) = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0 + 4]);
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t(&cur)[16] = (ch & 1) ? rb : ra;
+                    uint32_t(&nxt)[16] = (ch & 1) ? ra : rb;
+                    if (ch < 7) tmem_ld16(tbase + (ch + 1) * 16, nxt);
+                    const int tl0 = half * 32 + ch * 4;
+                    const float4 th = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
+                    const float thv[4] = {th.x, th.y, th.z, th.w};
+                    int4 c4;
+                    if constexpr (!DENSE) c4 = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0]);
+                    int cnt4[4] = {c4.x, c4.y, c4.z, c4.w};
+                    float sv[4];
+#pragma unroll
+                    for (int tk = 0; tk < 4; ++tk) {
+                        const float4 wv = *reinterpret_cast<const float4 *>(&sW[(tl0 + tk) * 4]);
+                        // the first product is added to +0 so the sum is never -0
+                        float sc = fmaf(wv.x, fmaxf(__uint_as_float(cur[4 * tk + 0]), 0.f), 0.0f);
+                        sc = fmaf(wv.y, fmaxf(__uint_as_float(cur[4 * tk + 1]), 0.f), sc);
+                        sc = fmaf(wv.z, fmaxf(__uint_as_float(cur[4 * tk + 2]), 0.f), sc);
+                        sv[tk] = fmaf(wv.w, fmaxf(__uint_as_float(cur[4 * tk + 3]), 0.f), sc);
                     }
 #pragma unroll
-                    for (int tk = 0; tk < 8; ++tk) {
+                    for (int tk = 0; tk < 4; ++tk) {
                         const int tl = tl0 + tk;
-                        const float4 wv = *reinterpret_cast<const float4 *>(&sW[tl * 4]);
-                        // the first product is added to +0 so the sum is never -0
-                        float s = fmaf(wv.x, fmaxf(__uint_as_float(cur[4 * tk + 0]), 0.f), 0.0f);
-                        s = fmaf(wv.y, fmaxf(__uint_as_float(cur[4 * tk + 1]), 0.f), s);
-                        s = fmaf(wv.z, fmaxf(__uint_as_float(cur[4 * tk + 2]), 0.f), s);
-                        s = fmaf(wv.w, fmaxf(__uint_as_float(cur[4 * tk + 3]), 0.f), s);
                         const int64_t t = t0 + tl;
-                        bool valid = true;
-                        if (masked) valid = (t < p.L) && (b < t / kBlock);
+                        const bool valid = !masked || ((t < p.L) && (b < (t >> 2)));
                         if constexpr (DENSE) {
-                            if (valid) p.dense[t * p.dense_ld + b] = s;
+                            if (valid) p.dense[t * p.dense_ld + b] = sv[tk];
                         } else {
                             // a block enters the token's list when s >= its threshold:
                             // position from a ballot, no branch, no atomic
-                            const bool pass = valid && (s >= th[tk]);
+                            const bool pass = valid && (sv[tk] >= thv[tk]);
                             const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
-                            const int pos = cnt8[tk] + __popc(m & ltmask);
-                            if (pass && pos < SUB)
-                                sub[static_cast<int64_t>(tl) * CAP + pos] =
-                                    make_uint2(__float_as_uint(s), static_cast<uint32_t>(b));
-                            cnt8[tk] += __popc(m);
+                            const int pos = cnt4[tk] + __popc(m & ltmask);
+                            st_global_pred(sub + static_cast<int64_t>(tl) * CAP + pos,
+                                           make_uint2(__float_as_uint(sv[tk]), static_cast<uint32_t>(b)),
+                                           pass && pos < SUB);
+                            cnt4[tk] += __popc(m);
                         }
                     }
                     if constexpr (!DENSE) {
-                        *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0]) = *reinterpret_cast<const int4 *>(&cnt8[0]);
-                        *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0 + 4]) = *reinterpret_cast<const int4 *>(&cnt8[4]);
+                        *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0]) =
+                            make_int4(cnt4[0], cnt4[1], cnt4[2], cnt4[3]);
+                        // lists that might overflow on the next tile get flagged
+                        unsigned fl = 0;
+#pragma unroll
+                        for (int tk = 0; tk < 4; ++tk)
+                            if (cnt4[tk] > SUB - 32) fl |= 1u << (ch * 4 + tk);
+                        if (fl && lane == 0) atomicOr(&sFlag[half * 2 + (acc & 1)], fl);
                     }
-                    if (ch < 3) tmem_wait32(nxt);
+                    if (ch < 7) tmem_wait16(nxt);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -353,9 +605,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                 ++acc;
                 if constexpr (!DENSE) {
                     // lists that might overflow on the next tile are cut back
-                    named_bar(1 + half, 128);
+                    if (group_sync_fail(gbar, sMisc[1] != 0)) { ok = false; break; }
+                    const unsigned flags = sFlag[half * 2 + ((acc - 1) & 1)];
                     for (int i = 0; i < 8; ++i) {
                         const int tl = half * 32 + quarter + 4 * i;
+                        if (!((flags >> (tl - half * 32)) & 1u)) continue;
                         int n[4];
 #pragma unroll
                         for (int q = 0; q < 4; ++q) n[q] = sCnt[q * TQ + tl];
@@ -365,31 +619,26 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int q = 0; q < 4; ++q) n[q] = min(n[q], SUB);
                             uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
-                            uint32_t key[NI], blk[NI];
-                            const uint32_t vm = load_union(lst, n, key, blk, lane);
+                            fetch_union(lst, n, stage, lane);
                             // cheap pass: a bucket bound 16 bits below the shared prefix
-                            const RadixOut r = warp_radix<NI>(key, vm, p.k_sel, 2, hist, lane);
-                            uint32_t sel = 0;
+                            const RadixOut r = warp_radix_staged<false, false>(stage, n, 0u, p.k_sel, 2, hist, lane);
                             float th;
-                            if ((p.k_sel - r.krem) + r.eq <= KEEP_MAX) {
-#pragma unroll
-                                for (int q2 = 0; q2 < NI; ++q2)
-                                    if (((vm >> q2) & 1u) && key[q2] >= r.thr) sel |= 1u << q2;
+                            StagedRule rule{r.thr, 0u, 1};
+                            if ((p.k_sel - r.krem) + r.eq <= KEEP_MAX)
                                 th = r.lo == 0 ? nextafterf(key2f(r.thr), INFINITY) : key2f(r.thr);
-                            } else {
-                                sel = warp_select_exact<NI>(key, blk, vm, p.k_sel, hist, lane, &th);
-                            }
-                            const int kept = store_union(lst, key, blk, sel, lane);
+                            else
+                                rule = staged_select_exact(stage, n, p.k_sel, hist, lane, &th);
+                            const int kept = restore_union(lst, stage, n, rule, lane);
                             if (lane < 4) sCnt[lane * TQ + tl] = (kept + 3 - lane) / 4;
                             if (lane == 0) sTheta[tl] = th;
                             __syncwarp();
                         }
                     }
-                    named_bar(1 + half, 128);
+                    if (group_sync_fail(gbar, !ok)) { ok = false; break; }
+                    if (tid_h == 0) sFlag[half * 2 + ((acc - 1) & 1)] = 0u;
                 }
-                if (sMisc[1]) { ok = false; break; }
             }
-            if (!ok) break;
+            if (!ok) continue;  // the next tile-start barrier takes everyone out
             if constexpr (!DENSE) {
                 // ---- finalize: one warp per token
                 for (int i = 0; i < 8; ++i) {
@@ -402,48 +651,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int q = 0; q < 4; ++q) nq4[q] = min(sCnt[q * TQ + tl], SUB);
                     const int n = nq4[0] + nq4[1] + nq4[2] + nq4[3];
                     const uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
-                    uint32_t key[NI], blk[NI];
-                    const uint32_t vm = load_union(lst, nq4, key, blk, lane);
-                    uint32_t sel = vm;
+                    fetch_union(lst, nq4, stage, lane);
+                    StagedRule rule{0u, 0u, 1};
                     if (n > p.k_sel) {
                         float th;
-                        sel = warp_select_exact<NI>(key, blk, vm, p.k_sel, hist, lane, &th);
+                        rule = staged_select_exact(stage, nq4, p.k_sel, hist, lane, &th);
                     }
-                    // the kept items as (block << 32 | score bits), sorted by block
+                    // kept items -> front of the staging buffer as (block << 32 | score bits),
+                    // in place: every lane has read its item of a chunk before any write
+                    unsigned long long *sortb = reinterpret_cast<unsigned long long *>(stage);
                     int m = 0;
-#pragma unroll
-                    for (int q2 = 0; q2 < NI; ++q2) {
-                        const bool keep = (sel >> q2) & 1u;
-                        const unsigned ball = __ballot_sync(0xFFFFFFFFu, keep);
-                        if (keep) {
-                            const int pos = m + __popc(ball & ((1u << lane) - 1u));
-                            if (pos < SORTN)
-                                sortb[pos] = (static_cast<unsigned long long>(blk[q2]) << 32) |
-                                             __float_as_uint(key2f(key[q2]));
-                        }
+                    for_staged(nq4, lane, [&](int i2, bool v) {
+                        const uint2 it = stage[i2];
+                        const bool kp = v && staged_keep(rule, it);
+                        const unsigned ball = __ballot_sync(0xFFFFFFFFu, kp);
+                        if (kp)
+                            sortb[m + __popc(ball & ((1u << lane) - 1u))] =
+                                (static_cast<unsigned long long>(it.y) << 32) | __float_as_uint(key2f(it.x));
                         m += __popc(ball);
-                    }
-                    if (m > SORTN) { report(p.status, QSA_ERR_DEVICE_CHECK); m = SORTN; }
-                    int P2 = 32;
-                    while (P2 < m) P2 <<= 1;
-                    for (int ii = m + lane; ii < P2; ii += 32) sortb[ii] = ~0ull;
-                    __syncwarp();
-                    for (int kb = 2; kb <= P2; kb <<= 1) {
-                        for (int jb = kb >> 1; jb > 0; jb >>= 1) {
-                            for (int ii = lane; ii < P2; ii += 32) {
-                                const int ix = ii ^ jb;
-                                if (ix > ii) {
-                                    const unsigned long long a = sortb[ii], bb = sortb[ix];
-                                    const bool up = (ii & kb) == 0;
-                                    if ((a > bb) == up) {
-                                        sortb[ii] = bb;
-                                        sortb[ix] = a;
-                                    }
-                                }
-                            }
-                            __syncwarp();
-                        }
-                    }
+                        __syncwarp();
+                    });
+                    if (m > 512) { report(p.status, QSA_ERR_DEVICE_CHECK); m = 512; }
+                    // order by block: enough 8-bit digits to cover blocks < c
+                    const int passes = c < (1 << 8) ? 1 : (c < (1 << 16) ? 2 : (c < (1 << 24) ? 3 : 4));
+                    warp_sort_by_block(sortb, sortb + 512, m, passes, hist, lane);
                     int32_t *row = p.idx + t * p.budget;
                     float *srow = p.score ? p.score + t * p.budget : nullptr;
                     for (int ii = lane; ii < p.budget; ii += 32) {
