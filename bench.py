@@ -42,8 +42,9 @@ WORKLOADS = {
     "qsa_1m": (1 << 20, 512, 4, 8, 1 << 20, 4),
     "qsa_128k": (131072, 512, 2, 64, 262144, 3),
     "qsa_small": (32768, 512, 1, 4, 65536, 5),
-    # profiling case: K/V (268 MB) larger than L2, a few GB on the device
+    # profiling cases: inputs larger than L2, a few GB on the device
     "prof_128k": (131072, 512, 2, 1, 65536, 3),
+    "prof_decode": (4096, 512, 6, 8, 131072, 6),
 }
 
 
@@ -316,6 +317,54 @@ def run_reference(args):
     }), flush=True)
 
 
+# ----------------------------------------------------------- traffic --
+
+ATTN_SOURCES = ["block_sparse_long_19_b300/csrc/sparse_attn.cu",
+                "block_sparse_long_19_b300/csrc/qsa_common.cuh"]
+
+
+def attn_sources_digest() -> str:
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in ATTN_SOURCES:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()
+
+
+def attn_traffic(wl) -> int | None:
+    """DRAM bytes (read + write) of one prefill-attention launch, from the
+    committed ncu capture of this workload -- only while the kernel sources
+    are the ones that capture measured (else None)."""
+    path = os.path.join(ROOT, "profiles", "attn_prefill_traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        pj = json.load(open(path))
+    except Exception:
+        return None
+    if pj.get("source_sha256") != attn_sources_digest() or pj.get("L") != wl.L:
+        return None
+    return int(pj["dram_bytes_read"] + pj["dram_bytes_write"])
+
+
+# ------------------------------------------------------------- ranks --
+
+def job_time_ms(ms: float, pg=None) -> float:
+    """Whole-job time of a step: the slowest rank's (replicas run
+    independently, so the job is done when the last one is)."""
+    if pg is None:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, world: int, ms: float) -> float:
+    """Aggregate throughput: every rank's tokens over the whole-job time."""
+    return tokens_per_rank * world / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ main --
 
 def main():
@@ -380,13 +429,8 @@ def main():
     idx_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(K))
     attn_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(K))
     dec_ms = statistics.mean(evs[i][2].elapsed_time(evs[i][3]) for i in range(K))
-    if pg:
-        t = torch.tensor([ms], dtype=torch.float64)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-
-    tokens = (wl.L + wl.B) * world
-    value = tokens / (ms / 1e3)
+    ms = job_time_ms(ms, pg)
+    value = job_tokens_per_s(wl.L + wl.B, world, ms)
 
     hbm = peaks.get("hbm_gbs")
     tc = peaks.get("bf16_tflops")
@@ -397,15 +441,7 @@ def main():
     attn_gbs = attn_bytes / (attn_ms / 1e3) / 1e9
     idx_tflops = wl.index_flops() / (idx_ms / 1e3) / 1e12
     dec_gbs = wl.decode_bytes() / (dec_ms / 1e3) / 1e9
-    traffic = None
-    prof = os.path.join(ROOT, "profiles", "attn_prefill_traffic.json")
-    if os.path.exists(prof):
-        try:
-            pj = json.load(open(prof))
-            if pj.get("L") and pj.get("bytes_per_query"):
-                traffic = int(pj["bytes_per_query"] * wl.L)
-        except Exception:
-            traffic = None
+    traffic = attn_traffic(wl)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
