@@ -269,13 +269,19 @@ def oracle_sample(wl_name: str, target_s: float = 12.0, host_inputs=None) -> dic
 
     cores = O.max_threads()
     n0 = max(2, cores)
-    rows0 = np.sort(pool[:n0])
-    fill(rows0)
-    t0 = time.perf_counter()
-    O.prefill_rows(hb, rows0, budget)
-    dt0 = time.perf_counter() - t0
-    n1 = int(max(n0, min(len(pool), n0 * max(1.0, target_s / max(dt0, 1e-3)))))
-    rows1 = np.sort(pool[n0:n0 + n1]) if n0 + n1 <= len(pool) else np.sort(pool[:n1])
+    # calibrate: two sizes separate the per-row cost from the fixed cost (the
+    # block keys of the whole sequence are recomputed on every call)
+    times = []
+    for mult in (1, 2):
+        rows0 = np.sort(pool[:n0 * mult])
+        fill(rows0)
+        t0 = time.perf_counter()
+        O.prefill_rows(hb, rows0, budget)
+        times.append(time.perf_counter() - t0)
+    per_row = max((times[1] - times[0]) / n0, 1e-6)
+    fixed = max(times[0] - n0 * per_row, 0.0)
+    n1 = int(max(n0, min(len(pool) - 2 * n0, (target_s - fixed) / per_row)))
+    rows1 = np.sort(pool[2 * n0:2 * n0 + n1])
     fill(rows1)
     t1 = time.perf_counter()
     O.prefill_rows(hb, rows1, budget)
