@@ -37,12 +37,17 @@ namespace ix {
 constexpr int TQ = 64;               // query tokens per tile
 constexpr int NCOL = TQ * kHI;       // 256 MMA columns (token-major, head-minor)
 constexpr int TB = 128;              // block keys per block tile (MMA M)
-constexpr int NSTAGE = 2;            // kblk tile ring
-constexpr int CAP = 1024;            // candidate slots per token (32 per lane)
+constexpr int NSTAGE = 3;            // kblk tile ring
+constexpr int CAP = 1024;            // candidate slots per token
 constexpr int SUB = CAP / 4;         // per-warp sub-list of a token (one per TMEM lane quarter)
 constexpr int KSTEPS = kDI / 16;     // 8 MMAs of K = 16
-constexpr int NEPI = 8;              // epilogue warps
+constexpr int NGRP = 4;              // epilogue groups
+constexpr int GTOK = TQ / NGRP;      // 16 tokens (64 TMEM columns) per group
+constexpr int NEPI = 4 * NGRP;       // 16 epilogue warps: group x TMEM lane quarter
+constexpr int GT = 128;              // threads per group
+constexpr int PER = CAP / GT;        // staged items per group thread
 constexpr int THREADS = (4 + NEPI) * 32;
+static_assert(SUB == 2 * GT, "staged item u of a thread is entry (u%2)*GT + tg of sub-list u/2");
 
 constexpr uint32_t IDESC = idesc_bf16_f32(TB, NCOL);
 
@@ -50,13 +55,14 @@ constexpr int SQ_BYTES = 2 * NCOL * 128;     // two 64-wide K halves, 128-B rows
 constexpr int SK_BYTES = 2 * TB * 128;
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + SQ_BYTES;
-constexpr int OFF_STAGE = OFF_K + NSTAGE * SK_BYTES;   // per epilogue warp: one candidate union
-constexpr int OFF_HIST = OFF_STAGE + NEPI * CAP * 8;
-constexpr int OFF_W = OFF_HIST + NEPI * 256 * 4;
+constexpr int OFF_STAGE = OFF_K + NSTAGE * SK_BYTES;  // per group: one staged candidate union
+constexpr int OFF_HIST = OFF_STAGE + NGRP * CAP * 8;
+constexpr int OFF_CTL = OFF_HIST + NGRP * 256 * 4;
+constexpr int OFF_W = OFF_CTL + NGRP * 64 * 4;
 constexpr int OFF_THETA = OFF_W + TQ * 4 * 4;
-constexpr int OFF_CNT = OFF_THETA + TQ * 4;  // [4 quarters][TQ] sub-list counts
-constexpr int OFF_FLAG = OFF_CNT + 4 * TQ * 4;  // [2 halves][2 parities] token masks
-constexpr int OFF_BAR = OFF_FLAG + 16;
+constexpr int OFF_CNT = OFF_THETA + TQ * 4;      // [4 quarters][TQ] sub-list counts
+constexpr int OFF_FLAG = OFF_CNT + 4 * TQ * 4;   // [NGRP groups][2 parities] token masks
+constexpr int OFF_BAR = OFF_FLAG + NGRP * 2 * 4;
 constexpr int NBAR = 2 * NSTAGE + 2 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -75,10 +81,10 @@ struct Params {
     int32_t *status;
 };
 
-// Barrier among the 4 epilogue warps of one token half that is also a vote:
-// every thread gets the OR of all `fail` flags, so the warps of a half always
-// leave together (a warp that left alone would strand the others at the
-// next barrier; every wait before a barrier is bounded).
+// Barrier among the 4 warps (128 threads) of one epilogue group that is also a
+// vote: every thread gets the OR of all `fail` flags, so a group always
+// leaves together (a warp that left alone would strand the others at the next
+// barrier; every wait before a barrier is bounded).
 __device__ __forceinline__ bool group_sync_fail(int id, bool fail) {
     int r;
     asm volatile(
@@ -89,6 +95,9 @@ __device__ __forceinline__ bool group_sync_fail(int id, bool fail) {
         : "memory");
     return r != 0;
 }
+__device__ __forceinline__ void group_bar(int id) {
+    asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
+}
 
 __device__ __forceinline__ int num_btiles(int64_t L, int q) {
     int64_t t_last = static_cast<int64_t>(q) * TQ + TQ - 1;
@@ -98,82 +107,86 @@ __device__ __forceinline__ int num_btiles(int64_t L, int q) {
 }
 
 // A token's candidate list is 4 sub-lists of SUB entries, one per epilogue
-// warp of its half (the warp that owns TMEM lane quarter q appends to
+// warp of its group (the warp that owns TMEM lane quarter q appends to
 // sub-list q with a warp-private count, so appending needs neither atomics
-// nor shuffles).  Entries are (score bits, block).  For selection a warp
-// copies the union into its shared-memory staging buffer (as order keys) and
-// works from there; staged entry i belongs to sub-list i / SUB.
+// nor shuffles).  Entries are (score bits, block).  Selection work on a list
+// is done by the 128 threads of the group together, on a copy in the group's
+// shared staging buffer (as order keys): thread tg holds staged items
+// i = tg + 128 u (u < 8), which is entry (u % 2) * 128 + tg of sub-list u / 2.
 constexpr int KEEP_MAX = CAP - 2 * TB;  // a lower-bound compaction must keep at most this many
 
-// Visit every staged slot: f(i, valid) with i = q*SUB + e, the loop fully
-// unrolled so q is a compile-time constant (n[q] stays in a register).
-template <typename F>
-__device__ __forceinline__ void for_staged(const int (&n)[4], int lane, F f) {
-#pragma unroll
-    for (int c = 0; c < CAP / 32; ++c) {
-        const int q = c / (SUB / 32);
-        const int e = (c % (SUB / 32)) * 32 + lane;
-        f(q * SUB + e, e < n[q]);
-    }
+struct StagedRule {
+    uint32_t thr_key;
+    uint32_t thr_nblk;
+    int by_bucket;  // 1: keep key >= thr_key
+};
+
+__device__ __forceinline__ bool staged_valid(int u, int tg, const int (&n)[4]) {
+    return (u & 1) * GT + tg < n[u >> 1];
 }
 
-// Copy a token's 4 sub-lists into this warp's staging buffer with plain
-// loads (all independent, so they overlap), converting scores to keys.
-__device__ __forceinline__ void fetch_union(const uint2 *__restrict__ lst, const int (&n)[4],
-                                            uint2 *__restrict__ stage, int lane) {
-    // 8 loads in flight before any of them is stored
-#pragma unroll
-    for (int g = 0; g < CAP / 256; ++g) {
-        uint2 it[8];
-        bool v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = g * 8 + u;
-            const int q = c / (SUB / 32);
-            const int e = (c % (SUB / 32)) * 32 + lane;
-            v[u] = e < n[q];
-            it[u] = v[u] ? __ldcg(lst + q * SUB + e) : make_uint2(0u, 0u);
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const int c = g * 8 + u;
-            const int q = c / (SUB / 32);
-            const int e = (c % (SUB / 32)) * 32 + lane;
-            if (v[u]) stage[q * SUB + e] = make_uint2(f2key(__uint_as_float(it[u].x)), it[u].y);
-        }
-    }
-    __syncwarp();
+__device__ __forceinline__ bool staged_keep(const StagedRule &r, uint2 it) {
+    if (r.by_bucket) return it.x >= r.thr_key;
+    return it.x > r.thr_key || (it.x == r.thr_key && ~it.y >= r.thr_nblk);
 }
 
-// After a fetch: score bits -> order-preserving keys, in place (x field).
-__device__ __forceinline__ void stage_to_keys(uint2 *stage, const int (&n)[4], int lane) {
-    for_staged(n, lane, [&](int i, bool v) {
-        if (v) stage[i].x = f2key(__uint_as_float(stage[i].x));
-    });
-    __syncwarp();
+// Copy the 4 sub-lists into the staging buffer (all 8 loads of a thread in
+// flight first), scores turned into order keys.
+__device__ __forceinline__ void group_fetch(const uint2 *__restrict__ lst, const int (&n)[4],
+                                            uint2 *__restrict__ stage, int tg, int bar) {
+    uint2 it[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+        it[u] = staged_valid(u, tg, n) ? __ldcg(lst + tg + GT * u) : make_uint2(0u, 0u);
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+        if (staged_valid(u, tg, n)) stage[tg + GT * u] = make_uint2(f2key(__uint_as_float(it[u].x)), it[u].y);
+    group_bar(bar);
 }
 
-// Warp radix over the staged items (same contract as warp_radix in
-// qsa_select.cuh).  NEG ranks ~block instead of the key; `tie` restricts the
-// items to those whose key equals tie_key.
+// Group radix over the staged items (contract of warp_radix in
+// qsa_select.cuh).  NEG ranks ~block instead of the key; TIE restricts the
+// items to those whose key equals tie_key.  ctl: 16 ints of the group.
 template <bool NEG, bool TIE>
-__device__ __forceinline__ RadixOut warp_radix_staged(const uint2 *stage, const int (&n)[4], uint32_t tie_key,
-                                                      int k, int max_passes, uint32_t *hist, int lane) {
-    auto val = [&](int i) { return NEG ? ~stage[i].y : stage[i].x; };
-    auto use = [&](int i, bool v) { return v && (!TIE || stage[i].x == tie_key); };
+__device__ __forceinline__ RadixOut group_radix(const uint2 *stage, const int (&n)[4], uint32_t tie_key, int k,
+                                                int max_passes, uint32_t *hist, int *ctl, int tg, int bar) {
+    const int lane = tg & 31, gw = tg >> 5;
+    uint32_t v[PER];
+    bool use[PER];
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        const uint2 it = stage[tg + GT * u];
+        use[u] = staged_valid(u, tg, n) && (!TIE || it.x == tie_key);
+        v[u] = NEG ? ~it.y : it.x;
+    }
     uint32_t mx = 0u, mn = 0xFFFFFFFFu;
     int nv = 0;
-    for_staged(n, lane, [&](int i, bool v) {
-        if (use(i, v)) {
-            const uint32_t x = val(i);
-            mx = max(mx, x);
-            mn = min(mn, x);
+#pragma unroll
+    for (int u = 0; u < PER; ++u)
+        if (use[u]) {
+            mx = max(mx, v[u]);
+            mn = min(mn, v[u]);
             ++nv;
         }
-    });
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
     mn = __reduce_min_sync(0xFFFFFFFFu, mn);
     nv = __reduce_add_sync(0xFFFFFFFFu, nv);
+    if (lane == 0) {
+        ctl[8 + gw] = static_cast<int>(mx);
+        ctl[12 + gw] = static_cast<int>(mn);
+        ctl[4 + gw] = nv;
+    }
+    group_bar(bar);
+    mx = 0u;
+    mn = 0xFFFFFFFFu;
+    nv = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        mx = max(mx, static_cast<uint32_t>(ctl[8 + w]));
+        mn = min(mn, static_cast<uint32_t>(ctl[12 + w]));
+        nv += ctl[4 + w];
+    }
+    group_bar(bar);  // ctl is reused below
     RadixOut r;
     r.krem = k;
     if (mx == mn) {
@@ -190,55 +203,50 @@ __device__ __forceinline__ RadixOut warp_radix_staged(const uint2 *stage, const 
         const int w = lo >= 8 ? 8 : lo;
         lo -= w;
         const uint32_t dmask = (1u << w) - 1u;
-#pragma unroll
-        for (int b = 0; b < 8; ++b) hist[lane * 8 + b] = 0u;
-        __syncwarp();
+        hist[tg] = 0u;
+        hist[tg + GT] = 0u;
+        group_bar(bar);
         const unsigned long long want = prefix >> (lo + w);
-        for_staged(n, lane, [&](int i, bool v) {
-            if (use(i, v)) {
-                const uint32_t x = val(i);
-                if ((static_cast<unsigned long long>(x) >> (lo + w)) == want) atomicAdd(&hist[(x >> lo) & dmask], 1u);
-            }
-        });
-        __syncwarp();
-        uint32_t cnt[8];
-        uint32_t sum = 0;
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
-            cnt[b] = hist[255 - (lane * 8 + b)];
-            sum += cnt[b];
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        const uint32_t excl = incl - sum;
-        const bool mine = excl < static_cast<uint32_t>(r.krem) && static_cast<uint32_t>(r.krem) <= incl;
-        int digit = 0;
-        uint32_t above = 0, e = 0;
-        if (mine) {
-            uint32_t acc = excl;
+        for (int u = 0; u < PER; ++u)
+            if (use[u] && (static_cast<unsigned long long>(v[u]) >> (lo + w)) == want)
+                atomicAdd(&hist[(v[u] >> lo) & dmask], 1u);
+        group_bar(bar);
+        if (gw == 0) {
+            uint32_t cnt[8];
+            uint32_t sum = 0;
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
-                if (acc + cnt[b] >= static_cast<uint32_t>(r.krem)) {
-                    digit = 255 - (lane * 8 + b);
-                    above = acc;
-                    e = cnt[b];
-                    break;
+                cnt[b] = hist[255 - (lane * 8 + b)];
+                sum += cnt[b];
+            }
+            uint32_t incl = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            const uint32_t excl = incl - sum;
+            if (excl < static_cast<uint32_t>(r.krem) && static_cast<uint32_t>(r.krem) <= incl) {
+                uint32_t acc = excl;
+#pragma unroll
+                for (int b = 0; b < 8; ++b) {
+                    if (acc + cnt[b] >= static_cast<uint32_t>(r.krem)) {
+                        ctl[0] = 255 - (lane * 8 + b);
+                        ctl[1] = static_cast<int>(acc);
+                        ctl[2] = static_cast<int>(cnt[b]);
+                        break;
+                    }
+                    acc += cnt[b];
                 }
-                acc += cnt[b];
             }
         }
-        const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1;
-        digit = __shfl_sync(0xFFFFFFFFu, digit, src);
-        above = __shfl_sync(0xFFFFFFFFu, above, src);
-        e = __shfl_sync(0xFFFFFFFFu, e, src);
-        r.krem -= static_cast<int>(above);
-        eq = static_cast<int>(e);
+        group_bar(bar);
+        const int digit = ctl[0];
+        r.krem -= ctl[1];
+        eq = ctl[2];
         prefix |= static_cast<unsigned long long>(digit) << lo;
-        __syncwarp();
+        group_bar(bar);  // everyone has read ctl before it is written again
         if (eq == r.krem) break;
     }
     r.thr = static_cast<uint32_t>(prefix);
@@ -247,23 +255,12 @@ __device__ __forceinline__ RadixOut warp_radix_staged(const uint2 *stage, const 
     return r;
 }
 
-struct StagedRule {
-    uint32_t thr_key;
-    uint32_t thr_nblk;
-    int by_bucket;  // 1: keep key >= thr_key
-};
-
-// staged items hold (key, block) after stage_to_keys
-__device__ __forceinline__ bool staged_keep(const StagedRule &r, uint2 it) {
-    if (r.by_bucket) return it.x >= r.thr_key;
-    return it.x > r.thr_key || (it.x == r.thr_key && ~it.y >= r.thr_nblk);
-}
-
 // Exact k best (key desc, block asc) of the staged union, plus the streaming
 // threshold a later (higher-index) block must reach: s >= *theta.
-__device__ __forceinline__ StagedRule staged_select_exact(const uint2 *stage, const int (&n)[4], int k,
-                                                          uint32_t *hist, int lane, float *theta) {
-    const RadixOut r = warp_radix_staged<false, false>(stage, n, 0u, k, 8, hist, lane);
+__device__ __forceinline__ StagedRule group_select_exact(const uint2 *stage, const int (&n)[4], int k,
+                                                         uint32_t *hist, int *ctl, int tg, int bar,
+                                                         float *theta) {
+    const RadixOut r = group_radix<false, false>(stage, n, 0u, k, 8, hist, ctl, tg, bar);
     StagedRule rule;
     rule.thr_key = r.thr;
     rule.thr_nblk = 0;
@@ -273,92 +270,44 @@ __device__ __forceinline__ StagedRule staged_select_exact(const uint2 *stage, co
         return rule;
     }
     // the k-th key is exactly r.thr; take the r.krem ties with the lowest blocks
-    const RadixOut r2 = warp_radix_staged<true, true>(stage, n, r.thr, r.krem, 8, hist, lane);
+    const RadixOut r2 = group_radix<true, true>(stage, n, r.thr, r.krem, 8, hist, ctl, tg, bar);
     rule.by_bucket = 0;
     rule.thr_nblk = r2.thr;
     *theta = nextafterf(key2f(r.thr), INFINITY);
     return rule;
 }
 
-// Write the staged items that the rule keeps back to the global list (keys
-// turned back into score bits), dealt round-robin over the 4 sub-lists;
-// returns the number kept.
-__device__ __forceinline__ int restore_union(uint2 *lst, const uint2 *stage, const int (&n)[4],
-                                             const StagedRule &rule, int lane) {
-    int out = 0;
-    for_staged(n, lane, [&](int i, bool v) {
-        const uint2 it = stage[i];
-        const bool kp = v && staged_keep(rule, it);
-        const unsigned ball = __ballot_sync(0xFFFFFFFFu, kp);
-        if (kp) {
-            const int r = out + __popc(ball & ((1u << lane) - 1u));
-            lst[(r & 3) * SUB + (r >> 2)] = make_uint2(__float_as_uint(key2f(it.x)), it.y);
-        }
-        out += __popc(ball);
-    });
-    return out;
-}
-
-// Stable LSD radix sort (warp) of m <= 512 64-bit items by their high word
-// (the block index, < 2^(8*passes)); a and b are two 512-entry buffers, the
-// result ends in a.  hist: 256 words of this warp.
-__device__ __forceinline__ void warp_sort_by_block(unsigned long long *a, unsigned long long *b, int m,
-                                                   int passes, uint32_t *hist, int lane) {
-    for (int pass = 0; pass < passes; ++pass) {
-        const int shift = 32 + 8 * pass;
+// Ranks of the kept staged items in staging order (u-major, then thread):
+// pos[u] for kept items; returns the number kept.  tab: 32 ints of the group.
+__device__ __forceinline__ int group_ranks(const bool (&kp)[PER], int (&pos)[PER], int *tab, int tg, int bar) {
+    const int lane = tg & 31, gw = tg >> 5;
+    unsigned ball[PER];
 #pragma unroll
-        for (int d = 0; d < 8; ++d) hist[lane * 8 + d] = 0u;
-        __syncwarp();
-        for (int i = lane; i < m; i += 32) atomicAdd(&hist[(a[i] >> shift) & 255], 1u);
-        __syncwarp();
-        // exclusive scan of the 256 counts (lane owns 8 consecutive digits)
-        uint32_t c8[8], sum = 0;
-#pragma unroll
-        for (int d = 0; d < 8; ++d) {
-            c8[d] = hist[lane * 8 + d];
-            sum += c8[d];
-        }
-        uint32_t incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-            if (lane >= o) incl += t;
-        }
-        uint32_t run = incl - sum;
-#pragma unroll
-        for (int d = 0; d < 8; ++d) {
-            hist[lane * 8 + d] = run;
-            run += c8[d];
-        }
-        __syncwarp();
-        // stable scatter, 32 items at a time in order
-        for (int i0 = 0; i0 < m; i0 += 32) {
-            const int i = i0 + lane;
-            const bool v = i < m;
-            const unsigned long long x = v ? a[i] : 0ull;
-            const unsigned d = v ? static_cast<unsigned>((x >> shift) & 255) : 256u + lane;
-            const unsigned peers = __match_any_sync(0xFFFFFFFFu, d);
-            const uint32_t base = v ? hist[d] : 0u;
-            __syncwarp();
-            if (v) {
-                b[base + __popc(peers & ((1u << lane) - 1u))] = x;
-                if ((peers & ((1u << lane) - 1u)) == 0u) hist[d] = base + __popc(peers);
-            }
-            __syncwarp();
-        }
-        unsigned long long *t = a;
-        a = b;
-        b = t;
+    for (int u = 0; u < PER; ++u) {
+        ball[u] = __ballot_sync(0xFFFFFFFFu, kp[u]);
+        if (lane == 0) tab[u * 4 + gw] = __popc(ball[u]);
     }
-    if (passes & 1) {  // result is in the second buffer: copy back
-        for (int i = lane; i < m; i += 32) b[i] = a[i];
-        __syncwarp();
+    group_bar(bar);
+    int run = 0;
+#pragma unroll
+    for (int u = 0; u < PER; ++u) {
+        int before = 0, all = 0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const int c = tab[u * 4 + w];
+            before += w < gw ? c : 0;
+            all += c;
+        }
+        pos[u] = run + before + __popc(ball[u] & ((1u << lane) - 1u));
+        run += all;
     }
+    group_bar(bar);  // tab may be reused after this
+    return run;
 }
 
 // Store only where pred holds, as a predicated instruction (no branch).  No
 // "memory" clobber: the compiler may move other loads across it (ordering
-// against the list readers comes from the proxy fence and group barrier).
+// against the list readers comes from the group barrier).
 __device__ __forceinline__ void st_global_pred(uint2 *addr, uint2 v, bool pred) {
     asm volatile(
         "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %0, 0;\n\t@p st.global.v2.b32 [%1], {%2, %3};\n\t}" ::"r"(
@@ -376,11 +325,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *sQ = smem + OFF_Q;
     uint8_t *sK = smem + OFF_K;
     uint2 *sStage = reinterpret_cast<uint2 *>(smem + OFF_STAGE);
+    int *sCtl = reinterpret_cast<int *>(smem + OFF_CTL);
     uint32_t *sHist = reinterpret_cast<uint32_t *>(smem + OFF_HIST);
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sTheta = reinterpret_cast<float *>(smem + OFF_THETA);
     int *sCnt = reinterpret_cast<int *>(smem + OFF_CNT);  // sCnt[q * TQ + tl]
-    unsigned *sFlag = reinterpret_cast<unsigned *>(smem + OFF_FLAG);  // sFlag[half * 2 + parity]
+    unsigned *sFlag = reinterpret_cast<unsigned *>(smem + OFF_FLAG);  // sFlag[group * 2 + parity]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
     uint64_t *full = bars;
     uint64_t *empty = bars + NSTAGE;
@@ -406,7 +356,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[i], NEPI);
         }
         sMisc[1] = 0;
-        for (int i = 0; i < 4; ++i) sFlag[i] = 0u;
+        for (int i = 0; i < NGRP * 2; ++i) sFlag[i] = 0u;
         fence_barrier_init();
     }
     if (warp == 2) {
@@ -493,13 +443,17 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
     } else if (warp >= 4) {
         // --------------------------------------------------- epilogue --
+        // 16 warps = 4 groups x 4 TMEM lane quarters; group g scores tokens
+        // g*16 .. g*16+15 (TMEM columns g*64 .. g*64+63) for the 128 blocks of
+        // a tile; the group's 128 threads together do its selection work.
         const int e = warp - 4;
         const int quarter = warp & 3;  // TMEM lane quarter this warp may access
-        const int half = e >> 2;       // token half: columns [half*128, half*128+128)
-        const int tid_h = quarter * 32 + lane;
-        uint32_t *hist = sHist + e * 256;
-        uint2 *stage = sStage + e * CAP;
-        const int gbar = 1 + half;  // hardware barrier id of this half
+        const int g = e >> 2;          // group
+        const int tg = quarter * 32 + lane;  // thread index within the group
+        const int bar = 1 + g;         // hardware barrier id of the group
+        uint32_t *hist = sHist + g * 256;
+        int *ctl = sCtl + g * 64;      // [0..15] radix, [16..47] rank table
+        uint2 *stage = sStage + g * CAP;
         const unsigned ltmask = (1u << lane) - 1u;
         // this warp's sub-lists: token tl's at sub[tl * CAP]
         uint2 *sub = p.cand + static_cast<int64_t>(blockIdx.x) * TQ * CAP + quarter * SUB;
@@ -509,12 +463,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int q = p.nq - 1 - kk;
             const int64_t t0 = static_cast<int64_t>(q) * TQ;
             const int nbt = num_btiles(p.L, q);
-            if (group_sync_fail(gbar, !ok || sMisc[1] != 0)) { ok = false; break; }
-            if (tid_h < 32) {
-                const int tl = half * 32 + tid_h;
+            if (group_sync_fail(bar, !ok || sMisc[1] != 0)) { ok = false; break; }
+            if (tg < GTOK) {
+                const int tl = g * GTOK + tg;
                 const int64_t t = t0 + tl;
 #pragma unroll
-                for (int q = 0; q < 4; ++q) sCnt[q * TQ + tl] = 0;
+                for (int qq = 0; qq < 4; ++qq) sCnt[qq * TQ + tl] = 0;
                 sTheta[tl] = -INFINITY;
 #pragma unroll
                 for (int h = 0; h < kHI; ++h) {
@@ -523,17 +477,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                     sW[tl * 4 + h] = wv;
                 }
             }
-            if (group_sync_fail(gbar, false)) { ok = false; break; }
+            if (group_sync_fail(bar, false)) { ok = false; break; }
             const bool tile_all_in = (t0 + TQ <= p.L);
             const int64_t c_min = t0 / kBlock;
             for (int j = 0; j < nbt; ++j) {
                 const uint32_t buf = acc & 1;
                 const uint32_t use = acc >> 1;
+                const int par = static_cast<int>(acc & 1);
                 if (ok && !mbar_wait(&tfull[buf], use & 1)) ok = false;
                 if (!ok) {  // skip the work, keep taking part in the barriers
                     ++acc;
                     if constexpr (!DENSE) {
-                        if (group_sync_fail(gbar, true)) break;
+                        if (group_sync_fail(bar, true)) break;
                     }
                     continue;
                 }
@@ -541,21 +496,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int64_t b = static_cast<int64_t>(j) * TB + quarter * 32 + lane;
                 const bool masked = !(tile_all_in && (static_cast<int64_t>(j) * TB + TB <= c_min));
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       buf * NCOL + half * 128;
-                // 8 chunks of 4 tokens (16 columns), the load of chunk ch+1 in
+                                       buf * NCOL + g * (GTOK * kHI);
+                // 4 chunks of 4 tokens (16 columns), the load of chunk ch+1 in
                 // flight while chunk ch is scored
                 uint32_t ra[16], rb[16];
                 tmem_ld16(tbase, ra);
                 tmem_wait16(ra);
+                unsigned fl = 0;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int ch = 0; ch < GTOK / 4; ++ch) {
                     uint32_t(&cur)[16] = (ch & 1) ? rb : ra;
                     uint32_t(&nxt)[16] = (ch & 1) ? ra : rb;
-                    if (ch < 7) tmem_ld16(tbase + (ch + 1) * 16, nxt);
-                    const int tl0 = half * 32 + ch * 4;
+                    if (ch < GTOK / 4 - 1) tmem_ld16(tbase + (ch + 1) * 16, nxt);
+                    const int tl0 = g * GTOK + ch * 4;
                     const float4 th = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
                     const float thv[4] = {th.x, th.y, th.z, th.w};
-                    int4 c4;
+                    int4 c4 = make_int4(0, 0, 0, 0);
                     if constexpr (!DENSE) c4 = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0]);
                     int cnt4[4] = {c4.x, c4.y, c4.z, c4.w};
                     float sv[4];
@@ -585,116 +541,123 @@ __global__ void __launch_bounds__(THREADS, 1)
                                            make_uint2(__float_as_uint(sv[tk]), static_cast<uint32_t>(b)),
                                            pass && pos < SUB);
                             cnt4[tk] += __popc(m);
+                            if (cnt4[tk] > SUB - 32) fl |= 1u << (ch * 4 + tk);
                         }
                     }
-                    if constexpr (!DENSE) {
+                    if constexpr (!DENSE)
                         *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0]) =
                             make_int4(cnt4[0], cnt4[1], cnt4[2], cnt4[3]);
-                        // lists that might overflow on the next tile get flagged
-                        unsigned fl = 0;
-#pragma unroll
-                        for (int tk = 0; tk < 4; ++tk)
-                            if (cnt4[tk] > SUB - 32) fl |= 1u << (ch * 4 + tk);
-                        if (fl && lane == 0) atomicOr(&sFlag[half * 2 + (acc & 1)], fl);
-                    }
-                    if (ch < 7) tmem_wait16(nxt);
+                    if (ch < GTOK / 4 - 1) tmem_wait16(nxt);
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 ++acc;
                 if constexpr (!DENSE) {
-                    // lists that might overflow on the next tile are cut back
-                    if (group_sync_fail(gbar, sMisc[1] != 0)) { ok = false; break; }
-                    const unsigned flags = sFlag[half * 2 + ((acc - 1) & 1)];
-                    for (int i = 0; i < 8; ++i) {
-                        const int tl = half * 32 + quarter + 4 * i;
-                        if (!((flags >> (tl - half * 32)) & 1u)) continue;
+                    // lists that might overflow on the next tile get cut back
+                    if (fl && lane == 0) atomicOr(&sFlag[g * 2 + par], fl);
+                    if (group_sync_fail(bar, sMisc[1] != 0)) { ok = false; break; }
+                    unsigned flags = sFlag[g * 2 + par];
+                    while (flags) {
+                        const int t16 = __ffs(flags) - 1;
+                        flags &= flags - 1;
+                        const int tl = g * GTOK + t16;
                         int n[4];
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) n[q] = sCnt[q * TQ + tl];
-                        const int nmax = max(max(n[0], n[1]), max(n[2], n[3]));
-                        if (nmax > SUB) report(p.status, QSA_ERR_DEVICE_CHECK);
-                        if (nmax > SUB - 32) {
+                        for (int qq = 0; qq < 4; ++qq) n[qq] = sCnt[qq * TQ + tl];
+                        if (max(max(n[0], n[1]), max(n[2], n[3])) > SUB && tg == 0)
+                            report(p.status, QSA_ERR_DEVICE_CHECK);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) n[q] = min(n[q], SUB);
-                            uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
-                            fetch_union(lst, n, stage, lane);
-                            // cheap pass: a bucket bound 16 bits below the shared prefix
-                            const RadixOut r = warp_radix_staged<false, false>(stage, n, 0u, p.k_sel, 2, hist, lane);
-                            float th;
-                            StagedRule rule{r.thr, 0u, 1};
-                            if ((p.k_sel - r.krem) + r.eq <= KEEP_MAX)
-                                th = r.lo == 0 ? nextafterf(key2f(r.thr), INFINITY) : key2f(r.thr);
-                            else
-                                rule = staged_select_exact(stage, n, p.k_sel, hist, lane, &th);
-                            const int kept = restore_union(lst, stage, n, rule, lane);
-                            if (lane < 4) sCnt[lane * TQ + tl] = (kept + 3 - lane) / 4;
-                            if (lane == 0) sTheta[tl] = th;
-                            __syncwarp();
+                        for (int qq = 0; qq < 4; ++qq) n[qq] = min(n[qq], SUB);
+                        uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
+                        group_fetch(lst, n, stage, tg, bar);
+                        // cheap pass: a bucket bound 16 bits below the shared prefix
+                        const RadixOut r = group_radix<false, false>(stage, n, 0u, p.k_sel, 2, hist, ctl, tg, bar);
+                        float th;
+                        StagedRule rule{r.thr, 0u, 1};
+                        if ((p.k_sel - r.krem) + r.eq <= KEEP_MAX)
+                            th = r.lo == 0 ? nextafterf(key2f(r.thr), INFINITY) : key2f(r.thr);
+                        else
+                            rule = group_select_exact(stage, n, p.k_sel, hist, ctl, tg, bar, &th);
+                        // survivors back to the list, dealt round-robin over the 4 sub-lists
+                        uint2 it[PER];
+                        bool kp[PER];
+                        int pos[PER];
+#pragma unroll
+                        for (int u = 0; u < PER; ++u) {
+                            it[u] = stage[tg + GT * u];
+                            kp[u] = staged_valid(u, tg, n) && staged_keep(rule, it[u]);
                         }
+                        const int kept = group_ranks(kp, pos, ctl + 16, tg, bar);
+#pragma unroll
+                        for (int u = 0; u < PER; ++u)
+                            if (kp[u])
+                                lst[(pos[u] & 3) * SUB + (pos[u] >> 2)] =
+                                    make_uint2(__float_as_uint(key2f(it[u].x)), it[u].y);
+                        if (tg < 4) sCnt[tg * TQ + tl] = (kept + 3 - tg) / 4;
+                        if (tg == 0) sTheta[tl] = th;
+                        group_bar(bar);  // stage, counts and list settled before the next token
                     }
-                    if (group_sync_fail(gbar, !ok)) { ok = false; break; }
-                    if (tid_h == 0) sFlag[half * 2 + ((acc - 1) & 1)] = 0u;
+                    if (group_sync_fail(bar, false)) { ok = false; break; }
+                    if (tg == 0) sFlag[g * 2 + par] = 0u;  // next written two tiles from now
                 }
             }
             if (!ok) continue;  // the next tile-start barrier takes everyone out
             if constexpr (!DENSE) {
-                // ---- finalize: one warp per token
-                for (int i = 0; i < 8; ++i) {
-                    const int tl = half * 32 + quarter + 4 * i;
+                // ---- finalize: the group's 16 tokens one after the other
+                for (int t16 = 0; t16 < GTOK; ++t16) {
+                    const int tl = g * GTOK + t16;
                     const int64_t t = t0 + tl;
-                    if (t >= p.L) continue;
+                    if (t >= p.L) break;
                     const int64_t c = t / kBlock;
-                    int nq4[4];
+                    int n[4];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) nq4[q] = min(sCnt[q * TQ + tl], SUB);
-                    const int n = nq4[0] + nq4[1] + nq4[2] + nq4[3];
+                    for (int qq = 0; qq < 4; ++qq) n[qq] = min(sCnt[qq * TQ + tl], SUB);
+                    const int ntot = n[0] + n[1] + n[2] + n[3];
                     const uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
-                    fetch_union(lst, nq4, stage, lane);
+                    group_fetch(lst, n, stage, tg, bar);
                     StagedRule rule{0u, 0u, 1};
-                    if (n > p.k_sel) {
+                    if (ntot > p.k_sel) {
                         float th;
-                        rule = staged_select_exact(stage, nq4, p.k_sel, hist, lane, &th);
+                        rule = group_select_exact(stage, n, p.k_sel, hist, ctl, tg, bar, &th);
                     }
-                    // kept items -> front of the staging buffer as (block << 32 | score bits),
-                    // in place: every lane has read its item of a chunk before any write
+                    uint2 it[PER];
+                    bool kp[PER];
+                    int pos[PER];
+#pragma unroll
+                    for (int u = 0; u < PER; ++u) {
+                        it[u] = stage[tg + GT * u];
+                        kp[u] = staged_valid(u, tg, n) && staged_keep(rule, it[u]);
+                    }
+                    int m = group_ranks(kp, pos, ctl + 16, tg, bar);  // also: all stage reads done
                     unsigned long long *sortb = reinterpret_cast<unsigned long long *>(stage);
-                    int m = 0;
-                    for_staged(nq4, lane, [&](int i2, bool v) {
-                        const uint2 it = stage[i2];
-                        const bool kp = v && staged_keep(rule, it);
-                        const unsigned ball = __ballot_sync(0xFFFFFFFFu, kp);
-                        if (kp)
-                            sortb[m + __popc(ball & ((1u << lane) - 1u))] =
-                                (static_cast<unsigned long long>(it.y) << 32) | __float_as_uint(key2f(it.x));
-                        m += __popc(ball);
-                        __syncwarp();
-                    });
-                    if (m > 512) { report(p.status, QSA_ERR_DEVICE_CHECK); m = 512; }
-                    // order by block: enough 8-bit digits to cover blocks < c
-                    const int passes = c < (1 << 8) ? 1 : (c < (1 << 16) ? 2 : (c < (1 << 24) ? 3 : 4));
-                    warp_sort_by_block(sortb, sortb + 512, m, passes, hist, lane);
+#pragma unroll
+                    for (int u = 0; u < PER; ++u)
+                        if (kp[u] && pos[u] < 512)
+                            sortb[pos[u]] = (static_cast<unsigned long long>(it[u].y) << 32) |
+                                            __float_as_uint(key2f(it[u].x));
+                    if (m > 512) {
+                        if (tg == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
+                        m = 512;
+                    }
+                    group_bar(bar);
+                    // order by block: blocks are distinct, so an item's place is the
+                    // number of smaller blocks (broadcast reads of the list)
                     int32_t *row = p.idx + t * p.budget;
                     float *srow = p.score ? p.score + t * p.budget : nullptr;
-                    for (int ii = lane; ii < p.budget; ii += 32) {
-                        int32_t bi;
-                        float sv;
-                        if (ii < m) {
-                            const unsigned long long v = sortb[ii];
-                            bi = static_cast<int32_t>(v >> 32);
-                            sv = __uint_as_float(static_cast<uint32_t>(v));
-                        } else if (ii == m) {
-                            bi = static_cast<int32_t>(c);
-                            sv = INFINITY;
-                        } else {
-                            bi = -1;
-                            sv = -INFINITY;
-                        }
-                        row[ii] = bi;
-                        if (srow) srow[ii] = sv;
+                    for (int i = tg; i < m; i += GT) {
+                        const unsigned long long vi = sortb[i];
+                        const uint32_t bi = static_cast<uint32_t>(vi >> 32);
+                        int rank = 0;
+                        for (int jj = 0; jj < m; ++jj) rank += static_cast<uint32_t>(sortb[jj] >> 32) < bi;
+                        row[rank] = static_cast<int32_t>(bi);
+                        if (srow) srow[rank] = __uint_as_float(static_cast<uint32_t>(vi));
                     }
-                    __syncwarp();
+                    for (int i = m + tg; i < p.budget; i += GT) {
+                        row[i] = i == m ? static_cast<int32_t>(c) : -1;
+                        if (srow) srow[i] = i == m ? INFINITY : -INFINITY;
+                    }
+                    group_bar(bar);  // sortb (= stage) is reused by the next token
                 }
             }
         }
