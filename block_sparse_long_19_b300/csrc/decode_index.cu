@@ -370,33 +370,17 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
         }
     }
     __syncthreads();
-    int P2 = 32;
-    while (P2 < m) P2 <<= 1;
-    for (int i = m + threadIdx.x; i < P2; i += MERGE_THREADS) sortb[i] = ~0ull;
-    __syncthreads();
-    for (int kb = 2; kb <= P2; kb <<= 1) {
-        for (int jb = kb >> 1; jb > 0; jb >>= 1) {
-            for (int i = threadIdx.x; i < P2; i += MERGE_THREADS) {
-                const int ix = i ^ jb;
-                if (ix > i) {
-                    const unsigned long long a = sortb[i], b = sortb[ix];
-                    const bool up = (i & kb) == 0;
-                    if ((a > b) == up) {
-                        sortb[i] = b;
-                        sortb[ix] = a;
-                    }
-                }
-            }
-            __syncthreads();
-        }
+    // order by block: blocks are distinct, so an item's place is the number
+    // of smaller blocks (every thread scans the list with broadcast reads)
+    m = min(ctl[3], kMaxBudget);
+    for (int i = threadIdx.x; i < m; i += MERGE_THREADS) {
+        const uint32_t bi = static_cast<uint32_t>(sortb[i] >> 32);
+        int rank = 0;
+        for (int j = 0; j < m; ++j) rank += static_cast<uint32_t>(sortb[j] >> 32) < bi;
+        if (rank < p.budget) row[rank] = static_cast<int32_t>(bi);
     }
-    for (int i = threadIdx.x; i < p.budget; i += MERGE_THREADS) {
-        int32_t v;
-        if (i < m) v = static_cast<int32_t>(sortb[i] >> 32);
-        else if (i == m) v = static_cast<int32_t>(c);
-        else v = -1;
-        row[i] = v;
-    }
+    for (int i = m + threadIdx.x; i < p.budget; i += MERGE_THREADS)
+        row[i] = i == m ? static_cast<int32_t>(c) : -1;
 }
 
 }  // namespace dx

@@ -27,6 +27,8 @@
 //     threshold always loses the tie and is never needed;
 //   * after the last block tile a warp per token selects the final k, sorts
 //     them by block index and writes the row.
+#include <type_traits>
+
 #include "qsa_common.cuh"
 #include "qsa_kernels.h"
 #include "qsa_select.cuh"
@@ -305,6 +307,55 @@ __device__ __forceinline__ int group_ranks(const bool (&kp)[PER], int (&pos)[PER
     return run;
 }
 
+// Ascending bitonic sort of 512 distinct keys held by the 128 threads of a
+// group, thread tg holding positions 4tg .. 4tg+3.  Partners one or two
+// positions away are in the same thread, up to 64 away in the same warp
+// (shuffles); the three steps that cross warps go through shared memory,
+// alternating between buf[0..511] and buf[512..1023].  The caller's initial
+// array may sit in buf[512..1023]: every thread has loaded its keys before
+// the first write to buf[0..511] passes a barrier.
+template <typename T>
+__device__ __forceinline__ void group_sort512(T (&v)[4], T *buf, int tg, int bar) {
+    int flip = 0;
+#pragma unroll
+    for (int k = 2; k <= 512; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j >= 1; j >>= 1) {
+            if (j < 4) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (r & j) continue;
+                    const int e = 4 * tg + r;
+                    const bool asc = (e & k) == 0;
+                    const T lo = v[r], hi = v[r ^ j];
+                    const bool sw = asc ? (lo > hi) : (lo < hi);
+                    v[r] = sw ? hi : lo;
+                    v[r ^ j] = sw ? lo : hi;
+                }
+            } else {
+                T o[4];
+                if (j >= 128) {
+                    T *b = buf + (flip & 1) * 512;
+                    ++flip;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) b[4 * tg + r] = v[r];
+                    group_bar(bar);
+                    const int pt = tg ^ (j >> 2);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) o[r] = b[4 * pt + r];
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) o[r] = __shfl_xor_sync(0xFFFFFFFFu, v[r], j >> 2);
+                }
+                const int e = 4 * tg;
+                const bool keep_min = ((e & j) == 0) == ((e & k) == 0);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) v[r] = keep_min ? min(v[r], o[r]) : max(v[r], o[r]);
+            }
+        }
+    }
+}
+
 // Store only where pred holds, as a predicated instruction (no branch).  No
 // "memory" clobber: the compiler may move other loads across it (ordering
 // against the list readers comes from the group barrier).
@@ -474,7 +525,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int h = 0; h < kHI; ++h) {
                     float wv = 0.f;
                     if (t < p.L) wv = __uint_as_float(static_cast<uint32_t>(p.w[t * kHI + h]) << 16);
-                    sW[tl * 4 + h] = wv;
+                    sW[(tl >> 2) * 16 + h * 4 + (tl & 3)] = wv;  // [token quad][head][token]
                 }
             }
             if (group_sync_fail(bar, false)) { ok = false; break; }
@@ -503,52 +554,72 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tmem_ld16(tbase, ra);
                 tmem_wait16(ra);
                 unsigned fl = 0;
+                // MASKED: the tile holds blocks that some of the tokens may not see
+                auto score_tile = [&](auto masked_c) {
+                    constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll
-                for (int ch = 0; ch < GTOK / 4; ++ch) {
-                    uint32_t(&cur)[16] = (ch & 1) ? rb : ra;
-                    uint32_t(&nxt)[16] = (ch & 1) ? ra : rb;
-                    if (ch < GTOK / 4 - 1) tmem_ld16(tbase + (ch + 1) * 16, nxt);
-                    const int tl0 = g * GTOK + ch * 4;
-                    const float4 th = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
-                    const float thv[4] = {th.x, th.y, th.z, th.w};
-                    int4 c4 = make_int4(0, 0, 0, 0);
-                    if constexpr (!DENSE) c4 = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0]);
-                    int cnt4[4] = {c4.x, c4.y, c4.z, c4.w};
-                    float sv[4];
+                    for (int ch = 0; ch < GTOK / 4; ++ch) {
+                        uint32_t(&cur)[16] = (ch & 1) ? rb : ra;
+                        uint32_t(&nxt)[16] = (ch & 1) ? ra : rb;
+                        if (ch < GTOK / 4 - 1) tmem_ld16(tbase + (ch + 1) * 16, nxt);
+                        const int tl0 = g * GTOK + ch * 4;
+                        // s = sum_h w_h * max(0, x_h) for two tokens per packed FMA,
+                        // heads in order 0..3, the first product added to +0 (the
+                        // sum is never -0); per component this is plain fmaf
+                        float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
-                    for (int tk = 0; tk < 4; ++tk) {
-                        const float4 wv = *reinterpret_cast<const float4 *>(&sW[(tl0 + tk) * 4]);
-                        // the first product is added to +0 so the sum is never -0
-                        float sc = fmaf(wv.x, fmaxf(__uint_as_float(cur[4 * tk + 0]), 0.f), 0.0f);
-                        sc = fmaf(wv.y, fmaxf(__uint_as_float(cur[4 * tk + 1]), 0.f), sc);
-                        sc = fmaf(wv.z, fmaxf(__uint_as_float(cur[4 * tk + 2]), 0.f), sc);
-                        sv[tk] = fmaf(wv.w, fmaxf(__uint_as_float(cur[4 * tk + 3]), 0.f), sc);
-                    }
-#pragma unroll
-                    for (int tk = 0; tk < 4; ++tk) {
-                        const int tl = tl0 + tk;
-                        const int64_t t = t0 + tl;
-                        const bool valid = !masked || ((t < p.L) && (b < (t >> 2)));
-                        if constexpr (DENSE) {
-                            if (valid) p.dense[t * p.dense_ld + b] = sv[tk];
-                        } else {
-                            // a block enters the token's list when s >= its threshold:
-                            // position from a ballot, no branch, no atomic
-                            const bool pass = valid && (sv[tk] >= thv[tk]);
-                            const unsigned m = __ballot_sync(0xFFFFFFFFu, pass);
-                            const int pos = cnt4[tk] + __popc(m & ltmask);
-                            st_global_pred(sub + static_cast<int64_t>(tl) * CAP + pos,
-                                           make_uint2(__float_as_uint(sv[tk]), static_cast<uint32_t>(b)),
-                                           pass && pos < SUB);
-                            cnt4[tk] += __popc(m);
-                            if (cnt4[tk] > SUB - 32) fl |= 1u << (ch * 4 + tk);
+                        for (int h = 0; h < kHI; ++h) {
+                            const float4 wv = *reinterpret_cast<const float4 *>(&sW[(tl0 >> 2) * 16 + h * 4]);
+                            const float2 x01 = make_float2(fmaxf(__uint_as_float(cur[h]), 0.f),
+                                                           fmaxf(__uint_as_float(cur[4 + h]), 0.f));
+                            const float2 x23 = make_float2(fmaxf(__uint_as_float(cur[8 + h]), 0.f),
+                                                           fmaxf(__uint_as_float(cur[12 + h]), 0.f));
+                            s01 = __ffma2_rn(make_float2(wv.x, wv.y), x01, s01);
+                            s23 = __ffma2_rn(make_float2(wv.z, wv.w), x23, s23);
                         }
+                        const float sv[4] = {s01.x, s01.y, s23.x, s23.y};
+                        if constexpr (DENSE) {
+#pragma unroll
+                            for (int tk = 0; tk < 4; ++tk) {
+                                const int64_t t = t0 + tl0 + tk;
+                                const bool valid = !MASKED || ((t < p.L) && (b < (t >> 2)));
+                                if (valid) p.dense[t * p.dense_ld + b] = sv[tk];
+                            }
+                        } else {
+                            const float4 th = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
+                            const float thv[4] = {th.x, th.y, th.z, th.w};
+                            unsigned m[4];
+#pragma unroll
+                            for (int tk = 0; tk < 4; ++tk) {
+                                const int64_t t = t0 + tl0 + tk;
+                                const bool valid = !MASKED || ((t < p.L) && (b < (t >> 2)));
+                                m[tk] = __ballot_sync(0xFFFFFFFFu, valid && (sv[tk] >= thv[tk]));
+                            }
+                            // a block enters the token's list when s >= its threshold;
+                            // late in the scan most warps have no such block at all
+                            if ((m[0] | m[1] | m[2] | m[3]) != 0u) {
+                                const int4 c4 = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0]);
+                                int cnt4[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                                for (int tk = 0; tk < 4; ++tk) {
+                                    if (m[tk] == 0u) continue;  // warp-uniform
+                                    const bool pass = (m[tk] >> lane) & 1u;
+                                    const int pos = cnt4[tk] + __popc(m[tk] & ltmask);
+                                    st_global_pred(sub + static_cast<int64_t>(tl0 + tk) * CAP + pos,
+                                                   make_uint2(__float_as_uint(sv[tk]), static_cast<uint32_t>(b)),
+                                                   pass && pos < SUB);
+                                    cnt4[tk] += __popc(m[tk]);
+                                    if (cnt4[tk] > SUB - 32) fl |= 1u << (ch * 4 + tk);
+                                }
+                                *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0]) =
+                                    make_int4(cnt4[0], cnt4[1], cnt4[2], cnt4[3]);
+                            }
+                        }
+                        if (ch < GTOK / 4 - 1) tmem_wait16(nxt);
                     }
-                    if constexpr (!DENSE)
-                        *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0]) =
-                            make_int4(cnt4[0], cnt4[1], cnt4[2], cnt4[3]);
-                    if (ch < GTOK / 4 - 1) tmem_wait16(nxt);
-                }
+                };
+                if (masked) score_tile(std::true_type{});
+                else score_tile(std::false_type{});
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
@@ -630,32 +701,57 @@ __global__ void __launch_bounds__(THREADS, 1)
                         kp[u] = staged_valid(u, tg, n) && staged_keep(rule, it[u]);
                     }
                     int m = group_ranks(kp, pos, ctl + 16, tg, bar);  // also: all stage reads done
-                    unsigned long long *sortb = reinterpret_cast<unsigned long long *>(stage);
-#pragma unroll
-                    for (int u = 0; u < PER; ++u)
-                        if (kp[u] && pos[u] < 512)
-                            sortb[pos[u]] = (static_cast<unsigned long long>(it[u].y) << 32) |
-                                            __float_as_uint(key2f(it[u].x));
                     if (m > 512) {
                         if (tg == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
                         m = 512;
                     }
-                    group_bar(bar);
-                    // order by block: blocks are distinct, so an item's place is the
-                    // number of smaller blocks (broadcast reads of the list)
+                    // order by block (blocks are distinct): a group sort of 512 keys,
+                    // block indices alone or (block, score bits) when scores are written
                     int32_t *row = p.idx + t * p.budget;
                     float *srow = p.score ? p.score + t * p.budget : nullptr;
-                    for (int i = tg; i < m; i += GT) {
-                        const unsigned long long vi = sortb[i];
-                        const uint32_t bi = static_cast<uint32_t>(vi >> 32);
-                        int rank = 0;
-                        for (int jj = 0; jj < m; ++jj) rank += static_cast<uint32_t>(sortb[jj] >> 32) < bi;
-                        row[rank] = static_cast<int32_t>(bi);
-                        if (srow) srow[rank] = __uint_as_float(static_cast<uint32_t>(vi));
-                    }
-                    for (int i = m + tg; i < p.budget; i += GT) {
-                        row[i] = i == m ? static_cast<int32_t>(c) : -1;
-                        if (srow) srow[i] = i == m ? INFINITY : -INFINITY;
+                    auto emit = [&](int e, uint32_t blk, float sc) {
+                        if (e >= p.budget) return;
+                        const bool in = e < m;
+                        row[e] = in ? static_cast<int32_t>(blk) : (e == m ? static_cast<int32_t>(c) : -1);
+                        if (srow) srow[e] = in ? sc : (e == m ? INFINITY : -INFINITY);
+                    };
+                    if (srow) {
+                        unsigned long long *sb = reinterpret_cast<unsigned long long *>(stage);
+#pragma unroll
+                        for (int u = 0; u < PER; ++u)
+                            if (kp[u] && pos[u] < 512)
+                                sb[512 + pos[u]] = (static_cast<unsigned long long>(it[u].y) << 32) |
+                                                   __float_as_uint(key2f(it[u].x));
+                        for (int i = m + tg; i < 512; i += GT) sb[512 + i] = ~0ull;
+                        group_bar(bar);
+                        unsigned long long v[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) v[r] = sb[512 + 4 * tg + r];
+                        group_sort512(v, sb, tg, bar);
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            emit(4 * tg + r, static_cast<uint32_t>(v[r] >> 32),
+                                 __uint_as_float(static_cast<uint32_t>(v[r])));
+                    } else {
+                        uint32_t *sb = reinterpret_cast<uint32_t *>(stage);
+#pragma unroll
+                        for (int u = 0; u < PER; ++u)
+                            if (kp[u] && pos[u] < 512) sb[512 + pos[u]] = it[u].y;
+                        for (int i = m + tg; i < 512; i += GT) sb[512 + i] = 0xFFFFFFFFu;
+                        group_bar(bar);
+                        uint32_t v[4];
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) v[r] = sb[512 + 4 * tg + r];
+                        group_sort512(v, sb, tg, bar);
+                        const int e0 = 4 * tg;
+                        if ((p.budget & 3) == 0 && e0 + 3 < m) {
+                            *reinterpret_cast<int4 *>(row + e0) = make_int4(
+                                static_cast<int>(v[0]), static_cast<int>(v[1]), static_cast<int>(v[2]),
+                                static_cast<int>(v[3]));
+                        } else {
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) emit(e0 + r, v[r], 0.f);
+                        }
                     }
                     group_bar(bar);  // sortb (= stage) is reused by the next token
                 }
