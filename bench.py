@@ -44,6 +44,7 @@ WORKLOADS = {
     "qsa_small": (32768, 512, 1, 4, 65536, 5),
     # profiling cases: inputs larger than L2, a few GB on the device
     "prof_128k": (131072, 512, 2, 1, 65536, 3),
+    "prof_256k": (262144, 512, 4, 1, 65536, 3),
     "prof_decode": (4096, 512, 6, 8, 131072, 6),
 }
 

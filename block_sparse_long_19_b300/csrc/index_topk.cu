@@ -9,24 +9,28 @@
 // the highest s (ties: lower block first).  The score matrix is never
 // written to memory.
 //
-// Design (one persistent CTA per SM, 12 warps):
+// Design (one persistent CTA per SM, 20 warps):
 //   * the contraction runs "swap-AB": the MMA's M = 128 block keys (A, from a
 //     TMA tile of kblk), N = 256 columns = 64 query tokens x 4 indexer heads
 //     (B, a TMA tile of qi that stays resident for the whole query tile),
 //     K = 128; fp32 accumulators live in TMEM, double-buffered (2 x 256 cols);
 //   * warp 0 issues the TMA loads, warp 1 issues tcgen05.mma (one thread),
-//     warps 4..11 are the epilogue: each thread owns one TMEM lane = one
-//     block, reads the 4 head columns of a token, forms the score and tests it
+//     warp 2 owns the TMEM allocation, warps 4..19 are the epilogue: four
+//     groups of four warps, group g owning tokens 16g .. 16g+15 and warp q of
+//     a group TMEM lane quarter q (32 blocks of the tile).  A thread reads the
+//     4 head columns of each of its 16 tokens, forms the score and tests it
 //     against the token's running threshold;
 //   * selection is an exact streaming top-k: every token keeps a candidate
-//     list (global workspace, L2-resident) of the blocks that beat its
-//     threshold.  When a list fills up, a warp radix-selects its k-th best
-//     (score desc, index asc), compacts the list to exactly k entries and
-//     raises the threshold to that score.  Block tiles are visited in
-//     ascending block order, so a later block with a score equal to the
-//     threshold always loses the tie and is never needed;
-//   * after the last block tile a warp per token selects the final k, sorts
-//     them by block index and writes the row.
+//     list (global workspace, mostly L2-resident) of the blocks that beat its
+//     threshold.  Every second tile a group checks its lists; one that could
+//     overflow is cut back by the group's 128 threads together: a radix
+//     select finds a bound at or below the k-th best (score desc, index asc),
+//     the survivors are written back and the threshold is raised to it.
+//     Block tiles are visited in ascending block order, so a later block with
+//     a score equal to the threshold always loses the tie and is never needed;
+//   * after the last block tile the group selects each token's final k
+//     exactly, sorts them by block index (bitonic, in registers) and writes
+//     the row.
 #include <type_traits>
 
 #include "qsa_common.cuh"
@@ -40,27 +44,30 @@ constexpr int TQ = 64;               // query tokens per tile
 constexpr int NCOL = TQ * kHI;       // 256 MMA columns (token-major, head-minor)
 constexpr int TB = 128;              // block keys per block tile (MMA M)
 constexpr int NSTAGE = 3;            // kblk tile ring
-constexpr int CAP = 1024;            // candidate slots per token
+constexpr int CAP = 2048;            // candidate slots per token
 constexpr int SUB = CAP / 4;         // per-warp sub-list of a token (one per TMEM lane quarter)
 constexpr int KSTEPS = kDI / 16;     // 8 MMAs of K = 16
 constexpr int NGRP = 4;              // epilogue groups
 constexpr int GTOK = TQ / NGRP;      // 16 tokens (64 TMEM columns) per group
 constexpr int NEPI = 4 * NGRP;       // 16 epilogue warps: group x TMEM lane quarter
 constexpr int GT = 128;              // threads per group
-constexpr int PER = CAP / GT;        // staged items per group thread
 constexpr int THREADS = (4 + NEPI) * 32;
-static_assert(SUB == 2 * GT, "staged item u of a thread is entry (u%2)*GT + tg of sub-list u/2");
+constexpr int CHK = 2;               // tiles between list checks
+constexpr int FLAG_AT = SUB - 32 * CHK;  // a sub-list longer than this is cut back at a check
+constexpr int HIST_INTS = 3 * 256;   // per group: 3 rotating histogram slots
+constexpr int CTL_INTS = 3 * 16;     // per group: 3 rotating control slots
 
+constexpr int GCOL = GTOK * kHI;     // 64 MMA columns per group
 constexpr uint32_t IDESC = idesc_bf16_f32(TB, NCOL);
 
 constexpr int SQ_BYTES = 2 * NCOL * 128;     // two 64-wide K halves, 128-B rows
 constexpr int SK_BYTES = 2 * TB * 128;
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + SQ_BYTES;
-constexpr int OFF_STAGE = OFF_K + NSTAGE * SK_BYTES;  // per group: one staged candidate union
-constexpr int OFF_HIST = OFF_STAGE + NGRP * CAP * 8;
-constexpr int OFF_CTL = OFF_HIST + NGRP * 256 * 4;
-constexpr int OFF_W = OFF_CTL + NGRP * 64 * 4;
+constexpr int OFF_HIST = OFF_K + NSTAGE * SK_BYTES;
+constexpr int OFF_CTL = OFF_HIST + NGRP * HIST_INTS * 4;
+constexpr int OFF_SORT = OFF_CTL + NGRP * CTL_INTS * 4;  // per group: 1024 sort slots of 8 bytes
+constexpr int OFF_W = OFF_SORT + NGRP * 1024 * 8;
 constexpr int OFF_THETA = OFF_W + TQ * 4 * 4;
 constexpr int OFF_CNT = OFF_THETA + TQ * 4;      // [4 quarters][TQ] sub-list counts
 constexpr int OFF_FLAG = OFF_CNT + 4 * TQ * 4;   // [NGRP groups][2 parities] token masks
@@ -68,6 +75,7 @@ constexpr int OFF_BAR = OFF_FLAG + NGRP * 2 * 4;
 constexpr int NBAR = 2 * NSTAGE + 2 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Params {
     int64_t L;
@@ -112,10 +120,13 @@ __device__ __forceinline__ int num_btiles(int64_t L, int q) {
 // warp of its group (the warp that owns TMEM lane quarter q appends to
 // sub-list q with a warp-private count, so appending needs neither atomics
 // nor shuffles).  Entries are (score bits, block).  Selection work on a list
-// is done by the 128 threads of the group together, on a copy in the group's
-// shared staging buffer (as order keys): thread tg holds staged items
-// i = tg + 128 u (u < 8), which is entry (u % 2) * 128 + tg of sub-list u / 2.
-constexpr int KEEP_MAX = CAP - 2 * TB;  // a lower-bound compaction must keep at most this many
+// is done by the group's 128 threads together, each warp holding its own
+// sub-list in registers (lane l: entries l + 32 i, i < IPL) with the score
+// bits turned into order keys.
+constexpr int IPL = SUB / 32;  // list entries per lane
+constexpr int KEEP_MAX = 768;  // a lower-bound compaction must keep at most this many
+static_assert(FLAG_AT + 32 * CHK <= SUB, "a sub-list takes at most 32 entries per tile");
+static_assert((KEEP_MAX + 3) / 4 < FLAG_AT, "a compacted list must leave room");
 
 struct StagedRule {
     uint32_t thr_key;
@@ -123,72 +134,92 @@ struct StagedRule {
     int by_bucket;  // 1: keep key >= thr_key
 };
 
-__device__ __forceinline__ bool staged_valid(int u, int tg, const int (&n)[4]) {
-    return (u & 1) * GT + tg < n[u >> 1];
-}
-
 __device__ __forceinline__ bool staged_keep(const StagedRule &r, uint2 it) {
     if (r.by_bucket) return it.x >= r.thr_key;
     return it.x > r.thr_key || (it.x == r.thr_key && ~it.y >= r.thr_nblk);
 }
 
-// Copy the 4 sub-lists into the staging buffer (all 8 loads of a thread in
-// flight first), scores turned into order keys.
-__device__ __forceinline__ void group_fetch(const uint2 *__restrict__ lst, const int (&n)[4],
-                                            uint2 *__restrict__ stage, int tg, int bar) {
-    uint2 it[PER];
-#pragma unroll
-    for (int u = 0; u < PER; ++u)
-        it[u] = staged_valid(u, tg, n) ? __ldcg(lst + tg + GT * u) : make_uint2(0u, 0u);
-#pragma unroll
-    for (int u = 0; u < PER; ++u)
-        if (staged_valid(u, tg, n)) stage[tg + GT * u] = make_uint2(f2key(__uint_as_float(it[u].x)), it[u].y);
-    group_bar(bar);
+// The group's cooperative steps.  Every step ends in one barrier of the
+// group's 128 threads; step s keeps its data in slot s % 3 (a 256-counter
+// histogram and 16 control ints) and, before its barrier, clears the
+// histogram of slot (s + 1) % 3 for the step after it.  That slot was last
+// read in step s - 2, which every thread finished before the barrier of step
+// s - 1, so one barrier per step suffices.  `step` counts in every thread
+// alike.
+struct Group {
+    uint32_t *hist;  // [3][256]
+    int *ctl;        // [3][16]
+    int tg, lane, gw, bar;
+    uint32_t step;
+};
+
+__device__ __forceinline__ int group_step_begin(Group &G) {
+    const int s = static_cast<int>(G.step % 3u);
+    uint32_t *nh = G.hist + ((G.step + 1u) % 3u) * 256;
+    nh[G.tg] = 0u;
+    nh[G.tg + GT] = 0u;
+    return s;
+}
+__device__ __forceinline__ void group_step_end(Group &G) {
+    group_bar(G.bar);
+    ++G.step;
 }
 
-// Group radix over the staged items (contract of warp_radix in
-// qsa_select.cuh).  NEG ranks ~block instead of the key; TIE restricts the
-// items to those whose key equals tie_key.  ctl: 16 ints of the group.
-template <bool NEG, bool TIE>
-__device__ __forceinline__ RadixOut group_radix(const uint2 *stage, const int (&n)[4], uint32_t tie_key, int k,
-                                                int max_passes, uint32_t *hist, int *ctl, int tg, int bar) {
-    const int lane = tg & 31, gw = tg >> 5;
-    uint32_t v[PER];
-    bool use[PER];
+// Loads this warp's sub-list (n entries) into registers as (key, block).
+__device__ __forceinline__ void group_load(const uint2 *__restrict__ lst, int n, uint2 (&it)[IPL], int lane) {
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        const uint2 it = stage[tg + GT * u];
-        use[u] = staged_valid(u, tg, n) && (!TIE || it.x == tie_key);
-        v[u] = NEG ? ~it.y : it.x;
+    for (int i = 0; i < IPL; ++i) {
+        const bool v = lane + 32 * i < n;
+        it[i] = v ? __ldcg(lst + lane + 32 * i) : make_uint2(0u, 0u);
     }
+#pragma unroll
+    for (int i = 0; i < IPL; ++i) it[i].x = f2key(__uint_as_float(it[i].x));
+}
+
+// Group radix over the register-held items (contract of warp_radix in
+// qsa_select.cuh).  NEG ranks ~block instead of the key; TIE restricts the
+// items to those whose key equals tie_key.  n: this warp's item count.
+template <bool NEG, bool TIE>
+__device__ __forceinline__ RadixOut group_radix(const uint2 (&it)[IPL], int n, uint32_t tie_key, int k,
+                                                int max_passes, Group &G) {
+    auto item = [&](int i, uint32_t &v) {
+        v = NEG ? ~it[i].y : it[i].x;
+        return G.lane + 32 * i < n && (!TIE || it[i].x == tie_key);
+    };
     uint32_t mx = 0u, mn = 0xFFFFFFFFu;
     int nv = 0;
 #pragma unroll
-    for (int u = 0; u < PER; ++u)
-        if (use[u]) {
-            mx = max(mx, v[u]);
-            mn = min(mn, v[u]);
+    for (int i = 0; i < IPL; ++i) {
+        if (32 * i >= n) break;
+        uint32_t v;
+        if (item(i, v)) {
+            mx = max(mx, v);
+            mn = min(mn, v);
             ++nv;
         }
+    }
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
     mn = __reduce_min_sync(0xFFFFFFFFu, mn);
     nv = __reduce_add_sync(0xFFFFFFFFu, nv);
-    if (lane == 0) {
-        ctl[8 + gw] = static_cast<int>(mx);
-        ctl[12 + gw] = static_cast<int>(mn);
-        ctl[4 + gw] = nv;
-    }
-    group_bar(bar);
-    mx = 0u;
-    mn = 0xFFFFFFFFu;
-    nv = 0;
+    {
+        const int s = group_step_begin(G);
+        int *c = G.ctl + s * 16;
+        if (G.lane == 0) {
+            c[8 + G.gw] = static_cast<int>(mx);
+            c[12 + G.gw] = static_cast<int>(mn);
+            c[4 + G.gw] = nv;
+        }
+        group_step_end(G);
+        mx = 0u;
+        mn = 0xFFFFFFFFu;
+        nv = 0;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        mx = max(mx, static_cast<uint32_t>(ctl[8 + w]));
-        mn = min(mn, static_cast<uint32_t>(ctl[12 + w]));
-        nv += ctl[4 + w];
+        for (int w = 0; w < 4; ++w) {
+            mx = max(mx, static_cast<uint32_t>(c[8 + w]));
+            mn = min(mn, static_cast<uint32_t>(c[12 + w]));
+            nv += c[4 + w];
+        }
     }
-    group_bar(bar);  // ctl is reused below
     RadixOut r;
     r.krem = k;
     if (mx == mn) {
@@ -205,50 +236,55 @@ __device__ __forceinline__ RadixOut group_radix(const uint2 *stage, const int (&
         const int w = lo >= 8 ? 8 : lo;
         lo -= w;
         const uint32_t dmask = (1u << w) - 1u;
-        hist[tg] = 0u;
-        hist[tg + GT] = 0u;
-        group_bar(bar);
         const unsigned long long want = prefix >> (lo + w);
+        const int s = group_step_begin(G);
+        uint32_t *h = G.hist + s * 256;
 #pragma unroll
-        for (int u = 0; u < PER; ++u)
-            if (use[u] && (static_cast<unsigned long long>(v[u]) >> (lo + w)) == want)
-                atomicAdd(&hist[(v[u] >> lo) & dmask], 1u);
-        group_bar(bar);
-        if (gw == 0) {
-            uint32_t cnt[8];
-            uint32_t sum = 0;
+        for (int i = 0; i < IPL; ++i) {
+            if (32 * i >= n) break;
+            uint32_t v;
+            if (item(i, v) && (static_cast<unsigned long long>(v) >> (lo + w)) == want)
+                atomicAdd(&h[(v >> lo) & dmask], 1u);
+        }
+        group_step_end(G);
+        // every warp finds the digit itself (no second barrier)
+        uint32_t cnt[8];
+        uint32_t sum = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            cnt[b] = h[255 - (G.lane * 8 + b)];
+            sum += cnt[b];
+        }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (G.lane >= o) incl += t;
+        }
+        const uint32_t excl = incl - sum;
+        const bool mine = excl < static_cast<uint32_t>(r.krem) && static_cast<uint32_t>(r.krem) <= incl;
+        int digit = 0;
+        uint32_t above = 0, e = 0;
+        if (mine) {
+            uint32_t acc = excl;
 #pragma unroll
             for (int b = 0; b < 8; ++b) {
-                cnt[b] = hist[255 - (lane * 8 + b)];
-                sum += cnt[b];
-            }
-            uint32_t incl = sum;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            const uint32_t excl = incl - sum;
-            if (excl < static_cast<uint32_t>(r.krem) && static_cast<uint32_t>(r.krem) <= incl) {
-                uint32_t acc = excl;
-#pragma unroll
-                for (int b = 0; b < 8; ++b) {
-                    if (acc + cnt[b] >= static_cast<uint32_t>(r.krem)) {
-                        ctl[0] = 255 - (lane * 8 + b);
-                        ctl[1] = static_cast<int>(acc);
-                        ctl[2] = static_cast<int>(cnt[b]);
-                        break;
-                    }
-                    acc += cnt[b];
+                if (acc + cnt[b] >= static_cast<uint32_t>(r.krem)) {
+                    digit = 255 - (G.lane * 8 + b);
+                    above = acc;
+                    e = cnt[b];
+                    break;
                 }
+                acc += cnt[b];
             }
         }
-        group_bar(bar);
-        const int digit = ctl[0];
-        r.krem -= ctl[1];
-        eq = ctl[2];
+        const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1;
+        digit = __shfl_sync(0xFFFFFFFFu, digit, src);
+        above = __shfl_sync(0xFFFFFFFFu, above, src);
+        e = __shfl_sync(0xFFFFFFFFu, e, src);
+        r.krem -= static_cast<int>(above);
+        eq = static_cast<int>(e);
         prefix |= static_cast<unsigned long long>(digit) << lo;
-        group_bar(bar);  // everyone has read ctl before it is written again
         if (eq == r.krem) break;
     }
     r.thr = static_cast<uint32_t>(prefix);
@@ -257,12 +293,11 @@ __device__ __forceinline__ RadixOut group_radix(const uint2 *stage, const int (&
     return r;
 }
 
-// Exact k best (key desc, block asc) of the staged union, plus the streaming
-// threshold a later (higher-index) block must reach: s >= *theta.
-__device__ __forceinline__ StagedRule group_select_exact(const uint2 *stage, const int (&n)[4], int k,
-                                                         uint32_t *hist, int *ctl, int tg, int bar,
+// Exact k best (key desc, block asc) of the group's items, plus the
+// streaming threshold a later (higher-index) block must reach: s >= *theta.
+__device__ __forceinline__ StagedRule group_select_exact(const uint2 (&it)[IPL], int n, int k, Group &G,
                                                          float *theta) {
-    const RadixOut r = group_radix<false, false>(stage, n, 0u, k, 8, hist, ctl, tg, bar);
+    const RadixOut r = group_radix<false, false>(it, n, 0u, k, 8, G);
     StagedRule rule;
     rule.thr_key = r.thr;
     rule.thr_nblk = 0;
@@ -272,48 +307,48 @@ __device__ __forceinline__ StagedRule group_select_exact(const uint2 *stage, con
         return rule;
     }
     // the k-th key is exactly r.thr; take the r.krem ties with the lowest blocks
-    const RadixOut r2 = group_radix<true, true>(stage, n, r.thr, r.krem, 8, hist, ctl, tg, bar);
+    const RadixOut r2 = group_radix<true, true>(it, n, r.thr, r.krem, 8, G);
     rule.by_bucket = 0;
     rule.thr_nblk = r2.thr;
     *theta = nextafterf(key2f(r.thr), INFINITY);
     return rule;
 }
 
-// Ranks of the kept staged items in staging order (u-major, then thread):
-// pos[u] for kept items; returns the number kept.  tab: 32 ints of the group.
-__device__ __forceinline__ int group_ranks(const bool (&kp)[PER], int (&pos)[PER], int *tab, int tg, int bar) {
-    const int lane = tg & 31, gw = tg >> 5;
-    unsigned ball[PER];
+// Hands every kept item to emit(item, rank), ranks counted warp by warp
+// (then entry order within the warp); returns the number kept.  One step.
+template <typename Keep, typename Emit>
+__device__ __forceinline__ int group_ranks_apply(const uint2 (&it)[IPL], int n, Keep keep, Emit emit, Group &G) {
+    int mine = 0;
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        ball[u] = __ballot_sync(0xFFFFFFFFu, kp[u]);
-        if (lane == 0) tab[u * 4 + gw] = __popc(ball[u]);
+    for (int i = 0; i < IPL; ++i) {
+        if (32 * i >= n) break;
+        mine += __popc(__ballot_sync(0xFFFFFFFFu, G.lane + 32 * i < n && keep(it[i])));
     }
-    group_bar(bar);
-    int run = 0;
+    const int s = group_step_begin(G);
+    int *c = G.ctl + s * 16;
+    if (G.lane == 0) c[G.gw] = mine;
+    group_step_end(G);
+    const int4 cw = *reinterpret_cast<const int4 *>(c);
+    int run = (G.gw > 0 ? cw.x : 0) + (G.gw > 1 ? cw.y : 0) + (G.gw > 2 ? cw.z : 0);
+    const unsigned ltmask = (1u << G.lane) - 1u;
 #pragma unroll
-    for (int u = 0; u < PER; ++u) {
-        int before = 0, all = 0;
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            const int c = tab[u * 4 + w];
-            before += w < gw ? c : 0;
-            all += c;
-        }
-        pos[u] = run + before + __popc(ball[u] & ((1u << lane) - 1u));
-        run += all;
+    for (int i = 0; i < IPL; ++i) {
+        if (32 * i >= n) break;
+        const bool kp = G.lane + 32 * i < n && keep(it[i]);
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, kp);
+        if (kp) emit(it[i], run + __popc(ball & ltmask));
+        run += __popc(ball);
     }
-    group_bar(bar);  // tab may be reused after this
-    return run;
+    return cw.x + cw.y + cw.z + cw.w;
 }
 
 // Ascending bitonic sort of 512 distinct keys held by the 128 threads of a
 // group, thread tg holding positions 4tg .. 4tg+3.  Partners one or two
 // positions away are in the same thread, up to 64 away in the same warp
 // (shuffles); the three steps that cross warps go through shared memory,
-// alternating between buf[0..511] and buf[512..1023].  The caller's initial
-// array may sit in buf[512..1023]: every thread has loaded its keys before
-// the first write to buf[0..511] passes a barrier.
+// alternating between buf[0..511] and buf[512..1023].  The caller's input may
+// sit in buf[512..1023]: the first write there comes after the barrier of
+// the first crossing step, which every thread reaches with its keys loaded.
 template <typename T>
 __device__ __forceinline__ void group_sort512(T (&v)[4], T *buf, int tg, int bar) {
     int flip = 0;
@@ -375,9 +410,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *sQ = smem + OFF_Q;
     uint8_t *sK = smem + OFF_K;
-    uint2 *sStage = reinterpret_cast<uint2 *>(smem + OFF_STAGE);
     int *sCtl = reinterpret_cast<int *>(smem + OFF_CTL);
     uint32_t *sHist = reinterpret_cast<uint32_t *>(smem + OFF_HIST);
+    unsigned long long *sSort = reinterpret_cast<unsigned long long *>(smem + OFF_SORT);
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sTheta = reinterpret_cast<float *>(smem + OFF_THETA);
     int *sCnt = reinterpret_cast<int *>(smem + OFF_CNT);  // sCnt[q * TQ + tl]
@@ -471,11 +506,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tc_fence_after();
                     const uint32_t d = tmem_base + buf * NCOL;
 #pragma unroll
-                    for (int ks = 0; ks < KSTEPS; ++ks) {
-                        const uint32_t half = ks >> 2, off = (ks & 3) * 32;
+                    for (int kx = 0; kx < KSTEPS; ++kx) {
+                        const uint32_t half = kx >> 2, off = (kx & 3) * 32;
                         const uint64_t ad = sdesc_sw128(sk_addr + st * SK_BYTES + half * (SK_BYTES / 2) + off);
                         const uint64_t bd = sdesc_sw128(sq_addr + half * (SQ_BYTES / 2) + off);
-                        tc_mma_bf16(d, ad, bd, IDESC, ks > 0 ? 1u : 0u);
+                        tc_mma_bf16(d, ad, bd, IDESC, kx > 0 ? 1u : 0u);
                     }
                     tc_commit(&empty[st]);
                     tc_commit(&tfull[buf]);
@@ -502,13 +537,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int g = e >> 2;          // group
         const int tg = quarter * 32 + lane;  // thread index within the group
         const int bar = 1 + g;         // hardware barrier id of the group
-        uint32_t *hist = sHist + g * 256;
-        int *ctl = sCtl + g * 64;      // [0..15] radix, [16..47] rank table
-        uint2 *stage = sStage + g * CAP;
+        Group G{sHist + g * HIST_INTS, sCtl + g * CTL_INTS, tg, lane, quarter, 1 + g, 0u};
+        unsigned long long *sort64 = sSort + g * 1024;  // [0..511] exchange, [512..1023] input
+        uint32_t *sort32 = reinterpret_cast<uint32_t *>(sort64);
         const unsigned ltmask = (1u << lane) - 1u;
         // this warp's sub-lists: token tl's at sub[tl * CAP]
         uint2 *sub = p.cand + static_cast<int64_t>(blockIdx.x) * TQ * CAP + quarter * SUB;
-        uint32_t acc = 0;
+        uint32_t acc = 0, nchk = 0;
         bool ok = true;
         for (int kk = blockIdx.x; kk < p.nq; kk += gridDim.x) {
             const int q = p.nq - 1 - kk;
@@ -534,26 +569,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int j = 0; j < nbt; ++j) {
                 const uint32_t buf = acc & 1;
                 const uint32_t use = acc >> 1;
-                const int par = static_cast<int>(acc & 1);
+                // lists are checked every CHK tiles and after the last one (that
+                // vote also makes sure the whole group goes on to the selection)
+                const bool last = j == nbt - 1;
+                const bool check = !DENSE && (last || (j + 1) % CHK == 0);
                 if (ok && !mbar_wait(&tfull[buf], use & 1)) ok = false;
-                if (!ok) {  // skip the work, keep taking part in the barriers
+                if (!ok) {  // skip the work, keep taking part in the votes
                     ++acc;
-                    if constexpr (!DENSE) {
-                        if (group_sync_fail(bar, true)) break;
-                    }
+                    if (check && group_sync_fail(bar, true)) break;
                     continue;
                 }
                 tc_fence_after();
                 const int64_t b = static_cast<int64_t>(j) * TB + quarter * 32 + lane;
                 const bool masked = !(tile_all_in && (static_cast<int64_t>(j) * TB + TB <= c_min));
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       buf * NCOL + g * (GTOK * kHI);
+                                       buf * NCOL + static_cast<uint32_t>(g * GCOL);
                 // 4 chunks of 4 tokens (16 columns), the load of chunk ch+1 in
                 // flight while chunk ch is scored
                 uint32_t ra[16], rb[16];
                 tmem_ld16(tbase, ra);
                 tmem_wait16(ra);
-                unsigned fl = 0;
                 // MASKED: the tile holds blocks that some of the tokens may not see
                 auto score_tile = [&](auto masked_c) {
                     constexpr bool MASKED = decltype(masked_c)::value;
@@ -587,29 +622,29 @@ __global__ void __launch_bounds__(THREADS, 1)
                             }
                         } else {
                             const float4 th = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
+                            const int4 c4 = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0]);
                             const float thv[4] = {th.x, th.y, th.z, th.w};
+                            bool pass[4];
                             unsigned m[4];
 #pragma unroll
                             for (int tk = 0; tk < 4; ++tk) {
                                 const int64_t t = t0 + tl0 + tk;
                                 const bool valid = !MASKED || ((t < p.L) && (b < (t >> 2)));
-                                m[tk] = __ballot_sync(0xFFFFFFFFu, valid && (sv[tk] >= thv[tk]));
+                                pass[tk] = valid && (sv[tk] >= thv[tk]);
+                                m[tk] = __ballot_sync(0xFFFFFFFFu, pass[tk]);
                             }
-                            // a block enters the token's list when s >= its threshold;
-                            // late in the scan most warps have no such block at all
+                            // a block enters the token's list when s >= its threshold
+                            // (no branch per token: the store is predicated)
                             if ((m[0] | m[1] | m[2] | m[3]) != 0u) {
-                                const int4 c4 = *reinterpret_cast<const int4 *>(&sCnt[quarter * TQ + tl0]);
+                                uint2 *base = sub + static_cast<int64_t>(tl0) * CAP;
                                 int cnt4[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                                 for (int tk = 0; tk < 4; ++tk) {
-                                    if (m[tk] == 0u) continue;  // warp-uniform
-                                    const bool pass = (m[tk] >> lane) & 1u;
                                     const int pos = cnt4[tk] + __popc(m[tk] & ltmask);
-                                    st_global_pred(sub + static_cast<int64_t>(tl0 + tk) * CAP + pos,
+                                    st_global_pred(base + tk * CAP + pos,
                                                    make_uint2(__float_as_uint(sv[tk]), static_cast<uint32_t>(b)),
-                                                   pass && pos < SUB);
+                                                   pass[tk] && pos < SUB);
                                     cnt4[tk] += __popc(m[tk]);
-                                    if (cnt4[tk] > SUB - 32) fl |= 1u << (ch * 4 + tk);
                                 }
                                 *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0]) =
                                     make_int4(cnt4[0], cnt4[1], cnt4[2], cnt4[3]);
@@ -624,54 +659,55 @@ __global__ void __launch_bounds__(THREADS, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&tempty[buf]);
                 ++acc;
-                if constexpr (!DENSE) {
-                    // lists that might overflow on the next tile get cut back
+                if (!check) continue;
+                // a sub-list that might overflow within the next CHK tiles gets
+                // cut back now (not needed after the last tile)
+                const int par = static_cast<int>(nchk & 1);
+                ++nchk;
+                if (!last) {
+                    const bool full_soon = lane < GTOK && sCnt[quarter * TQ + g * GTOK + lane] > FLAG_AT;
+                    const unsigned fl = __ballot_sync(0xFFFFFFFFu, full_soon);
                     if (fl && lane == 0) atomicOr(&sFlag[g * 2 + par], fl);
-                    if (group_sync_fail(bar, sMisc[1] != 0)) { ok = false; break; }
-                    unsigned flags = sFlag[g * 2 + par];
-                    while (flags) {
-                        const int t16 = __ffs(flags) - 1;
-                        flags &= flags - 1;
-                        const int tl = g * GTOK + t16;
-                        int n[4];
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq) n[qq] = sCnt[qq * TQ + tl];
-                        if (max(max(n[0], n[1]), max(n[2], n[3])) > SUB && tg == 0)
-                            report(p.status, QSA_ERR_DEVICE_CHECK);
-#pragma unroll
-                        for (int qq = 0; qq < 4; ++qq) n[qq] = min(n[qq], SUB);
-                        uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
-                        group_fetch(lst, n, stage, tg, bar);
-                        // cheap pass: a bucket bound 16 bits below the shared prefix
-                        const RadixOut r = group_radix<false, false>(stage, n, 0u, p.k_sel, 2, hist, ctl, tg, bar);
-                        float th;
-                        StagedRule rule{r.thr, 0u, 1};
-                        if ((p.k_sel - r.krem) + r.eq <= KEEP_MAX)
-                            th = r.lo == 0 ? nextafterf(key2f(r.thr), INFINITY) : key2f(r.thr);
-                        else
-                            rule = group_select_exact(stage, n, p.k_sel, hist, ctl, tg, bar, &th);
-                        // survivors back to the list, dealt round-robin over the 4 sub-lists
-                        uint2 it[PER];
-                        bool kp[PER];
-                        int pos[PER];
-#pragma unroll
-                        for (int u = 0; u < PER; ++u) {
-                            it[u] = stage[tg + GT * u];
-                            kp[u] = staged_valid(u, tg, n) && staged_keep(rule, it[u]);
-                        }
-                        const int kept = group_ranks(kp, pos, ctl + 16, tg, bar);
-#pragma unroll
-                        for (int u = 0; u < PER; ++u)
-                            if (kp[u])
-                                lst[(pos[u] & 3) * SUB + (pos[u] >> 2)] =
-                                    make_uint2(__float_as_uint(key2f(it[u].x)), it[u].y);
-                        if (tg < 4) sCnt[tg * TQ + tl] = (kept + 3 - tg) / 4;
-                        if (tg == 0) sTheta[tl] = th;
-                        group_bar(bar);  // stage, counts and list settled before the next token
-                    }
-                    if (group_sync_fail(bar, false)) { ok = false; break; }
-                    if (tg == 0) sFlag[g * 2 + par] = 0u;  // next written two tiles from now
                 }
+                if (group_sync_fail(bar, sMisc[1] != 0)) { ok = false; break; }
+                unsigned flags = last ? 0u : sFlag[g * 2 + par];
+                if (flags == 0u) continue;
+                while (flags) {
+                    const int t16 = __ffs(flags) - 1;
+                    flags &= flags - 1;
+                    const int tl = g * GTOK + t16;
+                    int n[4];
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) n[qq] = sCnt[qq * TQ + tl];
+                    if (max(max(n[0], n[1]), max(n[2], n[3])) > SUB && tg == 0)
+                        report(p.status, QSA_ERR_DEVICE_CHECK);
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) n[qq] = min(n[qq], SUB);
+                    uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
+                    const int nown = min(sCnt[quarter * TQ + tl], SUB);  // this warp's sub-list
+                    uint2 it[IPL];
+                    group_load(lst + quarter * SUB, nown, it, lane);
+                    // cheap pass: a bucket bound 16 bits below the shared prefix
+                    const RadixOut r = group_radix<false, false>(it, nown, 0u, p.k_sel, 2, G);
+                    float th;
+                    StagedRule rule{r.thr, 0u, 1};
+                    if ((p.k_sel - r.krem) + r.eq <= KEEP_MAX)
+                        th = r.lo == 0 ? nextafterf(key2f(r.thr), INFINITY) : key2f(r.thr);
+                    else
+                        rule = group_select_exact(it, nown, p.k_sel, G, &th);
+                    // survivors back to the list (every warp has its items in
+                    // registers by now), dealt round-robin over the 4 sub-lists
+                    const int kept = group_ranks_apply(
+                        it, nown, [&](uint2 e) { return staged_keep(rule, e); },
+                        [&](uint2 e, int pos) {
+                            lst[(pos & 3) * SUB + (pos >> 2)] = make_uint2(__float_as_uint(key2f(e.x)), e.y);
+                        },
+                        G);
+                    if (tg < 4) sCnt[tg * TQ + tl] = (kept + 3 - tg) / 4;
+                    if (tg == 0) sTheta[tl] = th;
+                }
+                if (group_sync_fail(bar, false)) { ok = false; break; }
+                if (tg == 0) sFlag[g * 2 + par] = 0u;  // next written two checks from now
             }
             if (!ok) continue;  // the next tile-start barrier takes everyone out
             if constexpr (!DENSE) {
@@ -686,29 +722,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                     for (int qq = 0; qq < 4; ++qq) n[qq] = min(sCnt[qq * TQ + tl], SUB);
                     const int ntot = n[0] + n[1] + n[2] + n[3];
                     const uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
-                    group_fetch(lst, n, stage, tg, bar);
+                    const int nown = min(sCnt[quarter * TQ + tl], SUB);  // this warp's sub-list
+                    uint2 it[IPL];
+                    group_load(lst + quarter * SUB, nown, it, lane);
                     StagedRule rule{0u, 0u, 1};
                     if (ntot > p.k_sel) {
                         float th;
-                        rule = group_select_exact(stage, n, p.k_sel, hist, ctl, tg, bar, &th);
+                        rule = group_select_exact(it, nown, p.k_sel, G, &th);
                     }
-                    uint2 it[PER];
-                    bool kp[PER];
-                    int pos[PER];
-#pragma unroll
-                    for (int u = 0; u < PER; ++u) {
-                        it[u] = stage[tg + GT * u];
-                        kp[u] = staged_valid(u, tg, n) && staged_keep(rule, it[u]);
-                    }
-                    int m = group_ranks(kp, pos, ctl + 16, tg, bar);  // also: all stage reads done
-                    if (m > 512) {
-                        if (tg == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
-                        m = 512;
-                    }
+                    auto keep = [&](uint2 e) { return staged_keep(rule, e); };
                     // order by block (blocks are distinct): a group sort of 512 keys,
-                    // block indices alone or (block, score bits) when scores are written
+                    // block indices alone or (block, score bits) when scores are written.
+                    // The sort input sits in slots 512.. of the group's sort area; the
+                    // sort's own first write goes to slots 0..511 (see group_sort512).
                     int32_t *row = p.idx + t * p.budget;
                     float *srow = p.score ? p.score + t * p.budget : nullptr;
+                    int m;
                     auto emit = [&](int e, uint32_t blk, float sc) {
                         if (e >= p.budget) return;
                         const bool in = e < m;
@@ -716,33 +745,43 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (srow) srow[e] = in ? sc : (e == m ? INFINITY : -INFINITY);
                     };
                     if (srow) {
-                        unsigned long long *sb = reinterpret_cast<unsigned long long *>(stage);
-#pragma unroll
-                        for (int u = 0; u < PER; ++u)
-                            if (kp[u] && pos[u] < 512)
-                                sb[512 + pos[u]] = (static_cast<unsigned long long>(it[u].y) << 32) |
-                                                   __float_as_uint(key2f(it[u].x));
-                        for (int i = m + tg; i < 512; i += GT) sb[512 + i] = ~0ull;
+                        m = group_ranks_apply(
+                            it, nown, keep,
+                            [&](uint2 e, int pos) {
+                                if (pos < 512)
+                                    sort64[512 + pos] = (static_cast<unsigned long long>(e.y) << 32) |
+                                                        __float_as_uint(key2f(e.x));
+                            },
+                            G);
                         group_bar(bar);
+                        if (m > 512) {
+                            if (tg == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
+                            m = 512;
+                        }
                         unsigned long long v[4];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) v[r] = sb[512 + 4 * tg + r];
-                        group_sort512(v, sb, tg, bar);
+                        for (int r = 0; r < 4; ++r) v[r] = 4 * tg + r < m ? sort64[512 + 4 * tg + r] : ~0ull;
+                        group_sort512(v, sort64, tg, bar);
 #pragma unroll
                         for (int r = 0; r < 4; ++r)
                             emit(4 * tg + r, static_cast<uint32_t>(v[r] >> 32),
                                  __uint_as_float(static_cast<uint32_t>(v[r])));
                     } else {
-                        uint32_t *sb = reinterpret_cast<uint32_t *>(stage);
-#pragma unroll
-                        for (int u = 0; u < PER; ++u)
-                            if (kp[u] && pos[u] < 512) sb[512 + pos[u]] = it[u].y;
-                        for (int i = m + tg; i < 512; i += GT) sb[512 + i] = 0xFFFFFFFFu;
+                        m = group_ranks_apply(
+                            it, nown, keep,
+                            [&](uint2 e, int pos) {
+                                if (pos < 512) sort32[512 + pos] = e.y;
+                            },
+                            G);
                         group_bar(bar);
+                        if (m > 512) {
+                            if (tg == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
+                            m = 512;
+                        }
                         uint32_t v[4];
 #pragma unroll
-                        for (int r = 0; r < 4; ++r) v[r] = sb[512 + 4 * tg + r];
-                        group_sort512(v, sb, tg, bar);
+                        for (int r = 0; r < 4; ++r) v[r] = 4 * tg + r < m ? sort32[512 + 4 * tg + r] : 0xFFFFFFFFu;
+                        group_sort512(v, sort32, tg, bar);
                         const int e0 = 4 * tg;
                         if ((p.budget & 3) == 0 && e0 + 3 < m) {
                             *reinterpret_cast<int4 *>(row + e0) = make_int4(
@@ -753,7 +792,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int r = 0; r < 4; ++r) emit(e0 + r, v[r], 0.f);
                         }
                     }
-                    group_bar(bar);  // sortb (= stage) is reused by the next token
                 }
             }
         }
