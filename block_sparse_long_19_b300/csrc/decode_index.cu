@@ -305,7 +305,6 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
     unsigned long long *sortb = reinterpret_cast<unsigned long long *>(items + cap);
     uint32_t *hist = reinterpret_cast<uint32_t *>(sortb + kMaxBudget);
     int *ctl = reinterpret_cast<int *>(hist + 256);
-    int *offs = ctl + 8;  // [MAX_NCHUNK + 1]; ctl uses 8 ints
 
     const int s = blockIdx.x;
     const int64_t T = p.seq_lens[s];
@@ -316,63 +315,62 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
         return;
     }
     const int64_t c = (T - 1) / kBlock;
-    // chunk counts in parallel, then every candidate slot of every chunk
-    // flattened over the threads (order does not matter: the selection is
-    // order-free and the output is sorted by block)
-    for (int ch = threadIdx.x; ch < p.nchunk; ch += MERGE_THREADS)
-        offs[ch] = p.k_sel > 0 ? p.cnt[static_cast<int64_t>(s) * p.nchunk + ch] : 0;
+    // every warp takes whole chunks: all of a chunk's candidate loads in
+    // flight at once, the ones at or above the bound appended with one
+    // shared atomic per warp
     if (threadIdx.x == 0) ctl[3] = 0;
     __syncthreads();
-    const int slots = p.nchunk * p.k_sel;
-    const uint2 *src = p.cand + static_cast<int64_t>(s) * p.nchunk * p.k_sel;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const unsigned ltmask = (1u << lane) - 1u;
     const uint32_t bound = p.thr ? p.thr[s] : 0u;
-    constexpr int U = 8;
-    for (int base = threadIdx.x; base < slots; base += MERGE_THREADS * U) {
-        uint2 it[U];
-        bool ok[U];
+    constexpr int PER_LANE = (MAX_SEL + 31) / 32;
+    for (int ch = warp; ch < p.nchunk; ch += MERGE_THREADS / 32) {
+        const int cnt = p.k_sel > 0 ? min(p.cnt[static_cast<int64_t>(s) * p.nchunk + ch], p.k_sel) : 0;
+        const uint2 *src = p.cand + (static_cast<int64_t>(s) * p.nchunk + ch) * p.k_sel;
+        uint2 it[PER_LANE];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int j = base + u * MERGE_THREADS;
-            ok[u] = false;
-            if (j < slots) {
-                const int ch = j / p.k_sel;
-                ok[u] = (j - ch * p.k_sel) < offs[ch];
-                if (ok[u]) {
-                    it[u] = src[j];
-                    ok[u] = f2key(__uint_as_float(it[u].x)) >= bound;
-                }
-            }
+        for (int u = 0; u < PER_LANE; ++u) {
+            const int i = u * 32 + lane;
+            it[u] = i < cnt ? src[i] : make_uint2(0u, 0u);
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u)
-            if (ok[u]) {
-                const int pos = atomicAdd(&ctl[3], 1);
-                if (pos < cap) items[pos] = it[u];
-            }
+        for (int u = 0; u < PER_LANE; ++u) {
+            if (u * 32 >= cnt) break;
+            const bool ok = u * 32 + lane < cnt && f2key(__uint_as_float(it[u].x)) >= bound;
+            const unsigned ball = __ballot_sync(0xFFFFFFFFu, ok);
+            if (!ball) continue;
+            int base = 0;
+            if (lane == 0) base = atomicAdd(&ctl[3], __popc(ball));
+            base = __shfl_sync(0xFFFFFFFFu, base, 0);
+            const int pos = base + __popc(ball & ltmask);
+            if (ok && pos < cap) items[pos] = it[u];
+        }
     }
     __syncthreads();
     const int n = min(ctl[3], cap);
     __syncthreads();
-    int m = n;
     SelectRule rule{0u, 0u, 1};
-    if (n > p.k_sel) {
+    if (n > p.k_sel)
         rule = cta_select<MERGE_THREADS>(
             n, p.k_sel, [&](int i) { return __uint_as_float(items[i].x); },
             [&](int i) { return items[i].y; }, hist, ctl);
-        m = p.k_sel;
-    }
     if (threadIdx.x == 0) ctl[3] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += MERGE_THREADS) {
-        if (n <= p.k_sel || selected(rule, __uint_as_float(items[i].x), items[i].y)) {
-            const int pos = atomicAdd(&ctl[3], 1);
-            if (pos < kMaxBudget) sortb[pos] = (static_cast<unsigned long long>(items[i].y) << 32) | items[i].x;
-        }
+    for (int i0 = 0; i0 < n; i0 += MERGE_THREADS) {
+        const int i = i0 + threadIdx.x;
+        const bool sel = i < n && (n <= p.k_sel || selected(rule, __uint_as_float(items[i].x), items[i].y));
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, sel);
+        if (!ball) continue;
+        int base = 0;
+        if (lane == 0) base = atomicAdd(&ctl[3], __popc(ball));
+        base = __shfl_sync(0xFFFFFFFFu, base, 0);
+        const int pos = base + __popc(ball & ltmask);
+        if (sel && pos < kMaxBudget) sortb[pos] = (static_cast<unsigned long long>(items[i].y) << 32) | items[i].x;
     }
     __syncthreads();
     // order by block: blocks are distinct, so an item's place is the number
     // of smaller blocks (every thread scans the list with broadcast reads)
-    m = min(ctl[3], kMaxBudget);
+    const int m = min(ctl[3], kMaxBudget);
     for (int i = threadIdx.x; i < m; i += MERGE_THREADS) {
         const uint32_t bi = static_cast<uint32_t>(sortb[i] >> 32);
         int rank = 0;

@@ -91,6 +91,43 @@ struct Params {
     int32_t *status;
 };
 
+// One TMEM load of 16 columns and its completion wait in a single statement:
+// the chunk's values are ordinary outputs, so nothing can read them early
+// and the compiler needs no register ties across the wait.
+__device__ __forceinline__ void tmem_load16_sync(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Bounded wait on an mbarrier phase that lets the hardware suspend the
+// thread until the phase completes (up to a microsecond per try) instead of
+// spinning on the issue slots the epilogue warps need.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
+    auto try_once = [&]() {
+        uint32_t done;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+            : "memory");
+        return done != 0;
+    };
+    if (try_once()) return true;
+    const unsigned long long t0 = globaltimer();
+    while (!try_once())
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
 // Barrier among the 4 warps (128 threads) of one epilogue group that is also a
 // vote: every thread gets the OR of all `fail` flags, so a group always
 // leaves together (a warp that left alone would strand the others at the next
@@ -406,8 +443,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     index_kernel(const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_k,
                  Params p) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // aligned by pointer arithmetic on the shared array itself (a round trip
+    // through an integer would hide the state space and turn every access
+    // into a generic one)
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint8_t *sQ = smem + OFF_Q;
     uint8_t *sK = smem + OFF_K;
     int *sCtl = reinterpret_cast<int *>(smem + OFF_CTL);
@@ -470,7 +509,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_2d(sQ + SQ_BYTES / 2, &map_q, qfull, 64, q * NCOL);
                 for (int j = 0; j < nbt; ++j) {
                     if (sMisc[1]) { ok = false; break; }
-                    if (!mbar_wait(&empty[st], ph ^ 1)) { ok = false; break; }
+                    if (!mbar_wait_sleep(&empty[st], ph ^ 1)) { ok = false; break; }
                     uint8_t *dst = sK + st * SK_BYTES;
                     mbar_arrive_expect_tx(&full[st], SK_BYTES);
                     tma_load_2d(dst, &map_k, &full[st], 0, j * TB);
@@ -501,8 +540,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (sMisc[1]) { ok = false; break; }
                     const uint32_t buf = acc & 1;
                     const uint32_t use = acc >> 1;
-                    if (!mbar_wait(&tempty[buf], (use & 1) ^ 1)) { ok = false; break; }
-                    if (!mbar_wait(&full[st], ph)) { ok = false; break; }
+                    if (!mbar_wait_sleep(&tempty[buf], (use & 1) ^ 1)) { ok = false; break; }
+                    if (!mbar_wait_sleep(&full[st], ph)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d = tmem_base + buf * NCOL;
 #pragma unroll
@@ -573,7 +612,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // vote also makes sure the whole group goes on to the selection)
                 const bool last = j == nbt - 1;
                 const bool check = !DENSE && (last || (j + 1) % CHK == 0);
-                if (ok && !mbar_wait(&tfull[buf], use & 1)) ok = false;
+                if (ok && !mbar_wait_sleep(&tfull[buf], use & 1)) ok = false;
                 if (!ok) {  // skip the work, keep taking part in the votes
                     ++acc;
                     if (check && group_sync_fail(bar, true)) break;
@@ -584,19 +623,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool masked = !(tile_all_in && (static_cast<int64_t>(j) * TB + TB <= c_min));
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        buf * NCOL + static_cast<uint32_t>(g * GCOL);
-                // 4 chunks of 4 tokens (16 columns), the load of chunk ch+1 in
-                // flight while chunk ch is scored
-                uint32_t ra[16], rb[16];
-                tmem_ld16(tbase, ra);
-                tmem_wait16(ra);
+                // 4 chunks of 4 tokens (16 columns each); the TMEM load latency is
+                // short next to a chunk's arithmetic, so each chunk loads and waits
+                uint32_t cur[16];
                 // MASKED: the tile holds blocks that some of the tokens may not see
                 auto score_tile = [&](auto masked_c) {
                     constexpr bool MASKED = decltype(masked_c)::value;
 #pragma unroll
                     for (int ch = 0; ch < GTOK / 4; ++ch) {
-                        uint32_t(&cur)[16] = (ch & 1) ? rb : ra;
-                        uint32_t(&nxt)[16] = (ch & 1) ? ra : rb;
-                        if (ch < GTOK / 4 - 1) tmem_ld16(tbase + (ch + 1) * 16, nxt);
+                        tmem_load16_sync(tbase + ch * 16, cur);
                         const int tl0 = g * GTOK + ch * 4;
                         // s = sum_h w_h * max(0, x_h) for two tokens per packed FMA,
                         // heads in order 0..3, the first product added to +0 (the
@@ -650,7 +685,6 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     make_int4(cnt4[0], cnt4[1], cnt4[2], cnt4[3]);
                             }
                         }
-                        if (ch < GTOK / 4 - 1) tmem_wait16(nxt);
                     }
                 };
                 if (masked) score_tile(std::true_type{});
