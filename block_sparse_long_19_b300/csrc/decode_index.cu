@@ -10,12 +10,18 @@
 //     16 blocks at a time with 16-byte loads straight into the warp-MMA
 //     operand registers (the contraction order inside a 32-dim slice is
 //     permuted identically on both operands, which leaves the dot products
-//     unchanged), forms s = sum_h w_h max(0, qi_h . kblk) and keeps the chunk's
-//     scores in shared memory; a CTA-wide radix select then writes the chunk's
-//     exact top-(budget-1) (score desc, block asc) as candidates;
-//   * merge kernel: one CTA per sequence selects the final (budget-1) among
-//     the chunks' candidates, sorts them by block and appends the current
-//     block.
+//     unchanged) and forms s = sum_h w_h max(0, qi_h . kblk).  The chunk's
+//     scores go to the workspace (L2-resident: 4 B per block), and a CTA
+//     radix step finds the chunk's kc-th best score with kc = ceil((budget-1)
+//     / (chunks - 1)): every full chunk holds kc blocks at or above its own
+//     value, so the smallest value over the chunks is a lower bound of the
+//     sequence's (budget-1)-th best score;
+//   * filter kernel: every block whose score reaches that bound becomes a
+//     candidate (on i.i.d. scores about twice the budget survive);
+//   * merge kernel: one CTA per sequence selects the exact (budget-1) best
+//     candidates (score desc, block asc), sorts them by block and appends the
+//     current block.  If ties leave more candidates than the candidate area
+//     holds, it selects over all of the sequence's scores instead.
 #include "qsa_common.cuh"
 #include "qsa_kernels.h"
 #include "qsa_select.cuh"
@@ -27,7 +33,9 @@ constexpr int SCAN_THREADS = 256;
 constexpr int MAX_CHUNK = 16384;
 constexpr int MAX_NCHUNK = 47;
 constexpr int MERGE_THREADS = 1024;
-constexpr int MAX_SEL = kMaxBudget - 1;
+constexpr int FILTER_THREADS = 256;
+constexpr int FILTER_PER_THREAD = 8;
+constexpr int CAND_CAP = 8192;  // filtered candidates kept per sequence
 
 // CTA-wide radix step over n items: value(i) -> uint32, pred(i) -> bool.
 // Finds a bucket [thr, thr + 2^lo) holding the k-th largest value, looking
@@ -174,9 +182,8 @@ struct ScanParams {
     int64_t chunk;
     int nchunk;
     int k_sel;
-    uint2 *cand;               // [B, nchunk, k_sel]
-    int32_t *cnt;              // [B, nchunk]
-    uint32_t *thr;             // [B] running max of the chunks' (budget-1)-th best key
+    float *scores;             // [B, max_ctx/4]
+    uint32_t *lb_inv;          // [B] ~(lower bound key), combined by atomicMax (0 = none yet)
     int32_t *status;
 };
 
@@ -190,22 +197,15 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     const int ch = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t T = p.seq_lens[s];
-    int32_t *cnt_out = p.cnt + static_cast<int64_t>(s) * p.nchunk + ch;
     if (T < 1 || T > p.max_ctx) {
-        if (threadIdx.x == 0) {
-            report(p.status, QSA_ERR_DEVICE_CHECK);
-            *cnt_out = 0;
-        }
+        if (threadIdx.x == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
         return;
     }
     const int64_t c = (T - 1) / kBlock;  // past blocks 0..c-1
     const int64_t b0 = static_cast<int64_t>(ch) * p.chunk;
     int64_t b1 = b0 + p.chunk;
     if (b1 > c) b1 = c;
-    if (b0 >= b1) {
-        if (threadIdx.x == 0) *cnt_out = 0;
-        return;
-    }
+    if (b0 >= b1) return;
     const int n = static_cast<int>(b1 - b0);
 
     // B operand: qi^T, columns = heads (4 live of 8), loaded once
@@ -251,58 +251,100 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     }
     __syncthreads();
 
-    uint2 *out = p.cand + (static_cast<int64_t>(s) * p.nchunk + ch) * p.k_sel;
-    if (n <= p.k_sel) {
-        for (int i = threadIdx.x; i < n; i += SCAN_THREADS)
-            out[i] = make_uint2(__float_as_uint(sc[i]), static_cast<uint32_t>(b0 + i));
-        if (threadIdx.x == 0) *cnt_out = n;
-        return;
+    float *srow = p.scores + static_cast<int64_t>(s) * (p.max_ctx / kBlock);
+    for (int i = threadIdx.x; i < n; i += SCAN_THREADS) srow[b0 + i] = sc[i];
+    if (c <= p.k_sel) return;  // every past block is selected
+    const int64_t nch_s = (c + p.chunk - 1) / p.chunk;
+    const int kc = nch_s == 1 ? p.k_sel : static_cast<int>((p.k_sel + nch_s - 2) / (nch_s - 1));
+    if (n < kc) return;  // a short last chunk: the full chunks already cover the bound
+    const RadixOut r = cta_radix<SCAN_THREADS>(
+        n, kc, [&](int i) { return f2key(sc[i]); }, [&](int) { return true; }, hist, ctl);
+    // at least kc of this chunk's keys are >= r.thr
+    if (threadIdx.x == 0) atomicMax(&p.lb_inv[s], ~r.thr);
+}
+
+struct FilterParams {
+    const int32_t *seq_lens;
+    int64_t max_ctx;
+    int k_sel;
+    const float *scores;     // [B, max_ctx/4]
+    const uint32_t *lb_inv;  // [B]
+    uint2 *cand;             // [B, CAND_CAP] {score bits, block}
+    int32_t *ccount;         // [B]
+};
+
+// Candidates: the past blocks whose score key reaches the sequence's bound.
+// One global atomic per CTA reserves the CTA's range of the candidate area
+// (the sequences' counters share cache lines, so per-warp atomics from every
+// CTA would queue up at one L2 slice).
+__global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) {
+    __shared__ int s_warp[FILTER_THREADS / 32 + 1];
+    const int s = blockIdx.y;
+    const int64_t T = p.seq_lens[s];
+    if (T < 1 || T > p.max_ctx) return;
+    const int64_t c = (T - 1) / kBlock;
+    if (c <= p.k_sel) return;
+    const uint32_t bound = ~p.lb_inv[s];
+    const float *srow = p.scores + static_cast<int64_t>(s) * (p.max_ctx / kBlock);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned ltmask = (1u << lane) - 1u;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * FILTER_THREADS * FILTER_PER_THREAD;
+    float v[FILTER_PER_THREAD];
+    unsigned ball[FILTER_PER_THREAD];
+    int mine = 0;
+#pragma unroll
+    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
+        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
+        v[u] = b < c ? __ldcg(srow + b) : -INFINITY;
     }
-    const SelectRule rule = cta_select<SCAN_THREADS>(
-        n, p.k_sel, [&](int i) { return sc[i]; },
-        [&](int i) { return static_cast<uint32_t>(b0 + i); }, hist, ctl);
-    // This chunk holds budget-1 blocks whose keys are >= rule.thr_key, so the
-    // sequence's (budget-1)-th best key is >= it too: publish it.  Candidates
-    // below the largest bound published so far can never be selected.
-    if (threadIdx.x == 0) {
-        const uint32_t old = atomicMax(&p.thr[s], rule.thr_key);
-        ctl[7] = static_cast<int>(max(old, rule.thr_key));
-        ctl[3] = 0;
+#pragma unroll
+    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
+        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
+        ball[u] = __ballot_sync(0xFFFFFFFFu, b < c && f2key(v[u]) >= bound);
+        mine += __popc(ball[u]);
     }
+    if (lane == 0) s_warp[warp] = mine;
     __syncthreads();
-    const uint32_t bound = static_cast<uint32_t>(ctl[7]);
-    for (int i = threadIdx.x; i < n; i += SCAN_THREADS) {
-        if (selected(rule, sc[i], static_cast<uint32_t>(b0 + i)) && f2key(sc[i]) >= bound) {
-            const int pos = atomicAdd(&ctl[3], 1);
-            if (pos < p.k_sel)
-                out[pos] = make_uint2(__float_as_uint(sc[i]), static_cast<uint32_t>(b0 + i));
+    if (threadIdx.x == 0) {
+        int tot = 0;
+        for (int w = 0; w < FILTER_THREADS / 32; ++w) {
+            const int x = s_warp[w];
+            s_warp[w] = tot;
+            tot += x;
         }
+        s_warp[FILTER_THREADS / 32] = tot > 0 ? atomicAdd(&p.ccount[s], tot) : 0;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-        if (ctl[3] > p.k_sel) report(p.status, QSA_ERR_DEVICE_CHECK);
-        *cnt_out = min(ctl[3], p.k_sel);
+    int pos = s_warp[FILTER_THREADS / 32] + s_warp[warp];
+#pragma unroll
+    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
+        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
+        if ((ball[u] >> lane) & 1u) {
+            const int at = pos + __popc(ball[u] & ltmask);
+            if (at < CAND_CAP)
+                p.cand[static_cast<int64_t>(s) * CAND_CAP + at] =
+                    make_uint2(__float_as_uint(v[u]), static_cast<uint32_t>(b));
+        }
+        pos += __popc(ball[u]);
     }
 }
 
 struct MergeParams {
     const int32_t *seq_lens;
     int64_t max_ctx;
-    int nchunk;
     int k_sel;
     int budget;
-    const uint2 *cand;
-    const int32_t *cnt;
-    const uint32_t *thr;  // [B] lower bound of the (budget-1)-th best key (null: none)
-    int32_t *idx;   // [B, budget]
+    const float *scores;    // [B, max_ctx/4] (used when the candidates overflowed)
+    const uint2 *cand;      // [B, CAND_CAP]
+    const int32_t *ccount;  // [B]
+    int32_t *idx;           // [B, budget]
     int32_t *status;
 };
 
 __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint2 *items = reinterpret_cast<uint2 *>(smem);
-    const int cap = MAX_NCHUNK * MAX_SEL;
-    unsigned long long *sortb = reinterpret_cast<unsigned long long *>(items + cap);
+    unsigned long long *sortb = reinterpret_cast<unsigned long long *>(items + CAND_CAP);
     uint32_t *hist = reinterpret_cast<uint32_t *>(sortb + kMaxBudget);
     int *ctl = reinterpret_cast<int *>(hist + 256);
 
@@ -315,62 +357,50 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
         return;
     }
     const int64_t c = (T - 1) / kBlock;
-    // every warp takes whole chunks: all of a chunk's candidate loads in
-    // flight at once, the ones at or above the bound appended with one
-    // shared atomic per warp
-    if (threadIdx.x == 0) ctl[3] = 0;
-    __syncthreads();
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (c <= p.k_sel) {  // every past block, then the current one
+        for (int i = threadIdx.x; i < p.budget; i += MERGE_THREADS)
+            row[i] = i < c ? i : (i == c ? static_cast<int32_t>(c) : -1);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
     const unsigned ltmask = (1u << lane) - 1u;
-    const uint32_t bound = p.thr ? p.thr[s] : 0u;
-    constexpr int PER_LANE = (MAX_SEL + 31) / 32;
-    for (int ch = warp; ch < p.nchunk; ch += MERGE_THREADS / 32) {
-        const int cnt = p.k_sel > 0 ? min(p.cnt[static_cast<int64_t>(s) * p.nchunk + ch], p.k_sel) : 0;
-        const uint2 *src = p.cand + (static_cast<int64_t>(s) * p.nchunk + ch) * p.k_sel;
-        uint2 it[PER_LANE];
-#pragma unroll
-        for (int u = 0; u < PER_LANE; ++u) {
-            const int i = u * 32 + lane;
-            it[u] = i < cnt ? src[i] : make_uint2(0u, 0u);
-        }
-#pragma unroll
-        for (int u = 0; u < PER_LANE; ++u) {
-            if (u * 32 >= cnt) break;
-            const bool ok = u * 32 + lane < cnt && f2key(__uint_as_float(it[u].x)) >= bound;
-            const unsigned ball = __ballot_sync(0xFFFFFFFFu, ok);
-            if (!ball) continue;
-            int base = 0;
-            if (lane == 0) base = atomicAdd(&ctl[3], __popc(ball));
-            base = __shfl_sync(0xFFFFFFFFu, base, 0);
-            const int pos = base + __popc(ball & ltmask);
-            if (ok && pos < cap) items[pos] = it[u];
-        }
+    const int nc = p.ccount[s];
+    const bool direct = nc > CAND_CAP;  // ties flooded the candidate area
+    const int n = direct ? static_cast<int>(c) : nc;
+    const float *srow = p.scores + static_cast<int64_t>(s) * (p.max_ctx / kBlock);
+    if (!direct) {
+        const uint2 *src = p.cand + static_cast<int64_t>(s) * CAND_CAP;
+        for (int i = threadIdx.x; i < n; i += MERGE_THREADS) items[i] = __ldcg(src + i);
     }
     __syncthreads();
-    const int n = min(ctl[3], cap);
-    __syncthreads();
+    auto score = [&](int i) { return direct ? __ldcg(srow + i) : __uint_as_float(items[i].x); };
+    auto block = [&](int i) { return direct ? static_cast<uint32_t>(i) : items[i].y; };
     SelectRule rule{0u, 0u, 1};
-    if (n > p.k_sel)
-        rule = cta_select<MERGE_THREADS>(
-            n, p.k_sel, [&](int i) { return __uint_as_float(items[i].x); },
-            [&](int i) { return items[i].y; }, hist, ctl);
+    if (n > p.k_sel) rule = cta_select<MERGE_THREADS>(n, p.k_sel, score, block, hist, ctl);
     if (threadIdx.x == 0) ctl[3] = 0;
     __syncthreads();
     for (int i0 = 0; i0 < n; i0 += MERGE_THREADS) {
         const int i = i0 + threadIdx.x;
-        const bool sel = i < n && (n <= p.k_sel || selected(rule, __uint_as_float(items[i].x), items[i].y));
+        float sv = 0.f;
+        uint32_t bv = 0u;
+        if (i < n) {
+            sv = score(i);
+            bv = block(i);
+        }
+        const bool sel = i < n && (n <= p.k_sel || selected(rule, sv, bv));
         const unsigned ball = __ballot_sync(0xFFFFFFFFu, sel);
         if (!ball) continue;
-        int base = 0;
-        if (lane == 0) base = atomicAdd(&ctl[3], __popc(ball));
-        base = __shfl_sync(0xFFFFFFFFu, base, 0);
-        const int pos = base + __popc(ball & ltmask);
-        if (sel && pos < kMaxBudget) sortb[pos] = (static_cast<unsigned long long>(items[i].y) << 32) | items[i].x;
+        int pos0 = 0;
+        if (lane == 0) pos0 = atomicAdd(&ctl[3], __popc(ball));
+        pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
+        const int pos = pos0 + __popc(ball & ltmask);
+        if (sel && pos < kMaxBudget) sortb[pos] = (static_cast<unsigned long long>(bv) << 32) | __float_as_uint(sv);
     }
     __syncthreads();
+    const int m = min(ctl[3], p.k_sel);
+    if (threadIdx.x == 0 && ctl[3] != p.k_sel) report(p.status, QSA_ERR_DEVICE_CHECK);
     // order by block: blocks are distinct, so an item's place is the number
     // of smaller blocks (every thread scans the list with broadcast reads)
-    const int m = min(ctl[3], kMaxBudget);
     for (int i = threadIdx.x; i < m; i += MERGE_THREADS) {
         const uint32_t bi = static_cast<uint32_t>(sortb[i] >> 32);
         int rank = 0;
@@ -407,18 +437,25 @@ DecodePlan decode_plan(int batch, int64_t max_ctx, int sms) {
 
 static size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Workspace of the decode indexer: scores, candidates, counters.
+static size_t index_ws_bytes(int batch, int64_t max_ctx) {
+    size_t b = 0;
+    b += align256(static_cast<size_t>(batch) * (max_ctx / kBlock) * sizeof(float));      // scores
+    b += align256(static_cast<size_t>(batch) * dx::CAND_CAP * sizeof(uint2));            // cand
+    b += align256(static_cast<size_t>(batch) * 2 * sizeof(uint32_t));                    // ccount, lb_inv
+    return b;
+}
+
 size_t decode_ws_bytes(int batch, int64_t max_ctx, int budget, int sms) {
     const DecodePlan pl = decode_plan(batch, max_ctx, sms);
-    const int k_sel = budget - 1 > 0 ? budget - 1 : 1;
-    size_t b = 0;
-    b += align256(static_cast<size_t>(batch) * pl.nchunk * k_sel * sizeof(uint2));   // cand
-    b += align256(static_cast<size_t>(batch) * pl.nchunk * sizeof(int32_t));         // cnt
-    b += align256(static_cast<size_t>(batch) * sizeof(uint32_t));                    // thr
+    size_t b = index_ws_bytes(batch, max_ctx);
     b += align256(static_cast<size_t>(batch) * budget * sizeof(int32_t));            // idx
     b += align256(static_cast<size_t>(batch) * pl.nsplit * kHQ * kD * sizeof(float)); // part_o
     b += align256(static_cast<size_t>(batch) * pl.nsplit * kHQ * sizeof(float));      // part_lse
     return b;
 }
+
+size_t decode_index_ws_bytes(int batch, int64_t max_ctx) { return index_ws_bytes(batch, max_ctx); }
 
 cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &plan,
                                 const uint16_t *qi, const uint16_t *w, const uint16_t *kblk,
@@ -426,15 +463,15 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
                                 int32_t *status, cudaStream_t stream) {
     const int k_sel = budget - 1;
     uint8_t *base = static_cast<uint8_t *>(ws);
-    const int k_alloc = k_sel > 0 ? k_sel : 1;
+    float *scores = reinterpret_cast<float *>(base);
+    base += align256(static_cast<size_t>(batch) * (max_ctx / kBlock) * sizeof(float));
     uint2 *cand = reinterpret_cast<uint2 *>(base);
-    base += align256(static_cast<size_t>(batch) * plan.nchunk * k_alloc * sizeof(uint2));
-    int32_t *cnt = reinterpret_cast<int32_t *>(base);
-    base += align256(static_cast<size_t>(batch) * plan.nchunk * sizeof(int32_t));
-    uint32_t *thr = reinterpret_cast<uint32_t *>(base);
+    base += align256(static_cast<size_t>(batch) * dx::CAND_CAP * sizeof(uint2));
+    int32_t *ccount = reinterpret_cast<int32_t *>(base);
+    uint32_t *lb_inv = reinterpret_cast<uint32_t *>(ccount + batch);
     cudaError_t e;
     if (k_sel > 0) {
-        e = cudaMemsetAsync(thr, 0, static_cast<size_t>(batch) * sizeof(uint32_t), stream);
+        e = cudaMemsetAsync(ccount, 0, static_cast<size_t>(batch) * 2 * sizeof(uint32_t), stream);
         if (e != cudaSuccess) return e;
         dx::ScanParams sp;
         sp.qi = qi;
@@ -445,31 +482,41 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
         sp.chunk = plan.chunk;
         sp.nchunk = plan.nchunk;
         sp.k_sel = k_sel;
-        sp.cand = cand;
-        sp.cnt = cnt;
-        sp.thr = thr;
+        sp.scores = scores;
+        sp.lb_inv = lb_inv;
         sp.status = status;
         const int smem = static_cast<int>(plan.chunk * 4 + 256 * 4 + 32);
         e = cudaFuncSetAttribute(dx::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        dim3 grid(plan.nchunk, batch);
-        dx::scan_kernel<<<grid, dx::SCAN_THREADS, smem, stream>>>(sp);
+        dx::scan_kernel<<<dim3(plan.nchunk, batch), dx::SCAN_THREADS, smem, stream>>>(sp);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        dx::FilterParams fp;
+        fp.seq_lens = seq_lens;
+        fp.max_ctx = max_ctx;
+        fp.k_sel = k_sel;
+        fp.scores = scores;
+        fp.lb_inv = lb_inv;
+        fp.cand = cand;
+        fp.ccount = ccount;
+        const int64_t cmax = (max_ctx - 1) / kBlock;
+        const int64_t per_cta = static_cast<int64_t>(dx::FILTER_THREADS) * dx::FILTER_PER_THREAD;
+        const int64_t fx = cmax > 0 ? (cmax + per_cta - 1) / per_cta : 1;
+        dx::filter_kernel<<<dim3(static_cast<unsigned>(fx), batch), dx::FILTER_THREADS, 0, stream>>>(fp);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     dx::MergeParams mp;
     mp.seq_lens = seq_lens;
     mp.max_ctx = max_ctx;
-    mp.nchunk = plan.nchunk;
     mp.k_sel = k_sel;
     mp.budget = budget;
+    mp.scores = scores;
     mp.cand = cand;
-    mp.cnt = cnt;
-    mp.thr = k_sel > 0 ? thr : nullptr;
+    mp.ccount = ccount;
     mp.idx = idx_out;
     mp.status = status;
-    const int smem = dx::MAX_NCHUNK * dx::MAX_SEL * 8 + kMaxBudget * 8 + 256 * 4 + 8 * 4 +
-                     (dx::MAX_NCHUNK + 1) * 4;
+    const int smem = dx::CAND_CAP * 8 + kMaxBudget * 8 + 256 * 4 + 8 * 4;
     e = cudaFuncSetAttribute(dx::merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dx::merge_kernel<<<batch, dx::MERGE_THREADS, smem, stream>>>(mp);

@@ -347,15 +347,13 @@ qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const qsa::DecodePlan plan = qsa::decode_plan(batch, max_ctx, sms);
     const int budget = cfg->budget_blocks;
-    const int k_alloc = budget - 1 > 0 ? budget - 1 : 1;
     uint8_t *p = static_cast<uint8_t *>(ws);
     auto take = [&](size_t bytes) {
         uint8_t *r = p;
         p += align_up(bytes, 256);
         return r;
     };
-    uint8_t *cand_region = take(static_cast<size_t>(batch) * plan.nchunk * k_alloc * 8);
-    take(static_cast<size_t>(batch) * plan.nchunk * 4);
+    uint8_t *cand_region = take(qsa::decode_index_ws_bytes(batch, max_ctx));
     int32_t *idx_ws = reinterpret_cast<int32_t *>(take(static_cast<size_t>(batch) * budget * 4));
     float *part_o = reinterpret_cast<float *>(take(static_cast<size_t>(batch) * plan.nsplit * qsa::kHQ * qsa::kD * 4));
     float *part_lse = reinterpret_cast<float *>(take(static_cast<size_t>(batch) * plan.nsplit * qsa::kHQ * 4));

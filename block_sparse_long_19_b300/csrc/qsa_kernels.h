@@ -61,6 +61,7 @@ struct DecodePlan {
 };
 DecodePlan decode_plan(int batch, int64_t max_ctx, int sms);
 size_t decode_ws_bytes(int batch, int64_t max_ctx, int budget, int sms);
+size_t decode_index_ws_bytes(int batch, int64_t max_ctx);  // leading part of the decode workspace
 cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &plan,
                                 const uint16_t *qi, const uint16_t *w, const uint16_t *kblk,
                                 const int32_t *seq_lens, int budget, void *ws, int32_t *idx_out,

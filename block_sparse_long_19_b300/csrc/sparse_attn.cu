@@ -129,40 +129,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     __syncthreads();
 
     // ---------------------------------- phase 2: slot count, Q with RoPE --
-    if (warp == 0) {
-        int last = -1;
-        for (int base = 0; base < a.budget; base += 32) {
-            const int i = base + lane;
-            const bool v = i < a.budget && sIdx[i] >= 0;
-            const unsigned ball = __ballot_sync(0xFFFFFFFFu, v);
-            if (ball) last = base + 31 - __clz(ball);
-        }
-        if (lane == 0) sMisc[0] = last + 1;
+    // Every warp counts the used slots itself; the producer starts its copies
+    // right away while the consumer warps put Q (with RoPE) into shared
+    // memory, so the first stages are in flight during that set-up.
+    int nslot = 0;
+    for (int base = 0; base < a.budget; base += 32) {
+        const int i = base + lane;
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, i < a.budget && sIdx[i] >= 0);
+        if (ball) nslot = base + 32 - __clz(ball);
     }
-    for (int i = threadIdx.x; i < kHQ * 32; i += THREADS) {
-        const int h = i >> 5, r = i & 31;
-        const float x1 = __uint_as_float(static_cast<uint32_t>(qrow[h * kD + r]) << 16);
-        const float x2 = __uint_as_float(static_cast<uint32_t>(qrow[h * kD + r + 32]) << 16);
-        const float cs = sCS[r], sn = sCS[32 + r];
-        __nv_bfloat16 y1 = __float2bfloat16_rn(fmaf(x1, cs, -x2 * sn));
-        __nv_bfloat16 y2 = __float2bfloat16_rn(fmaf(x2, cs, x1 * sn));
-        uint8_t *qr = sQ + (h / kGroup) * 16 * QROW + (h % kGroup) * QROW;
-        reinterpret_cast<__nv_bfloat16 *>(qr)[r] = y1;
-        reinterpret_cast<__nv_bfloat16 *>(qr)[r + 32] = y2;
-    }
-    for (int i = threadIdx.x; i < kHQ * 24; i += THREADS) {
-        const int h = i / 24, v = i % 24;
-        const uint4 x = *reinterpret_cast<const uint4 *>(qrow + h * kD + kRD + v * 8);
-        uint8_t *qr = sQ + (h / kGroup) * 16 * QROW + (h % kGroup) * QROW;
-        *reinterpret_cast<uint4 *>(qr + kRD * 2 + v * 16) = x;
-    }
-    for (int i = threadIdx.x; i < kHKV * 4 * 32; i += THREADS) {  // zero rows 12..15
-        const int g = i / 128, r = 12 + (i / 32) % 4, v = i % 32;
-        *reinterpret_cast<uint4 *>(sQ + g * 16 * QROW + r * QROW + v * 16) = make_uint4(0, 0, 0, 0);
-    }
-    __syncthreads();
-
-    const int nslot = sMisc[0];
     const int total_st = (nslot + SBLK - 1) / SBLK;
     int st_begin = 0, st_end = total_st;
     if constexpr (DECODE) {
@@ -170,6 +145,32 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
         st_begin = split * per;
         st_end = min(total_st, st_begin + per);
         if (st_begin > st_end) st_begin = st_end;
+    }
+    if (warp > 0) {
+        const int ct = threadIdx.x - 32;
+        constexpr int CT = NCONS * 32;
+        for (int i = ct; i < kHQ * 32; i += CT) {
+            const int h = i >> 5, r = i & 31;
+            const float x1 = __uint_as_float(static_cast<uint32_t>(qrow[h * kD + r]) << 16);
+            const float x2 = __uint_as_float(static_cast<uint32_t>(qrow[h * kD + r + 32]) << 16);
+            const float cs = sCS[r], sn = sCS[32 + r];
+            __nv_bfloat16 y1 = __float2bfloat16_rn(fmaf(x1, cs, -x2 * sn));
+            __nv_bfloat16 y2 = __float2bfloat16_rn(fmaf(x2, cs, x1 * sn));
+            uint8_t *qr = sQ + (h / kGroup) * 16 * QROW + (h % kGroup) * QROW;
+            reinterpret_cast<__nv_bfloat16 *>(qr)[r] = y1;
+            reinterpret_cast<__nv_bfloat16 *>(qr)[r + 32] = y2;
+        }
+        for (int i = ct; i < kHQ * 24; i += CT) {
+            const int h = i / 24, v = i % 24;
+            const uint4 x = *reinterpret_cast<const uint4 *>(qrow + h * kD + kRD + v * 8);
+            uint8_t *qr = sQ + (h / kGroup) * 16 * QROW + (h % kGroup) * QROW;
+            *reinterpret_cast<uint4 *>(qr + kRD * 2 + v * 16) = x;
+        }
+        for (int i = ct; i < kHKV * 4 * 32; i += CT) {  // zero rows 12..15
+            const int g = i / 128, r = 12 + (i / 32) % 4, v = i % 32;
+            *reinterpret_cast<uint4 *>(sQ + g * 16 * QROW + r * QROW + v * 16) = make_uint4(0, 0, 0, 0);
+        }
+        named_bar(1, CT);  // Q complete before any consumer reads it
     }
 
     if (warp == 0) {

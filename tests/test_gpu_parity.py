@@ -209,6 +209,32 @@ def test_decode_against_oracle(budget):
     check_outputs(lse.cpu().numpy().astype(np.float64), att["lse"], "LSE")
 
 
+def test_decode_all_ties():
+    """w = 0 makes every block score 0: the selection is blocks 0..budget-2
+    plus the current block (lower block wins a tie).  At 65,536 tokens the
+    16,383 tied candidates exceed the decode candidate area, which sends the
+    final selection over all of the sequence's scores; at 8,192 tokens the
+    2,047 ties fit."""
+    B, Tmax, budget = 2, 65536, 512
+    lens = [Tmax, 8192]
+    d = W.decode_inputs(B, Tmax, 32, DEV, seq_lens=lens)
+    d["w"].zero_()
+    hd = W.host_bits(d)
+    cfg = Q.default_config(budget=budget)
+    k_rot = torch.empty_like(d["k"])
+    kblk, _ = Q.kprep(cfg, d["ki"], d["k"], k_rot=k_rot)
+    out, lse, idx, st = Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], k_rot, d["v"], kblk,
+                                             d["seq_lens"])
+    torch.cuda.synchronize()
+    Q.check_status(st)
+    ref = O.decode(hd, budget, want_o=False)
+    idx_g = idx.cpu().numpy()
+    assert np.array_equal(idx_g, ref["idx"])
+    for s_ in range(B):
+        c = (lens[s_] - 1) // 4
+        assert np.array_equal(idx_g[s_], np.r_[np.arange(budget - 1), c])
+
+
 def test_decode_short_sequences():
     B, Tmax = 4, 64
     lens = [1, 2, 5, 64]
