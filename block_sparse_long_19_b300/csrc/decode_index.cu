@@ -32,7 +32,7 @@ namespace dx {
 constexpr int SCAN_THREADS = 256;
 constexpr int MAX_CHUNK = 16384;
 constexpr int MAX_NCHUNK = 47;
-constexpr int MERGE_THREADS = 1024;
+constexpr int MERGE_THREADS = 256;
 constexpr int FILTER_THREADS = 256;
 constexpr int FILTER_PER_THREAD = 8;
 constexpr int CAND_CAP = 8192;  // filtered candidates kept per sequence
@@ -183,7 +183,8 @@ struct ScanParams {
     int nchunk;
     int k_sel;
     float *scores;             // [B, max_ctx/4]
-    uint32_t *lb_inv;          // [B] ~(lower bound key), combined by atomicMax (0 = none yet)
+    uint32_t *lb;              // [B, nchunk] each chunk's bound key (0xFFFFFFFF: none)
+    int32_t *ccount;           // [B] candidate counters, zeroed here for the filter
     int32_t *status;
 };
 
@@ -193,10 +194,16 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.chunk * 4);  // dynamic size: chunk*4 + 256*4 + 32
     int *ctl = reinterpret_cast<int *>(hist + 256);
 
+    pdl_trigger();
     const int s = blockIdx.y;
     const int ch = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t T = p.seq_lens[s];
+    uint32_t *lb_out = p.lb + static_cast<int64_t>(s) * p.nchunk + ch;
+    if (threadIdx.x == 0) {
+        *lb_out = 0xFFFFFFFFu;  // overwritten below if this chunk bounds the selection
+        if (ch == 0) p.ccount[s] = 0;
+    }
     if (T < 1 || T > p.max_ctx) {
         if (threadIdx.x == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
         return;
@@ -260,7 +267,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     const RadixOut r = cta_radix<SCAN_THREADS>(
         n, kc, [&](int i) { return f2key(sc[i]); }, [&](int) { return true; }, hist, ctl);
     // at least kc of this chunk's keys are >= r.thr
-    if (threadIdx.x == 0) atomicMax(&p.lb_inv[s], ~r.thr);
+    if (threadIdx.x == 0) *lb_out = r.thr;
 }
 
 struct FilterParams {
@@ -268,7 +275,8 @@ struct FilterParams {
     int64_t max_ctx;
     int k_sel;
     const float *scores;     // [B, max_ctx/4]
-    const uint32_t *lb_inv;  // [B]
+    const uint32_t *lb;      // [B, nchunk]
+    int nchunk;
     uint2 *cand;             // [B, CAND_CAP] {score bits, block}
     int32_t *ccount;         // [B]
 };
@@ -279,12 +287,20 @@ struct FilterParams {
 // CTA would queue up at one L2 slice).
 __global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) {
     __shared__ int s_warp[FILTER_THREADS / 32 + 1];
+    pdl_trigger();
+    pdl_wait();  // scores and bounds of the scan
     const int s = blockIdx.y;
     const int64_t T = p.seq_lens[s];
     if (T < 1 || T > p.max_ctx) return;
     const int64_t c = (T - 1) / kBlock;
     if (c <= p.k_sel) return;
-    const uint32_t bound = ~p.lb_inv[s];
+    // the bound: the smallest chunk bound (chunks that bound nothing wrote
+    // 0xFFFFFFFF); every warp reduces the chunk slots itself, two per lane
+    const uint32_t *lbs = p.lb + static_cast<int64_t>(s) * p.nchunk;
+    const int ln = threadIdx.x & 31;
+    uint32_t bound = ln < p.nchunk ? __ldcg(lbs + ln) : 0xFFFFFFFFu;
+    for (int i = ln + 32; i < p.nchunk; i += 32) bound = min(bound, __ldcg(lbs + i));
+    bound = __reduce_min_sync(0xFFFFFFFFu, bound);
     const float *srow = p.scores + static_cast<int64_t>(s) * (p.max_ctx / kBlock);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned ltmask = (1u << lane) - 1u;
@@ -344,10 +360,12 @@ struct MergeParams {
 __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     uint2 *items = reinterpret_cast<uint2 *>(smem);
-    unsigned long long *sortb = reinterpret_cast<unsigned long long *>(items + CAND_CAP);
-    uint32_t *hist = reinterpret_cast<uint32_t *>(sortb + kMaxBudget);
+    uint32_t *sortb = reinterpret_cast<uint32_t *>(items + CAND_CAP);  // [1024]: sort input at 512..
+    uint32_t *hist = sortb + 1024;
     int *ctl = reinterpret_cast<int *>(hist + 256);
 
+    pdl_trigger();
+    pdl_wait();  // candidates of the filter (and, through it, the scan's scores)
     const int s = blockIdx.x;
     const int64_t T = p.seq_lens[s];
     int32_t *row = p.idx + static_cast<int64_t>(s) * p.budget;
@@ -357,9 +375,10 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
         return;
     }
     const int64_t c = (T - 1) / kBlock;
-    if (c <= p.k_sel) {  // every past block, then the current one
+    if (c <= p.k_sel || p.k_sel <= 0) {  // every past block (none for budget 1), then the current one
+        const int64_t np = p.k_sel <= 0 ? 0 : c;
         for (int i = threadIdx.x; i < p.budget; i += MERGE_THREADS)
-            row[i] = i < c ? i : (i == c ? static_cast<int32_t>(c) : -1);
+            row[i] = i < np ? i : (i == np ? static_cast<int32_t>(c) : -1);
         return;
     }
     const int lane = threadIdx.x & 31;
@@ -394,18 +413,26 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
         if (lane == 0) pos0 = atomicAdd(&ctl[3], __popc(ball));
         pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
         const int pos = pos0 + __popc(ball & ltmask);
-        if (sel && pos < kMaxBudget) sortb[pos] = (static_cast<unsigned long long>(bv) << 32) | __float_as_uint(sv);
+        if (sel && pos < kMaxBudget) sortb[512 + pos] = bv;
     }
     __syncthreads();
     const int m = min(ctl[3], p.k_sel);
     if (threadIdx.x == 0 && ctl[3] != p.k_sel) report(p.status, QSA_ERR_DEVICE_CHECK);
-    // order by block: blocks are distinct, so an item's place is the number
-    // of smaller blocks (every thread scans the list with broadcast reads)
-    for (int i = threadIdx.x; i < m; i += MERGE_THREADS) {
-        const uint32_t bi = static_cast<uint32_t>(sortb[i] >> 32);
-        int rank = 0;
-        for (int j = 0; j < m; ++j) rank += static_cast<uint32_t>(sortb[j] >> 32) < bi;
-        if (rank < p.budget) row[rank] = static_cast<int32_t>(bi);
+    // order by block (blocks are distinct): a bitonic sort of 512 keys by the
+    // first four warps, padded with the largest key
+    if (threadIdx.x < 128) {
+        uint32_t v[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int e = 4 * threadIdx.x + r;
+            v[r] = e < m ? sortb[512 + e] : 0xFFFFFFFFu;
+        }
+        group_sort512(v, sortb, threadIdx.x, 1);
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int e = 4 * threadIdx.x + r;
+            if (e < m && e < p.budget) row[e] = static_cast<int32_t>(v[r]);
+        }
     }
     for (int i = m + threadIdx.x; i < p.budget; i += MERGE_THREADS)
         row[i] = i == m ? static_cast<int32_t>(c) : -1;
@@ -442,7 +469,8 @@ static size_t index_ws_bytes(int batch, int64_t max_ctx) {
     size_t b = 0;
     b += align256(static_cast<size_t>(batch) * (max_ctx / kBlock) * sizeof(float));      // scores
     b += align256(static_cast<size_t>(batch) * dx::CAND_CAP * sizeof(uint2));            // cand
-    b += align256(static_cast<size_t>(batch) * 2 * sizeof(uint32_t));                    // ccount, lb_inv
+    b += align256(static_cast<size_t>(batch) * sizeof(int32_t));                         // ccount
+    b += align256(static_cast<size_t>(batch) * dx::MAX_NCHUNK * sizeof(uint32_t));       // chunk bounds
     return b;
 }
 
@@ -468,11 +496,10 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
     uint2 *cand = reinterpret_cast<uint2 *>(base);
     base += align256(static_cast<size_t>(batch) * dx::CAND_CAP * sizeof(uint2));
     int32_t *ccount = reinterpret_cast<int32_t *>(base);
-    uint32_t *lb_inv = reinterpret_cast<uint32_t *>(ccount + batch);
+    base += align256(static_cast<size_t>(batch) * sizeof(int32_t));
+    uint32_t *lb = reinterpret_cast<uint32_t *>(base);
     cudaError_t e;
     if (k_sel > 0) {
-        e = cudaMemsetAsync(ccount, 0, static_cast<size_t>(batch) * 2 * sizeof(uint32_t), stream);
-        if (e != cudaSuccess) return e;
         dx::ScanParams sp;
         sp.qi = qi;
         sp.w = w;
@@ -483,7 +510,8 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
         sp.nchunk = plan.nchunk;
         sp.k_sel = k_sel;
         sp.scores = scores;
-        sp.lb_inv = lb_inv;
+        sp.lb = lb;
+        sp.ccount = ccount;
         sp.status = status;
         const int smem = static_cast<int>(plan.chunk * 4 + 256 * 4 + 32);
         e = cudaFuncSetAttribute(dx::scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -496,14 +524,15 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
         fp.max_ctx = max_ctx;
         fp.k_sel = k_sel;
         fp.scores = scores;
-        fp.lb_inv = lb_inv;
+        fp.lb = lb;
+        fp.nchunk = plan.nchunk;
         fp.cand = cand;
         fp.ccount = ccount;
         const int64_t cmax = (max_ctx - 1) / kBlock;
         const int64_t per_cta = static_cast<int64_t>(dx::FILTER_THREADS) * dx::FILTER_PER_THREAD;
         const int64_t fx = cmax > 0 ? (cmax + per_cta - 1) / per_cta : 1;
-        dx::filter_kernel<<<dim3(static_cast<unsigned>(fx), batch), dx::FILTER_THREADS, 0, stream>>>(fp);
-        e = cudaGetLastError();
+        e = launch_pdl(dx::filter_kernel, dim3(static_cast<unsigned>(fx), batch), dim3(dx::FILTER_THREADS), 0,
+                       stream, fp);
         if (e != cudaSuccess) return e;
     }
     dx::MergeParams mp;
@@ -516,11 +545,11 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
     mp.ccount = ccount;
     mp.idx = idx_out;
     mp.status = status;
-    const int smem = dx::CAND_CAP * 8 + kMaxBudget * 8 + 256 * 4 + 8 * 4;
+    const int smem = dx::CAND_CAP * 8 + 1024 * 4 + 256 * 4 + 8 * 4;
     e = cudaFuncSetAttribute(dx::merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dx::merge_kernel<<<batch, dx::MERGE_THREADS, smem, stream>>>(mp);
-    return cudaGetLastError();
+    return launch_pdl(dx::merge_kernel, dim3(batch), dim3(dx::MERGE_THREADS), static_cast<size_t>(smem), stream,
+                      mp);
 }
 
 }  // namespace qsa

@@ -151,4 +151,54 @@ __device__ __forceinline__ uint32_t warp_select_exact(const uint32_t (&key)[NI],
     return sel;
 }
 
+// Ascending bitonic sort of 512 distinct keys held by 128 threads (four
+// whole warps that share hardware barrier `bar`), thread tg holding
+// positions 4tg .. 4tg+3.  Partners one or two positions away are in the
+// same thread, up to 64 away in the same warp
+// (shuffles); the three steps that cross warps go through shared memory,
+// alternating between buf[0..511] and buf[512..1023].  The caller's input may
+// sit in buf[512..1023]: the first write there comes after the barrier of
+// the first crossing step, which every thread reaches with its keys loaded.
+template <typename T>
+__device__ __forceinline__ void group_sort512(T (&v)[4], T *buf, int tg, int bar) {
+    int flip = 0;
+#pragma unroll
+    for (int k = 2; k <= 512; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j >= 1; j >>= 1) {
+            if (j < 4) {
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    if (r & j) continue;
+                    const int e = 4 * tg + r;
+                    const bool asc = (e & k) == 0;
+                    const T lo = v[r], hi = v[r ^ j];
+                    const bool sw = asc ? (lo > hi) : (lo < hi);
+                    v[r] = sw ? hi : lo;
+                    v[r ^ j] = sw ? lo : hi;
+                }
+            } else {
+                T o[4];
+                if (j >= 128) {
+                    T *b = buf + (flip & 1) * 512;
+                    ++flip;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) b[4 * tg + r] = v[r];
+                    asm volatile("bar.sync %0, 128;" ::"r"(bar) : "memory");
+                    const int pt = tg ^ (j >> 2);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) o[r] = b[4 * pt + r];
+                } else {
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) o[r] = __shfl_xor_sync(0xFFFFFFFFu, v[r], j >> 2);
+                }
+                const int e = 4 * tg;
+                const bool keep_min = ((e & j) == 0) == ((e & k) == 0);
+#pragma unroll
+                for (int r = 0; r < 4; ++r) v[r] = keep_min ? min(v[r], o[r]) : max(v[r], o[r]);
+            }
+        }
+    }
+}
+
 }  // namespace qsa

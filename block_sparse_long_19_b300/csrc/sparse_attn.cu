@@ -108,6 +108,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     const int64_t c = t / kBlock;
 
     // ---------------------------------------------- phase 1: idx, cos/sin --
+    if constexpr (DECODE) {
+        pdl_trigger();
+        pdl_wait();  // the selection of the decode indexer
+    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 1);
@@ -434,6 +438,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       const float *__restrict__ part_lse,
                                                       int nsplit, uint16_t *__restrict__ out,
                                                       float *__restrict__ lse) {
+    pdl_wait();  // the splits' partial outputs
     const int s = blockIdx.x / kHQ;
     const int h = blockIdx.x % kHQ;
     const int d = threadIdx.x;
@@ -480,15 +485,14 @@ cudaError_t launch_attn_decode(const AttnArgs &a, int batch, const RopeFreqs &f,
     cudaError_t e = cudaFuncSetAttribute(at::attn_kernel<kDecodeStages, true>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.nsplit, batch);
-    at::attn_kernel<kDecodeStages, true><<<grid, at::THREADS, smem, stream>>>(a, f);
-    return cudaGetLastError();
+    return launch_pdl(at::attn_kernel<kDecodeStages, true>, dim3(a.nsplit, batch), dim3(at::THREADS),
+                      static_cast<size_t>(smem), stream, a, f);
 }
 
 cudaError_t launch_attn_combine(const float *part_o, const float *part_lse, int batch,
                                 int nsplit, uint16_t *out, float *lse, cudaStream_t stream) {
-    at::combine_kernel<<<batch * kHQ, kD, 0, stream>>>(part_o, part_lse, nsplit, out, lse);
-    return cudaGetLastError();
+    return launch_pdl(at::combine_kernel, dim3(batch * kHQ), dim3(kD), 0, stream, part_o, part_lse, nsplit, out,
+                      lse);
 }
 
 }  // namespace qsa

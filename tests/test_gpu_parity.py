@@ -235,6 +235,25 @@ def test_decode_all_ties():
         assert np.array_equal(idx_g[s_], np.r_[np.arange(budget - 1), c])
 
 
+def test_decode_budget_one():
+    """Budget 1: only the current block is attended."""
+    B, Tmax = 3, 4096
+    lens = [Tmax, 9, 1]
+    d = W.decode_inputs(B, Tmax, 33, DEV, seq_lens=lens)
+    hd = W.host_bits(d)
+    cfg = Q.default_config(budget=1)
+    k_rot = torch.empty_like(d["k"])
+    kblk, _ = Q.kprep(cfg, d["ki"], d["k"], k_rot=k_rot)
+    out, lse, idx, st = Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], k_rot, d["v"], kblk,
+                                             d["seq_lens"])
+    torch.cuda.synchronize()
+    Q.check_status(st)
+    ref = O.decode(hd, 1)
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.array_equal(idx.cpu().numpy()[:, 0], [(T - 1) // 4 for T in lens])
+    check_outputs(bf16_to_f64(out), ref["o"], "O")
+
+
 def test_decode_short_sequences():
     B, Tmax = 4, 64
     lens = [1, 2, 5, 64]
