@@ -22,6 +22,8 @@
 //     candidates (score desc, block asc), sorts them by block and appends the
 //     current block.  If ties leave more candidates than the candidate area
 //     holds, it selects over all of the sequence's scores instead.
+#include <cmath>
+
 #include "qsa_common.cuh"
 #include "qsa_kernels.h"
 #include "qsa_select.cuh"
@@ -31,7 +33,7 @@ namespace dx {
 
 constexpr int SCAN_THREADS = 256;
 constexpr int MAX_CHUNK = 16384;
-constexpr int MAX_NCHUNK = 47;
+constexpr int MAX_NCHUNK = 256;  // scan CTAs per sequence
 constexpr int MERGE_THREADS = 256;
 constexpr int FILTER_THREADS = 256;
 constexpr int FILTER_PER_THREAD = 8;
@@ -230,30 +232,40 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     }
     const uint16_t *kb = p.kblk + static_cast<int64_t>(s) * (p.max_ctx / kBlock) * kDI;
 
-    for (int mt = warp; mt * 16 < n; mt += SCAN_THREADS / 32) {
-        const int64_t ra = b0 + mt * 16 + hr;
-        const int64_t rb = ra + 8;
-        const int64_t la = ra < b1 ? ra : b1 - 1;
-        const int64_t lb = rb < b1 ? rb : b1 - 1;
-        uint4 ua[4], ub[4];
+    // two 16-block tiles per warp and iteration: all 16 loads of a lane in
+    // flight before the first MMA
+    constexpr int NW = SCAN_THREADS / 32;
+    for (int mt0 = warp; mt0 * 16 < n; mt0 += 2 * NW) {
+        uint4 ua[2][4], ub[2][4];
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            ua[kk] = __ldcs(reinterpret_cast<const uint4 *>(kb + la * kDI + kk * 32 + qd * 8));
-            ub[kk] = __ldcs(reinterpret_cast<const uint4 *>(kb + lb * kDI + kk * 32 + qd * 8));
-        }
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int64_t ra = b0 + (mt0 + h2 * NW) * 16 + hr;
+            const int64_t la = ra < b1 ? ra : b1 - 1;
+            const int64_t lb = ra + 8 < b1 ? ra + 8 : b1 - 1;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            mma_bf16_16816(acc, ua[kk].x, ub[kk].x, ua[kk].y, ub[kk].y, bq[kk].x, bq[kk].y);
-            mma_bf16_16816(acc, ua[kk].z, ub[kk].z, ua[kk].w, ub[kk].w, bq[kk].z, bq[kk].w);
+            for (int kk = 0; kk < 4; ++kk) {
+                ua[h2][kk] = __ldcs(reinterpret_cast<const uint4 *>(kb + la * kDI + kk * 32 + qd * 8));
+                ub[h2][kk] = __ldcs(reinterpret_cast<const uint4 *>(kb + lb * kDI + kk * 32 + qd * 8));
+            }
         }
-        float pa = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);  // row hr
-        float pb = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);  // row hr + 8
-        pa += __shfl_xor_sync(0xFFFFFFFFu, pa, 1);
-        pb += __shfl_xor_sync(0xFFFFFFFFu, pb, 1);
-        if (qd == 0) {
-            if (ra < b1) sc[ra - b0] = pa + 0.0f;
-            if (rb < b1) sc[rb - b0] = pb + 0.0f;
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+            const int64_t ra = b0 + (mt0 + h2 * NW) * 16 + hr;
+            const int64_t rb = ra + 8;
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                mma_bf16_16816(acc, ua[h2][kk].x, ub[h2][kk].x, ua[h2][kk].y, ub[h2][kk].y, bq[kk].x, bq[kk].y);
+                mma_bf16_16816(acc, ua[h2][kk].z, ub[h2][kk].z, ua[h2][kk].w, ub[h2][kk].w, bq[kk].z, bq[kk].w);
+            }
+            float pa = w0 * fmaxf(acc[0], 0.f) + w1 * fmaxf(acc[1], 0.f);  // row hr
+            float pb = w0 * fmaxf(acc[2], 0.f) + w1 * fmaxf(acc[3], 0.f);  // row hr + 8
+            pa += __shfl_xor_sync(0xFFFFFFFFu, pa, 1);
+            pb += __shfl_xor_sync(0xFFFFFFFFu, pb, 1);
+            if (qd == 0) {
+                if (ra < b1) sc[ra - b0] = pa + 0.0f;
+                if (rb < b1) sc[rb - b0] = pb + 0.0f;
+            }
         }
     }
     __syncthreads();
@@ -442,15 +454,30 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
 
 DecodePlan decode_plan(int batch, int64_t max_ctx, int sms) {
     DecodePlan pl;
+    // Chunks per sequence: batch x chunks should fill the SMs evenly (the
+    // scan is bound by HBM bandwidth, so the SM with the most CTAs sets the
+    // time), and among even fillings fewer chunks are better: they give a
+    // tighter selection bound and so fewer candidates for the merge.
     const int64_t cmax = (max_ctx - 1) / kBlock;
-    int64_t target = (static_cast<int64_t>(batch) * cmax + static_cast<int64_t>(sms) * 4 - 1) /
-                     (static_cast<int64_t>(sms) * 4);
-    int64_t ch = ((target + 255) / 256) * 256;
+    int64_t nchunk = 1;
+    double best = -1.0;
+    for (int per_sm = 2; per_sm <= 8; ++per_sm) {
+        int64_t n = (static_cast<int64_t>(per_sm) * sms + batch / 2) / batch;
+        if (n < 1) n = 1;
+        const double ctas = static_cast<double>(batch) * static_cast<double>(n);
+        const double eff = ctas / (std::ceil(ctas / sms) * sms);
+        if (eff > best + 0.02) {
+            best = eff;
+            nchunk = n;
+        }
+    }
+    int64_t ch = cmax > 0 ? (cmax + nchunk - 1) / nchunk : 1;
+    ch = ((ch + 31) / 32) * 32;
     if (ch < 1024) ch = 1024;
     if (ch > dx::MAX_CHUNK) ch = dx::MAX_CHUNK;
-    int64_t nchunk = cmax > 0 ? (cmax + ch - 1) / ch : 1;
+    nchunk = cmax > 0 ? (cmax + ch - 1) / ch : 1;
     if (nchunk > dx::MAX_NCHUNK) {
-        ch = (((cmax + dx::MAX_NCHUNK - 1) / dx::MAX_NCHUNK + 255) / 256) * 256;
+        ch = (((cmax + dx::MAX_NCHUNK - 1) / dx::MAX_NCHUNK + 31) / 32) * 32;
         nchunk = (cmax + ch - 1) / ch;
     }
     pl.chunk = ch;
