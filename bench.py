@@ -166,9 +166,8 @@ class Workload:
             events[3].record()
 
     def launches_per_step(self) -> int:
-        plan_split = 1  # combine kernel launched when the decode splits > 1
-        n = 2 + 1 + 1   # kprep blocks + kprep rope, indexer, attention
-        n += 2 + 1 + plan_split  # decode scan + merge, attention, combine
+        n = 2 + 1 + 1      # kprep blocks + kprep rope, indexer, prefill attention
+        n += 3 + 1 + 1     # decode scan, filter, merge; split attention; combine
         return n
 
     def attn_bytes(self) -> int:
