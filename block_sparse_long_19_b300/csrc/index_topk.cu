@@ -78,13 +78,14 @@ constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Params {
-    int64_t L;
+    int64_t L;          // end position: queries are tokens q_off .. L-1
+    int64_t q_off;      // position of the first query row (a cached prefix before it)
     int nq;
     int k_sel;          // budget - 1
     int budget;
-    const uint16_t *w;  // [L, 4]
-    int32_t *idx;       // [L, budget]
-    float *score;       // [L, budget] or null
+    const uint16_t *w;  // [L - q_off, 4]
+    int32_t *idx;       // [L - q_off, budget]
+    float *score;       // [L - q_off, budget] or null
     float *dense;       // [L, L/4] (dense mode)
     int64_t dense_ld;
     uint2 *cand;        // [grid, TQ, CAP] {score bits, block}
@@ -146,9 +147,10 @@ __device__ __forceinline__ void group_bar(int id) {
     asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory");
 }
 
-__device__ __forceinline__ int num_btiles(int64_t L, int q) {
-    int64_t t_last = static_cast<int64_t>(q) * TQ + TQ - 1;
-    if (t_last > L - 1) t_last = L - 1;
+// Block tiles query tile q has to visit: blocks 0 .. c(t_last)-1.
+__device__ __forceinline__ int num_btiles(const Params &p, int q) {
+    int64_t t_last = p.q_off + static_cast<int64_t>(q) * TQ + TQ - 1;
+    if (t_last > p.L - 1) t_last = p.L - 1;
     const int64_t cmax = t_last / kBlock;  // blocks 0..cmax-1 are scored
     return static_cast<int>((cmax + TB - 1) / TB);
 }
@@ -451,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             bool ok = true;
             for (int kk = blockIdx.x; kk < p.nq && ok; kk += gridDim.x) {
                 const int q = p.nq - 1 - kk;
-                const int nbt = num_btiles(p.L, q);
+                const int nbt = num_btiles(p, q);
                 if (nbt == 0) continue;
                 if (!mbar_wait(qempty, qph ^ 1)) { ok = false; break; }
                 qph ^= 1;
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t sk_addr = smem_u32(sK);
             for (int kk = blockIdx.x; kk < p.nq && ok; kk += gridDim.x) {
                 const int q = p.nq - 1 - kk;
-                const int nbt = num_btiles(p.L, q);
+                const int nbt = num_btiles(p, q);
                 if (nbt == 0) continue;
                 if (!mbar_wait(qfull, qph)) { ok = false; break; }
                 qph ^= 1;
@@ -537,8 +539,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool ok = true;
         for (int kk = blockIdx.x; kk < p.nq; kk += gridDim.x) {
             const int q = p.nq - 1 - kk;
-            const int64_t t0 = static_cast<int64_t>(q) * TQ;
-            const int nbt = num_btiles(p.L, q);
+            const int64_t t0 = p.q_off + static_cast<int64_t>(q) * TQ;
+            const int nbt = num_btiles(p, q);
             if (group_sync_fail(bar, !ok || sMisc[1] != 0)) { ok = false; break; }
             if (tg < GTOK) {
                 const int tl = g * GTOK + tg;
@@ -549,7 +551,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < kHI; ++h) {
                     float wv = 0.f;
-                    if (t < p.L) wv = __uint_as_float(static_cast<uint32_t>(p.w[t * kHI + h]) << 16);
+                    if (t < p.L) wv = __uint_as_float(static_cast<uint32_t>(p.w[(t - p.q_off) * kHI + h]) << 16);
                     sW[(tl >> 2) * 16 + h * 4 + (tl & 3)] = wv;  // [token quad][head][token]
                 }
             }
@@ -720,8 +722,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // block indices alone or (block, score bits) when scores are written.
                     // The sort input sits in slots 512.. of the group's sort area; the
                     // sort's own first write goes to slots 0..511 (see group_sort512).
-                    int32_t *row = p.idx + t * p.budget;
-                    float *srow = p.score ? p.score + t * p.budget : nullptr;
+                    int32_t *row = p.idx + (t - p.q_off) * p.budget;
+                    float *srow = p.score ? p.score + (t - p.q_off) * p.budget : nullptr;
                     int m;
                     auto emit = [&](int e, uint32_t blk, float sc) {
                         if (e >= p.budget) return;
@@ -795,13 +797,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // Budget 1: only the current block, no scoring at all.
-__global__ void fill_current_kernel(int64_t L, int budget, int32_t *idx, float *score) {
-    const int64_t total = L * budget;
+__global__ void fill_current_kernel(int64_t q_off, int64_t Lq, int budget, int32_t *idx, float *score) {
+    const int64_t total = Lq * budget;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t t = i / budget;
-        const int r = static_cast<int>(i - t * budget);
-        idx[i] = r == 0 ? static_cast<int32_t>(t / kBlock) : -1;
+        const int64_t tl = i / budget;
+        const int r = static_cast<int>(i - tl * budget);
+        idx[i] = r == 0 ? static_cast<int32_t>((q_off + tl) / kBlock) : -1;
         if (score) score[i] = r == 0 ? INFINITY : -INFINITY;
     }
 }
@@ -817,13 +819,15 @@ size_t index_cand_bytes(int64_t L, int sms) {
     return static_cast<size_t>(index_grid(L, sms)) * ix::TQ * ix::CAP * sizeof(uint2);
 }
 
-cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t L,
+cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t q_off, int64_t Lq,
                          int budget, const uint16_t *w, int32_t *idx, float *score,
                          float *dense, void *cand_ws, int32_t *status, int sms,
                          cudaStream_t stream) {
     ix::Params p;
+    const int64_t L = q_off + Lq;
     p.L = L;
-    p.nq = static_cast<int>((L + ix::TQ - 1) / ix::TQ);
+    p.q_off = q_off;
+    p.nq = static_cast<int>((Lq + ix::TQ - 1) / ix::TQ);
     p.k_sel = budget - 1;
     p.budget = budget;
     p.w = w;
@@ -833,7 +837,7 @@ cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int
     p.dense_ld = L / kBlock;
     p.cand = reinterpret_cast<uint2 *>(cand_ws);
     p.status = status;
-    const int grid = index_grid(L, sms);
+    const int grid = index_grid(Lq, sms);
     cudaError_t e;
     if (dense) {
         e = cudaFuncSetAttribute(ix::index_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -849,11 +853,11 @@ cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int
     return cudaGetLastError();
 }
 
-cudaError_t launch_fill_current_only(int64_t L, int budget, int32_t *idx, float *score,
+cudaError_t launch_fill_current_only(int64_t q_off, int64_t Lq, int budget, int32_t *idx, float *score,
                                      cudaStream_t stream) {
-    int64_t blocks = (L * budget + 255) / 256;
+    int64_t blocks = (Lq * budget + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    ix::fill_current_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(L, budget, idx, score);
+    ix::fill_current_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(q_off, Lq, budget, idx, score);
     return cudaGetLastError();
 }
 

@@ -60,15 +60,15 @@ __device__ __forceinline__ double bf16_to_f64(uint16_t b) {
 // One thread per (sequence, block, 8-dim chunk).
 __global__ void __launch_bounds__(256) kprep_blocks_kernel(const uint16_t *__restrict__ ki,
                                                            uint16_t *__restrict__ kblk, int batch,
-                                                           int64_t nb, int64_t max_ctx) {
-    const int64_t per_seq = nb * (kDI / 8);
+                                                           int64_t b_lo, int64_t nb, int64_t max_ctx) {
+    const int64_t per_seq = (nb - b_lo) * (kDI / 8);
     const int64_t total = per_seq * batch;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t s = i / per_seq;
         const int64_t r = i - s * per_seq;
-        const int64_t b = r / (kDI / 8);
-        const int d8 = static_cast<int>(r - b * (kDI / 8));
+        const int64_t b = b_lo + r / (kDI / 8);
+        const int d8 = static_cast<int>(r % (kDI / 8));
         const uint16_t *src = ki + (s * max_ctx + b * kBlock) * kDI + d8 * 8;
         uint4 v[kBlock];
 #pragma unroll
@@ -93,17 +93,18 @@ __global__ void __launch_bounds__(256) kprep_blocks_kernel(const uint16_t *__res
 // output is a different buffer the pass-through dims are copied as well.
 __global__ void __launch_bounds__(256) kprep_rope_kernel(const uint16_t *__restrict__ k,
                                                          uint16_t *__restrict__ k_rot, int batch,
-                                                         int64_t L, int64_t max_ctx,
+                                                         int64_t j_lo, int64_t L, int64_t max_ctx,
                                                          RopeFreqs freqs, int copy_rest) {
     constexpr int kQuads = kRD / 2 / 4;  // 8 groups of 4 pairs
-    const int64_t per_seq = L * kHKV * kQuads;
+    const int64_t per_seq = (L - j_lo) * kHKV * kQuads;
     const int64_t total = per_seq * batch;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t s = i / per_seq;
         int64_t r = i - s * per_seq;
-        const int64_t j = r / (kHKV * kQuads);
-        r -= j * (kHKV * kQuads);
+        const int64_t jr = r / (kHKV * kQuads);
+        r -= jr * (kHKV * kQuads);
+        const int64_t j = j_lo + jr;
         const int g = static_cast<int>(r / kQuads);
         const int qd = static_cast<int>(r - g * kQuads);
         const int64_t row = ((s * max_ctx + j) * kHKV + g) * kD;
@@ -147,21 +148,22 @@ static int grid_for(int64_t work, int threads, int sms) {
     return static_cast<int>(g);
 }
 
-cudaError_t launch_kprep(int batch, int64_t L, int64_t max_ctx, const uint16_t *ki,
+cudaError_t launch_kprep(int batch, int64_t t_begin, int64_t L, int64_t max_ctx, const uint16_t *ki,
                          const uint16_t *k, uint16_t *k_rot, uint16_t *kblk,
                          const RopeFreqs &freqs, int sms, cudaStream_t stream) {
     const int64_t nb = L / kBlock;
-    if (nb > 0 && ki && kblk) {
-        const int64_t work = nb * (kDI / 8) * batch;
-        kprep_blocks_kernel<<<grid_for(work, 256, sms), 256, 0, stream>>>(ki, kblk, batch, nb,
+    const int64_t b_lo = t_begin / kBlock;
+    if (nb > b_lo && ki && kblk) {
+        const int64_t work = (nb - b_lo) * (kDI / 8) * batch;
+        kprep_blocks_kernel<<<grid_for(work, 256, sms), 256, 0, stream>>>(ki, kblk, batch, b_lo, nb,
                                                                           max_ctx);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (k && k_rot) {
-        const int64_t work = L * kHKV * 8 * batch;
+    if (k && k_rot && L > t_begin) {
+        const int64_t work = (L - t_begin) * kHKV * 8 * batch;
         kprep_rope_kernel<<<grid_for(work, 256, sms), 256, 0, stream>>>(
-            k, k_rot, batch, L, max_ctx, freqs, k != k_rot ? 1 : 0);
+            k, k_rot, batch, t_begin, L, max_ctx, freqs, k != k_rot ? 1 : 0);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

@@ -191,7 +191,7 @@ qsa_status qsa_kprep(const qsa_config *cfg, int batch, int64_t L, int64_t max_ct
     OPT_PTR(k_rot);
     if (batch > 1 && (max_ctx % qsa::kBlock) != 0 && L / qsa::kBlock > 0)
         return fail(QSA_ERR_INVALID_ARG, "max_ctx must be a multiple of 4 for batch > 1");
-    cudaError_t e = qsa::launch_kprep(batch, L, max_ctx, ki, k, k_rot, kblk, freqs_of(cfg), sm_count(),
+    cudaError_t e = qsa::launch_kprep(batch, 0, L, max_ctx, ki, k, k_rot, kblk, freqs_of(cfg), sm_count(),
                                       static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "kprep launch");
     return ok();
@@ -237,10 +237,10 @@ static qsa_status index_common(const qsa_config *cfg, const qsa_bf16 *qi, const 
     const size_t kblk_bytes = align_up(static_cast<size_t>(L / qsa::kBlock) * qsa::kDI * 2 + 16, 1024);
     void *cand = wsb + kblk_bytes;
 
-    cudaError_t e = qsa::launch_kprep(1, L, L, ki, k, k_rot, kblk, freqs_of(cfg), sms, s);
+    cudaError_t e = qsa::launch_kprep(1, 0, L, L, ki, k, k_rot, kblk, freqs_of(cfg), sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "kprep launch");
     if (!dense && cfg->budget_blocks == 1) {
-        e = qsa::launch_fill_current_only(L, 1, idx, score, s);
+        e = qsa::launch_fill_current_only(0, L, 1, idx, score, s);
         if (e != cudaSuccess) return cuda_fail(e, "selection launch");
         return ok();
     }
@@ -250,7 +250,7 @@ static qsa_status index_common(const qsa_config *cfg, const qsa_bf16 *qi, const 
     const int64_t nbk = L / qsa::kBlock;
     st = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
     if (st != QSA_OK) return st;
-    e = qsa::launch_index(map_q, map_k, L, cfg->budget_blocks, w, idx, score, dense, cand,
+    e = qsa::launch_index(map_q, map_k, 0, L, cfg->budget_blocks, w, idx, score, dense, cand,
                           dev_status, sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     return ok();
@@ -274,14 +274,15 @@ qsa_status qsa_index_scores(const qsa_config *cfg, const qsa_bf16 *qi, const qsa
                         dev_status, stream);
 }
 
-qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
-                                   const qsa_bf16 *k_rot, const qsa_bf16 *v, const int32_t *idx,
-                                   int64_t L, qsa_bf16 *out, float *lse, int32_t *dev_status,
-                                   void *stream) {
+qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 *q,
+                                          const qsa_bf16 *k_rot, const qsa_bf16 *v, const int32_t *idx,
+                                          int64_t q_offset, int64_t Lq, qsa_bf16 *out, float *lse,
+                                          int32_t *dev_status, void *stream) {
     qsa_status st = check_cfg(cfg);
     if (st != QSA_OK) return st;
-    if (L < 1) return fail(QSA_ERR_INVALID_ARG, "L must be >= 1");
-    if (L > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "L > %lld", static_cast<long long>(kMaxL));
+    if (Lq < 1) return fail(QSA_ERR_INVALID_ARG, "the number of query rows must be >= 1");
+    if (q_offset < 0) return fail(QSA_ERR_INVALID_ARG, "q_offset must be >= 0");
+    if (q_offset + Lq > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "more than %lld positions", static_cast<long long>(kMaxL));
     REQ_PTR(q);
     REQ_PTR(k_rot);
     REQ_PTR(v);
@@ -297,7 +298,8 @@ qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
     a.idx = idx;
     a.budget = cfg->budget_blocks;
     a.seq_lens = nullptr;
-    a.L = L;
+    a.L = Lq;
+    a.q_off = q_offset;
     a.out = out;
     a.lse = lse;
     a.nsplit = 1;
@@ -305,6 +307,75 @@ qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
     a.status = dev_status;
     cudaError_t e = qsa::launch_attn_prefill(a, freqs_of(cfg), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    return ok();
+}
+
+qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
+                                   const qsa_bf16 *k_rot, const qsa_bf16 *v, const int32_t *idx,
+                                   int64_t L, qsa_bf16 *out, float *lse, int32_t *dev_status,
+                                   void *stream) {
+    return qsa_sparse_attn_prefill_cached(cfg, q, k_rot, v, idx, 0, L, out, lse, dev_status, stream);
+}
+
+qsa_status qsa_kprep_range(const qsa_config *cfg, const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot,
+                           qsa_bf16 *kblk, int64_t t_begin, int64_t t_end, void *stream) {
+    qsa_status st = check_cfg(cfg);
+    if (st != QSA_OK) return st;
+    if (t_begin < 0 || t_end <= t_begin) return fail(QSA_ERR_INVALID_ARG, "need 0 <= t_begin < t_end");
+    if (t_end > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "t_end > %lld", static_cast<long long>(kMaxL));
+    REQ_PTR(ki);
+    REQ_PTR(kblk);
+    if ((k == nullptr) != (k_rot == nullptr))
+        return fail(QSA_ERR_INVALID_ARG, "k and k_rot must both be given or both be NULL");
+    OPT_PTR(k);
+    OPT_PTR(k_rot);
+    cudaError_t e = qsa::launch_kprep(1, t_begin, t_end, t_end, ki, k, k_rot, kblk, freqs_of(cfg), sm_count(),
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "kprep launch");
+    return ok();
+}
+
+size_t qsa_index_topk_cached_workspace_bytes(const qsa_config *cfg, int64_t Lq) {
+    if (check_cfg(cfg) != QSA_OK || Lq < 1 || Lq > kMaxL) return 0;
+    return align_up(qsa::index_cand_bytes(Lq, sm_count()), 256);
+}
+
+qsa_status qsa_index_topk_cached(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                                 const qsa_bf16 *kblk, int64_t q_offset, int64_t Lq, int32_t *idx,
+                                 float *score, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                 void *stream) {
+    qsa_status st = check_cfg(cfg);
+    if (st != QSA_OK) return st;
+    if (Lq < 1) return fail(QSA_ERR_INVALID_ARG, "the number of query rows must be >= 1");
+    if (q_offset < 0) return fail(QSA_ERR_INVALID_ARG, "q_offset must be >= 0");
+    if (q_offset + Lq > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "more than %lld positions", static_cast<long long>(kMaxL));
+    REQ_PTR(qi);
+    // w is read one element at a time: a chunk's rows may start at any row
+    if (!w || (reinterpret_cast<uintptr_t>(w) & 1u)) return fail(QSA_ERR_INVALID_ARG, "w is NULL or misaligned");
+    REQ_PTR(kblk);
+    REQ_PTR(idx);
+    OPT_PTR(score);
+    REQ_PTR(dev_status);
+    const size_t need = qsa_index_topk_cached_workspace_bytes(cfg, Lq);
+    if (!ws || ws_bytes < need)
+        return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (cfg->budget_blocks == 1) {
+        e = qsa::launch_fill_current_only(q_offset, Lq, 1, idx, score, s);
+        if (e != cudaSuccess) return cuda_fail(e, "selection launch");
+        return ok();
+    }
+    CUtensorMap map_q, map_k;
+    st = make_map(&map_q, qi, qsa::kDI, static_cast<uint64_t>(Lq) * qsa::kHI, 256);
+    if (st != QSA_OK) return st;
+    const int64_t nbk = (q_offset + Lq) / qsa::kBlock;
+    st = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
+    if (st != QSA_OK) return st;
+    e = qsa::launch_index(map_q, map_k, q_offset, Lq, cfg->budget_blocks, w, idx, score, nullptr, ws,
+                          dev_status, sm_count(), s);
+    if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     return ok();
 }
 

@@ -15,18 +15,22 @@ struct RopeFreqs {
     double inv_freq[32];
 };
 
-cudaError_t launch_kprep(int batch, int64_t L, int64_t max_ctx, const uint16_t *ki,
+// Block keys of blocks t_begin/4 .. L/4-1 and RoPE'd K rows t_begin .. L-1
+// (t_begin = 0: everything).
+cudaError_t launch_kprep(int batch, int64_t t_begin, int64_t L, int64_t max_ctx, const uint16_t *ki,
                          const uint16_t *k, uint16_t *k_rot, uint16_t *kblk,
                          const RopeFreqs &freqs, int sms, cudaStream_t stream);
 
 // ---- prefill indexer + selection (tcgen05) ----
 int index_grid(int64_t L, int sms);
 size_t index_cand_bytes(int64_t L, int sms);
-cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t L,
+// Queries are tokens q_off .. q_off+Lq-1 (qi, w, idx, score hold their Lq
+// rows); block keys cover every complete block before q_off+Lq.
+cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t q_off, int64_t Lq,
                          int budget, const uint16_t *w, int32_t *idx, float *score,
                          float *dense, void *cand_ws, int32_t *status, int sms,
                          cudaStream_t stream);
-cudaError_t launch_fill_current_only(int64_t L, int budget, int32_t *idx, float *score,
+cudaError_t launch_fill_current_only(int64_t q_off, int64_t Lq, int budget, int32_t *idx, float *score,
                                      cudaStream_t stream);
 
 // ---- block-sparse attention (prefill and decode splits) ----
@@ -38,7 +42,8 @@ struct AttnArgs {
     const int32_t *idx;      // [items, budget]
     int budget;
     const int32_t *seq_lens; // decode: [B] device; prefill: null
-    int64_t L;               // prefill length (prefill only)
+    int64_t L;               // prefill: number of query rows
+    int64_t q_off;           // prefill: position of the first query row (0 without a cached prefix)
     uint16_t *out;           // final output (nsplit == 1)
     float *lse;              // final lse or null
     float *part_o;           // [B, nsplit, 24, 256] (nsplit > 1)

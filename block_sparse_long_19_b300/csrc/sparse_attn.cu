@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
 
     // ------------------------------------------------------ work item --
     int64_t t;
+    int64_t orow_id;  // output row: the sequence (decode) or the query row (prefill)
     int s = 0, split = 0;
     const uint16_t *qrow;
     const int32_t *irow;
@@ -96,14 +97,16 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
             return;
         }
         t = T - 1;
+        orow_id = s;
         qrow = a.q + static_cast<int64_t>(s) * kHQ * kD;
         irow = a.idx + static_cast<int64_t>(s) * a.budget;
         kbase = a.k + static_cast<int64_t>(s) * a.seq_stride * (kHKV * kD);
         vbase = a.v + static_cast<int64_t>(s) * a.seq_stride * (kHKV * kD);
     } else {
-        t = a.L - 1 - blockIdx.x;
-        qrow = a.q + t * (kHQ * kD);
-        irow = a.idx + t * a.budget;
+        orow_id = a.L - 1 - blockIdx.x;
+        t = a.q_off + orow_id;
+        qrow = a.q + orow_id * (kHQ * kD);
+        irow = a.idx + orow_id * a.budget;
     }
     const int64_t c = t / kBlock;
 
@@ -387,7 +390,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
 
     constexpr float kLn2 = 0.693147180559945309f;
     if (!DECODE || a.nsplit == 1) {
-        uint16_t *orow = a.out + (DECODE ? static_cast<int64_t>(s) : t) * (kHQ * kD);
+        uint16_t *orow = a.out + orow_id * (kHQ * kD);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const float4 o1 = *reinterpret_cast<const float4 *>(&comb[(i * 32 + lane) * 4]);
@@ -402,7 +405,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
                 *reinterpret_cast<uint32_t *>(orow + (g * kGroup + r0 + 8) * kD + d) = pack_bf16(v2, v3);
         }
         if (a.lse && qd == 0) {
-            float *lrow = a.lse + (DECODE ? static_cast<int64_t>(s) : t) * kHQ;
+            float *lrow = a.lse + orow_id * kHQ;
             if (r0 < kGroup)
                 lrow[g * kGroup + r0] = lt[0] > 0.f ? (mt[0] + log2f(lt[0])) * kLn2 : -INFINITY;
             if (r0 + 8 < kGroup)

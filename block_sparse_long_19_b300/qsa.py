@@ -30,7 +30,8 @@ EXPORTED = [
     "qsa_default_config", "qsa_status_string", "qsa_last_error_detail", "qsa_kprep",
     "qsa_index_topk_workspace_bytes", "qsa_index_topk", "qsa_index_scores",
     "qsa_sparse_attn_prefill", "qsa_decode_workspace_bytes", "qsa_sparse_attn_decode",
-    "qsa_sparse_attn_decode_noalloc",
+    "qsa_sparse_attn_decode_noalloc", "qsa_kprep_range", "qsa_index_topk_cached_workspace_bytes",
+    "qsa_index_topk_cached", "qsa_sparse_attn_prefill_cached",
 ]
 
 
@@ -89,6 +90,14 @@ def load(path: str = LIB_PATH):
     L.qsa_sparse_attn_decode_noalloc.argtypes = [cfgp, c.c_int, P, P, P, P, P, P, c.c_int64, P, P,
                                                  P, P, P, P]
     L.qsa_sparse_attn_decode_noalloc.restype = c.c_int
+    L.qsa_kprep_range.argtypes = [cfgp, P, P, P, P, c.c_int64, c.c_int64, P]
+    L.qsa_kprep_range.restype = c.c_int
+    L.qsa_index_topk_cached_workspace_bytes.argtypes = [cfgp, c.c_int64]
+    L.qsa_index_topk_cached_workspace_bytes.restype = c.c_size_t
+    L.qsa_index_topk_cached.argtypes = [cfgp, P, P, P, c.c_int64, c.c_int64, P, P, P, c.c_size_t, P, P]
+    L.qsa_index_topk_cached.restype = c.c_int
+    L.qsa_sparse_attn_prefill_cached.argtypes = [cfgp, P, P, P, P, c.c_int64, c.c_int64, P, P, P, P]
+    L.qsa_sparse_attn_prefill_cached.restype = c.c_int
     _lib = L
     return L
 
@@ -233,6 +242,68 @@ def sparse_attn_prefill(cfg: Config, q, k_rot, v, idx, out=None, lse=None, statu
     _check(load().qsa_sparse_attn_prefill(ctypes.byref(cfg), _ptr(q), _ptr(k_rot), _ptr(v), _ptr(idx),
                                           L, _ptr(out), _ptr(lse), _ptr(status), _stream(stream)),
            "qsa_sparse_attn_prefill")
+    return out, lse, status
+
+
+def kprep_range(cfg: Config, ki, kblk, t_begin: int, t_end: int, k=None, k_rot=None, stream=None):
+    """Block keys of blocks t_begin//4 .. t_end//4-1 into kblk and RoPE'd key
+    rows t_begin .. t_end-1 (a new chunk after a cached prefix)."""
+    _need(ki, "ki", torch.bfloat16)
+    _need(kblk, "kblk", torch.bfloat16)
+    if ki.shape[0] < t_end or kblk.shape[0] < t_end // 4:
+        raise ValueError("ki must hold t_end rows and kblk t_end // 4 rows")
+    if (k is None) != (k_rot is None):
+        raise ValueError("k and k_rot must both be given or both be None")
+    _check(load().qsa_kprep_range(ctypes.byref(cfg), _ptr(ki), _ptr(k), _ptr(k_rot), _ptr(kblk), t_begin,
+                                  t_end, _stream(stream)), "qsa_kprep_range")
+
+
+def index_topk_cached(cfg: Config, qi, w, kblk, q_offset: int, idx=None, score=None, ws=None, status=None,
+                      want_score: bool = True, stream=None):
+    """Indexer + selection for the query rows q_offset .. q_offset+Lq-1 of a
+    sequence whose block keys so far are kblk.  Returns (idx, score, status)."""
+    Lq = qi.shape[0]
+    dev = qi.device
+    _need(qi, "qi", torch.bfloat16, (Lq, 4, 128))
+    _need(w, "w", torch.bfloat16, (Lq, 4))
+    _need(kblk, "kblk", torch.bfloat16)
+    if kblk.shape[0] < (q_offset + Lq) // 4:
+        raise ValueError("kblk must hold (q_offset + Lq) // 4 block keys")
+    B = cfg.budget_blocks
+    if idx is None:
+        idx = torch.empty((Lq, B), dtype=torch.int32, device=dev)
+    if score is None and want_score:
+        score = torch.empty((Lq, B), dtype=torch.float32, device=dev)
+    need = load().qsa_index_topk_cached_workspace_bytes(ctypes.byref(cfg), Lq)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_index_topk_cached(ctypes.byref(cfg), _ptr(qi), _ptr(w), _ptr(kblk), q_offset, Lq,
+                                        _ptr(idx), _ptr(score), _ptr(ws), ws.numel(), _ptr(status),
+                                        _stream(stream)), "qsa_index_topk_cached")
+    return idx, score, status
+
+
+def sparse_attn_prefill_cached(cfg: Config, q, k_rot, v, idx, q_offset: int, out=None, lse=None, status=None,
+                               want_lse: bool = True, stream=None):
+    """Attention for the query rows q_offset .. q_offset+Lq-1 over the whole
+    prefix k_rot / v [q_offset+Lq, 2, 256]."""
+    Lq = q.shape[0]
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (Lq, 24, 256))
+    _need(k_rot, "k_rot", torch.bfloat16, (q_offset + Lq, 2, 256))
+    _need(v, "v", torch.bfloat16, (q_offset + Lq, 2, 256))
+    _need(idx, "idx", torch.int32, (Lq, cfg.budget_blocks))
+    if out is None:
+        out = torch.empty((Lq, 24, 256), dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((Lq, 24), dtype=torch.float32, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_sparse_attn_prefill_cached(ctypes.byref(cfg), _ptr(q), _ptr(k_rot), _ptr(v), _ptr(idx),
+                                                 q_offset, Lq, _ptr(out), _ptr(lse), _ptr(status),
+                                                 _stream(stream)), "qsa_sparse_attn_prefill_cached")
     return out, lse, status
 
 

@@ -162,6 +162,43 @@ qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
                                    void *stream);
 
 /* ------------------------------------------------------------------------
+ * Prefill of a new chunk after a cached prefix (prefix-cache serving: the
+ * launch post, "Model Architecture / Attention: GDN + QSA for Efficient
+ * Memory and Precise Retrieval", measures prefill at a 90% prefix-cache hit
+ * rate).  Only the chunk's Lq query rows are computed; they are positions
+ * q_offset .. q_offset+Lq-1 of the sequence, and their keys are every block
+ * and token before them, cached or new.  The results are those of a full
+ * prefill restricted to these rows (same definition, same kernels).
+ *
+ * qsa_kprep_range: block keys of the complete blocks t_begin/4 .. t_end/4-1
+ *   and RoPE'd key rows t_begin .. t_end-1 (the rows and blocks a new chunk
+ *   adds; a block straddling t_begin is recomputed from ki, which must hold
+ *   every row before t_end).
+ *   ki [t_end, 128]; k, k_rot [t_end, 2, 256] (may alias; both NULL to skip
+ *   RoPE); kblk [t_end/4, 128] out.
+ * qsa_index_topk_cached: qi [Lq, 4, 128], w [Lq, 4] (the chunk's rows; w
+ *   needs only 2-byte alignment, so a chunk may start at any row);
+ *   kblk [(q_offset+Lq)/4, 128] the block keys so far; idx, score [Lq,
+ *   budget] as for qsa_index_topk.  ws: at least
+ *   qsa_index_topk_cached_workspace_bytes(cfg, Lq) bytes, 16-byte aligned.
+ * qsa_sparse_attn_prefill_cached: q [Lq, 24, 256] (the chunk's rows, before
+ *   RoPE); k_rot, v [q_offset+Lq, 2, 256]; idx [Lq, budget]; out [Lq, 24, 256];
+ *   lse [Lq, 24] or NULL.
+ * Errors as for the full-sequence calls; q_offset + Lq is at most 2^24.
+ * ---------------------------------------------------------------------- */
+qsa_status qsa_kprep_range(const qsa_config *cfg, const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot,
+                           qsa_bf16 *kblk, int64_t t_begin, int64_t t_end, void *stream);
+size_t qsa_index_topk_cached_workspace_bytes(const qsa_config *cfg, int64_t Lq);
+qsa_status qsa_index_topk_cached(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                                 const qsa_bf16 *kblk, int64_t q_offset, int64_t Lq, int32_t *idx,
+                                 float *score, void *ws, size_t ws_bytes, int32_t *dev_status,
+                                 void *stream);
+qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 *q,
+                                          const qsa_bf16 *k_rot, const qsa_bf16 *v, const int32_t *idx,
+                                          int64_t q_offset, int64_t Lq, qsa_bf16 *out, float *lse,
+                                          int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Decode: one new token for each of `batch` sequences.  Sequence s holds
  * seq_lens[s] = T tokens in its caches (the new token included, at position
  * T-1, its K/V already written); caches have a stride of max_ctx tokens.

@@ -123,3 +123,35 @@ def test_kprep_rejects(lib):
     assert f(ctypes.byref(cfg), 1, 16, 16, None, None, None, A, None) == 1
     assert f(ctypes.byref(cfg), 1, 16, 16, A, A, None, A, None) == 1
     assert f(ctypes.byref(cfg), 0, 16, 16, A, None, None, A, None) == 1
+
+
+def test_cached_prefix_calls_reject(lib):
+    """The cached-prefix calls validate before launching anything."""
+    cfg = Q.default_config()
+    kr = lib.qsa_kprep_range
+    assert kr(ctypes.byref(cfg), A, None, None, A, 8, 8, None) == 1      # empty range
+    assert kr(ctypes.byref(cfg), A, None, None, A, -1, 8, None) == 1     # negative start
+    assert kr(ctypes.byref(cfg), None, None, None, A, 0, 8, None) == 1   # no ki
+    assert kr(ctypes.byref(cfg), A, A, None, A, 0, 8, None) == 1         # k without k_rot
+    assert kr(ctypes.byref(cfg), A, None, None, A, 0, (1 << 24) + 4, None) == 2
+    assert lib.qsa_index_topk_cached_workspace_bytes(ctypes.byref(cfg), 0) == 0
+    need = lib.qsa_index_topk_cached_workspace_bytes(ctypes.byref(cfg), 1 << 16)
+    assert need > 0
+    ix = lib.qsa_index_topk_cached
+
+    def call(q_off=64, Lq=64, ws_bytes=1 << 40, **kw):
+        a = dict(qi=A, w=A, kb=A, idx=A, sc=None, ws=A, st=A)
+        a.update(kw)
+        return ix(ctypes.byref(cfg), a["qi"], a["w"], a["kb"], q_off, Lq, a["idx"], a["sc"], a["ws"],
+                  ws_bytes, a["st"], None)
+
+    assert call(q_off=-4) == 1
+    assert call(Lq=0) == 1
+    assert call(q_off=1 << 24) == 2
+    assert call(kb=None) == 1
+    assert call(kb=MIS) == 1
+    assert call(ws_bytes=16) == 3
+    at = lib.qsa_sparse_attn_prefill_cached
+    assert at(ctypes.byref(cfg), A, A, A, A, -1, 16, A, None, A, None) == 1
+    assert at(ctypes.byref(cfg), A, A, A, A, 16, 0, A, None, A, None) == 1
+    assert at(ctypes.byref(cfg), A, A, A, None, 16, 16, A, None, A, None) == 1
