@@ -144,6 +144,7 @@ class Workload:
         self.dlse = torch.empty((B, 24), dtype=torch.float32, device=dev)
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.ev = None
+        self.kblk_pre = None  # block keys of the whole sequence (prefix-cache measurement)
 
     def step(self, events=None):
         """One pass of the hot path.  events: optional list of 5 CUDA events
@@ -164,6 +165,25 @@ class Workload:
                              ws=self.ws_dec, status=self.status, want_idx=False)
         if events:
             events[3].record()
+
+    def prefix_step(self, q_off: int, events=None):
+        """Prefill of the rows q_off .. L-1 after a cached prefix of q_off
+        tokens: K-prep of the new rows and blocks, then the indexer and the
+        attention of the new rows only (the cache holds every earlier block
+        key and RoPE'd key row)."""
+        cfg, p = self.cfg, self.p
+        L = self.L
+        if events:
+            events[0].record()
+        Q.kprep_range(cfg, p["ki"], self.kblk_pre, q_off, L, k=p["k"], k_rot=self.k_rot)
+        Q.index_topk_cached(cfg, p["qi"][q_off:], p["w"][q_off:], self.kblk_pre, q_off, idx=self.idx[q_off:],
+                            score=None, ws=self.ws_pre, status=self.status, want_score=False)
+        if events:
+            events[1].record()
+        Q.sparse_attn_prefill_cached(cfg, p["q"][q_off:], self.k_rot, p["v"], self.idx[q_off:], q_off,
+                                     out=self.out[q_off:], lse=self.lse[q_off:], status=self.status)
+        if events:
+            events[2].record()
 
     def launches_per_step(self) -> int:
         n = 2 + 1 + 1      # kprep blocks + kprep rope, indexer, prefill attention
@@ -192,6 +212,32 @@ class Workload:
         c = (self.T - 1) // 4
         keys = min(c, self.budget - 1) * 4 + ((self.T - 1) % 4) + 1
         return self.B * (c * 256 + keys * 2048 + 2 * 24 * 256 * 2)
+
+
+# ------------------------------------------------------- prefix cache --
+
+def run_prefix_cached(wl: Workload, reps: int, warmup: int, full_prefill_ms: float) -> dict:
+    """The serving setup of a 90% prefix-cache hit: the last 10% of the
+    sequence prefilled against the cached 90% (device time, CUDA events)."""
+    L = wl.L
+    q_off = L - L // 10
+    if wl.kblk_pre is None:
+        wl.kblk_pre, _ = Q.kprep(wl.cfg, wl.p["ki"])
+    for _ in range(warmup):
+        wl.prefix_step(q_off)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for i in range(reps):
+        wl.prefix_step(q_off, evs[i])
+    torch.cuda.synchronize()
+    Q.check_status(wl.status, "prefix-cached steps")
+    ms = statistics.mean(e[0].elapsed_time(e[2]) for e in evs)
+    idx_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    att_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    new = L - q_off
+    return {"cached_tokens": q_off, "new_tokens": new, "ms": ms, "new_tokens_per_s": new / (ms / 1e3),
+            "kprep_indexer_ms": idx_ms, "attention_ms": att_ms,
+            "speedup_vs_uncached_prefill": full_prefill_ms / ms}
 
 
 # ----------------------------------------------------------------- e2e --
@@ -474,6 +520,10 @@ def main():
         "gpu_launches": wl.launches_per_step() * K,
         "clocks": clk,
     }
+    try:
+        line["prefix_cached_prefill"] = run_prefix_cached(wl, max(1, min(K, 3)), 2, idx_ms + attn_ms)
+    except Exception as ex:  # report, never fake
+        line["prefix_cached_prefill"] = {"ms": None, "error": str(ex)[:200]}
     if not args.no_e2e:
         try:
             line["e2e"] = run_e2e(wl, max(1, min(K, 3)))

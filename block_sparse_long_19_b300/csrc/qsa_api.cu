@@ -100,17 +100,46 @@ qsa_status check_cfg(const qsa_config *cfg) {
         return fail(QSA_ERR_INVALID_ARG, "rope_theta must be finite and > 0");
     if (!std::isfinite(cfg->softmax_scale))
         return fail(QSA_ERR_INVALID_ARG, "softmax_scale must be finite");
+    if (!std::isfinite(cfg->yarn_factor))
+        return fail(QSA_ERR_INVALID_ARG, "yarn_factor must be finite");
+    if (cfg->yarn_factor > 1.f &&
+        (cfg->yarn_original_max_pos < 1 || !(cfg->yarn_alpha >= 0.f) || !(cfg->yarn_beta > cfg->yarn_alpha) ||
+         !std::isfinite(cfg->yarn_beta)))
+        return fail(QSA_ERR_INVALID_ARG, "YaRN needs original_max_pos >= 1 and 0 <= alpha < beta");
     return QSA_OK;
 }
 
+// Rotary frequencies theta^(-2i/64), rescaled by YaRN when it is on: with
+// r = original context / wavelength, frequencies with r above beta keep their
+// value, those below alpha are divided by the factor, and a linear ramp in r
+// blends the two in between (model card "Processing Ultra-Long Texts"; the
+// published YaRN method).
 qsa::RopeFreqs freqs_of(const qsa_config *cfg) {
     qsa::RopeFreqs f;
-    for (int i = 0; i < 32; ++i) f.inv_freq[i] = std::pow(cfg->rope_theta, -2.0 * i / qsa::kRD);
+    const bool yarn = cfg->yarn_factor > 1.f;
+    for (int i = 0; i < 32; ++i) {
+        const double w = std::pow(cfg->rope_theta, -2.0 * i / qsa::kRD);
+        if (!yarn) {
+            f.inv_freq[i] = w;
+            continue;
+        }
+        const double ratio = static_cast<double>(cfg->yarn_original_max_pos) * w / (2.0 * 3.14159265358979323846);
+        const double a = cfg->yarn_alpha, b = cfg->yarn_beta;
+        double keep = (ratio - a) / (b - a);  // share of the original frequency
+        keep = keep < 0.0 ? 0.0 : (keep > 1.0 ? 1.0 : keep);
+        f.inv_freq[i] = keep * w + (1.0 - keep) * (w / cfg->yarn_factor);
+    }
     return f;
 }
 
+// Softmax scale in the log2 domain; YaRN multiplies the logits by
+// (0.1 ln s + 1)^2 (its temperature on both queries and keys).
 float scale_log2_of(const qsa_config *cfg) {
-    const double sc = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0 / std::sqrt(double(qsa::kD));
+    double sc = cfg->softmax_scale > 0.f ? cfg->softmax_scale : 1.0 / std::sqrt(double(qsa::kD));
+    if (cfg->yarn_factor > 1.f) {
+        const double m = 0.1 * std::log(static_cast<double>(cfg->yarn_factor)) + 1.0;
+        sc *= m * m;
+    }
     return static_cast<float>(sc * 1.4426950408889634);
 }
 
@@ -158,6 +187,10 @@ void qsa_default_config(qsa_config *cfg) {
     cfg->idx_dim = qsa::kDI;
     cfg->rope_theta = 1.0e7;
     cfg->softmax_scale = 1.0f / 16.0f;
+    cfg->yarn_factor = 1.0f;  // off; the model card's setting is 4
+    cfg->yarn_original_max_pos = 262144;
+    cfg->yarn_alpha = 1.0f;
+    cfg->yarn_beta = 32.0f;
 }
 
 const char *qsa_status_string(qsa_status s) {

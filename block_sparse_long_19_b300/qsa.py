@@ -47,6 +47,8 @@ class Config(ctypes.Structure):
         ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int),
         ("rope_dim", ctypes.c_int), ("n_idx_heads", ctypes.c_int), ("idx_dim", ctypes.c_int),
         ("rope_theta", ctypes.c_double), ("softmax_scale", ctypes.c_float),
+        ("yarn_factor", ctypes.c_float), ("yarn_original_max_pos", ctypes.c_int),
+        ("yarn_alpha", ctypes.c_float), ("yarn_beta", ctypes.c_float),
     ]
 
 
@@ -102,12 +104,16 @@ def load(path: str = LIB_PATH):
     return L
 
 
-def default_config(budget: int = 512, rope_theta: float = 1.0e7, softmax_scale: float = 1.0 / 16) -> Config:
+def default_config(budget: int = 512, rope_theta: float = 1.0e7, softmax_scale: float = 1.0 / 16,
+                   yarn_factor: float = 1.0) -> Config:
+    """The model card's configuration; yarn_factor > 1 turns YaRN on (the card
+    uses 4 over an original context of 262,144)."""
     cfg = Config()
     load().qsa_default_config(ctypes.byref(cfg))
     cfg.budget_blocks = budget
     cfg.rope_theta = rope_theta
     cfg.softmax_scale = softmax_scale
+    cfg.yarn_factor = yarn_factor
     return cfg
 
 

@@ -70,7 +70,15 @@ typedef enum {
  * block_size 4, n_q_heads 24, n_kv_heads 2, head_dim 256, rope_dim 64,
  * n_idx_heads 4, idx_dim 128 (anything else -> QSA_ERR_UNSUPPORTED).
  * budget_blocks may be 1..512.  rope_theta > 0.  softmax_scale <= 0 means
- * 1/sqrt(head_dim). */
+ * 1/sqrt(head_dim).
+ * YaRN (model card "Processing Ultra-Long Texts": factor 4 over an original
+ * context of 262,144; the published YaRN method): yarn_factor <= 1 turns it
+ * off (the default).  With s = yarn_factor > 1 every rotary frequency w of
+ * wavelength 2 pi / w becomes (1 - g) w / s + g w, where g ramps linearly
+ * from 0 to 1 as r = yarn_original_max_pos / wavelength goes from
+ * yarn_alpha to yarn_beta (defaults 1 and 32), and the attention logits are
+ * multiplied by (0.1 ln s + 1)^2 on top of softmax_scale.  The same
+ * configuration must be used for K-prep (keys) and attention (queries). */
 typedef struct {
     int block_size;
     int budget_blocks;
@@ -82,9 +90,15 @@ typedef struct {
     int idx_dim;
     double rope_theta;
     float softmax_scale;
+    float yarn_factor;
+    int yarn_original_max_pos;
+    float yarn_alpha;
+    float yarn_beta;
 } qsa_config;
 
-/* Fills the model card's configuration (budget 512, theta 1e7, scale 1/16). */
+/* Fills the model card's configuration (budget 512, theta 1e7, scale 1/16,
+ * YaRN off with the card's factor-4 settings ready: original context 262,144,
+ * alpha 1, beta 32). */
 void qsa_default_config(qsa_config *cfg);
 
 /* Human-readable name of a status code (static storage). */

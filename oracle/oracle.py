@@ -18,7 +18,8 @@ import threading
 import numpy as np
 
 __all__ = [
-    "BS", "HQ", "HKV", "D", "RD", "HI", "DI", "THETA", "SCALE",
+    "BS", "HQ", "HKV", "D", "RD", "HI", "DI", "THETA", "SCALE", "YARN_CARD",
+    "rope_inv_freq", "yarn_logit_factor",
     "build_oracle", "lib", "max_threads",
     "bf16_bits_to_f64", "f64_to_bf16_bits", "block_keys", "rope_exact",
     "rope_row_bf16", "rope_keys", "block_scores", "select", "attend",
@@ -79,23 +80,26 @@ def lib():
             L.qo_f64_to_bf16.argtypes = [c.c_double]
             L.qo_f64_to_bf16.restype = c.c_uint16
             L.qo_block_keys.argtypes = [c.c_int64, _u16p, _u16p]
-            L.qo_rope_exact.argtypes = [_u16p, c.c_double, c.c_int64, _f64p]
-            L.qo_rope_row_bf16.argtypes = [_u16p, c.c_double, c.c_int64, _u16p]
-            L.qo_rope_keys.argtypes = [c.c_int64, c.c_double, _u16p, _u16p]
+            L.qo_rope_inv_freq.argtypes = [c.c_double, c.c_double, c.c_double, c.c_double, c.c_double, _f64p]
+            L.qo_yarn_logit_factor.argtypes = [c.c_double]
+            L.qo_yarn_logit_factor.restype = c.c_double
+            L.qo_rope_exact.argtypes = [_u16p, _f64p, c.c_int64, _f64p]
+            L.qo_rope_row_bf16.argtypes = [_u16p, _f64p, c.c_int64, _u16p]
+            L.qo_rope_keys.argtypes = [c.c_int64, _f64p, _u16p, _u16p]
             L.qo_block_scores.argtypes = [_u16p, _u16p, _u16p, c.c_int64, _f64p]
             L.qo_select.argtypes = [_f64p, c.c_int64, c.c_int, _i32p, _opt(_f64p)]
             L.qo_select.restype = c.c_int
             L.qo_attend.argtypes = [_u16p, c.c_int64, _u16p, _u16p, _i32p, c.c_int,
-                                    c.c_double, c.c_double, _f64p, _f64p]
+                                    _f64p, c.c_double, _f64p, _f64p]
             L.qo_prefill_rows.argtypes = [
-                c.c_int64, c.c_int, c.c_double, c.c_double,
+                c.c_int64, c.c_int, _f64p, c.c_double,
                 _u16p, _u16p, _u16p, _u16p, _u16p, _u16p,
                 _i64p, c.c_int64, _opt(_i32p),
                 _opt(_i32p), _opt(_f64p), _opt(_f64p), _opt(_f64p), c.c_int]
             L.qo_prefill_scores.argtypes = [c.c_int64, _u16p, _u16p, _u16p, _i64p, c.c_int64,
                                             _f64p, c.c_int]
             L.qo_decode.argtypes = [
-                c.c_int, c.c_int64, _i64p, c.c_int, c.c_double, c.c_double,
+                c.c_int, c.c_int64, _i64p, c.c_int, _f64p, c.c_double,
                 _u16p, _u16p, _u16p, _u16p, _u16p, _u16p, _opt(_i32p),
                 _opt(_i32p), _opt(_f64p), _opt(_f64p), _opt(_f64p), c.c_int]
             L.qo_max_threads.restype = c.c_int
@@ -138,26 +142,49 @@ def block_keys(ki) -> np.ndarray:
     return out
 
 
-def rope_exact(x, pos: int, theta: float = THETA) -> np.ndarray:
+# YaRN settings (factor s, original context, ramp alpha, ramp beta) or None:
+# the model card's "Processing Ultra-Long Texts" enables factor 4 over
+# 262,144 positions; alpha = 1, beta = 32 are the published method's values.
+YARN_CARD = (4.0, 262144.0, 1.0, 32.0)
+
+
+def rope_inv_freq(theta: float = THETA, yarn=None) -> np.ndarray:
+    """The 32 rotary frequencies (fp64), YaRN-rescaled when yarn is given."""
+    s, l_orig, alpha, beta = yarn if yarn is not None else (1.0, 1.0, 1.0, 32.0)
+    out = np.zeros(RD // 2, dtype=np.float64)
+    lib().qo_rope_inv_freq(float(theta), float(s), float(l_orig), float(alpha), float(beta), out)
+    return out
+
+
+def yarn_logit_factor(s: float) -> float:
+    """YaRN's attention temperature 1/t = (0.1 ln s + 1)^2 (1 for s <= 1)."""
+    return float(lib().qo_yarn_logit_factor(float(s)))
+
+
+def _attn_scale(scale: float, yarn) -> float:
+    return scale * (yarn_logit_factor(yarn[0]) if yarn is not None else 1.0)
+
+
+def rope_exact(x, pos: int, theta: float = THETA, yarn=None) -> np.ndarray:
     """The 64 rotated dims of one head row, fp64, before rounding."""
     x = _u16(x)
     out = np.zeros(RD, dtype=np.float64)
-    lib().qo_rope_exact(x, theta, int(pos), out)
+    lib().qo_rope_exact(x, rope_inv_freq(theta, yarn), int(pos), out)
     return out
 
 
-def rope_row_bf16(x, pos: int, theta: float = THETA) -> np.ndarray:
+def rope_row_bf16(x, pos: int, theta: float = THETA, yarn=None) -> np.ndarray:
     x = _u16(x)
     out = np.zeros(D, dtype=np.uint16)
-    lib().qo_rope_row_bf16(x, theta, int(pos), out)
+    lib().qo_rope_row_bf16(x, rope_inv_freq(theta, yarn), int(pos), out)
     return out
 
 
-def rope_keys(k, theta: float = THETA) -> np.ndarray:
+def rope_keys(k, theta: float = THETA, yarn=None) -> np.ndarray:
     """K' [rows, 2, 256] bf16 bits for keys at positions 0..rows-1."""
     k = _u16(k)
     out = np.zeros_like(k)
-    lib().qo_rope_keys(k.shape[0], theta, k, out)
+    lib().qo_rope_keys(k.shape[0], rope_inv_freq(theta, yarn), k, out)
     return out
 
 
@@ -181,19 +208,20 @@ def select(s, c: int, budget: int):
     return sel, ss, n
 
 
-def attend(q_t, pos: int, k, v, sel, theta: float = THETA, scale: float = SCALE):
+def attend(q_t, pos: int, k, v, sel, theta: float = THETA, scale: float = SCALE, yarn=None):
     q_t, k, v = _u16(q_t), _u16(k), _u16(v)
     sel = np.ascontiguousarray(np.asarray(sel, dtype=np.int32))
     o = np.zeros((HQ, D), dtype=np.float64)
     lse = np.zeros(HQ, dtype=np.float64)
-    lib().qo_attend(q_t, int(pos), k, v, sel, int(sel.size), theta, scale, o, lse)
+    lib().qo_attend(q_t, int(pos), k, v, sel, int(sel.size), rope_inv_freq(theta, yarn),
+                    _attn_scale(scale, yarn), o, lse)
     return o, lse
 
 
 # ----------------------------------------------------------- whole layer --
 
 def prefill_rows(inputs: dict, rows, budget: int, *, idx_given=None, want_o: bool = True,
-                 theta: float = THETA, scale: float = SCALE, nthreads: int = 0):
+                 theta: float = THETA, scale: float = SCALE, yarn=None, nthreads: int = 0):
     """QSA prefill for the listed query rows.
 
     inputs: dict of uint16 arrays q [L,24,256], k [L,2,256], v [L,2,256],
@@ -213,7 +241,8 @@ def prefill_rows(inputs: dict, rows, budget: int, *, idx_given=None, want_o: boo
     given = None if idx_given is None else np.ascontiguousarray(np.asarray(idx_given, dtype=np.int32))
     if given is not None and given.shape != (n, budget):
         raise ValueError("idx_given must be [nrows, budget]")
-    lib().qo_prefill_rows(L, int(budget), theta, scale, q, k, v, qi, w, ki, rows, n, given,
+    lib().qo_prefill_rows(L, int(budget), rope_inv_freq(theta, yarn), _attn_scale(scale, yarn), q, k, v, qi, w,
+                          ki, rows, n, given,
                           idx, sc, o, lse, int(nthreads))
     return {"idx": idx, "score": sc, "o": o, "lse": lse}
 
@@ -230,7 +259,7 @@ def prefill_scores(inputs: dict, rows, nthreads: int = 0) -> np.ndarray:
 
 
 def decode(inputs: dict, budget: int, *, idx_given=None, want_o: bool = True,
-           theta: float = THETA, scale: float = SCALE, nthreads: int = 0):
+           theta: float = THETA, scale: float = SCALE, yarn=None, nthreads: int = 0):
     """QSA decode, one new token per sequence.
 
     inputs: q [B,24,256], qi [B,4,128], w [B,4], k [B,Tmax,2,256] (pre-RoPE),
@@ -247,6 +276,7 @@ def decode(inputs: dict, budget: int, *, idx_given=None, want_o: bool = True,
     o = np.zeros((B, HQ, D), dtype=np.float64) if want_o else None
     lse = np.zeros((B, HQ), dtype=np.float64) if want_o else None
     given = None if idx_given is None else np.ascontiguousarray(np.asarray(idx_given, dtype=np.int32))
-    lib().qo_decode(B, Tmax, seq, int(budget), theta, scale, q, qi, w, k, v, ki, given,
+    lib().qo_decode(B, Tmax, seq, int(budget), rope_inv_freq(theta, yarn), _attn_scale(scale, yarn), q, qi, w,
+                    k, v, ki, given,
                     idx, sc, o, lse, int(nthreads))
     return {"idx": idx, "score": sc, "o": o, "lse": lse}

@@ -19,7 +19,17 @@
  *         rotary dim 64, indexer = MQA with 4 query heads and 1 shared key
  *         head of dim 128, budget 512 blocks or 2048 tokens.
  *   [MCR] model card, section "Processing Ultra-Long Texts" (rope_parameters):
- *         rope_theta = 10000000, partial_rotary_factor = 0.25.
+ *         rope_theta = 10000000, partial_rotary_factor = 0.25; beyond 262,144
+ *         positions the card enables YaRN with factor 4 over an original
+ *         context of 262,144.
+ *   [YaRN] the published YaRN method (Peng et al., 2023, "YaRN: Efficient
+ *         Context Window Extension of Large Language Models", sections 3.2 to
+ *         3.4), which [MCR] names but does not restate: per rotary frequency
+ *         w_d with wavelength lambda_d = 2 pi / w_d and r_d = L_orig /
+ *         lambda_d, a ramp gamma(r) = 0 below alpha, 1 above beta, linear in
+ *         between (alpha = 1, beta = 32), and w'_d = (1 - gamma) w_d / s +
+ *         gamma w_d; the attention logits get the temperature 1/t with
+ *         sqrt(1/t) = 0.1 ln s + 1.
  *
  * Readings taken where the pages leave a step open (all are listed in the
  * design notes of the repository):
@@ -34,15 +44,17 @@
  *       the (budget-1) best by (score descending, block index ascending) are
  *       selected; if there are fewer past blocks, all of them are;
  *   R5  RoPE on the first 64 of 256 dims, rotate-half pairing (i, i+32),
- *       w_i = theta^(-2i/64), angle = pos * w_i; the rotated values are rounded
- *       to bf16 (the point where the GPU rounds before its tensor cores);
- *       the indexer tensors get no RoPE;
+ *       w_i = theta^(-2i/64) (or its YaRN rescaling, [YaRN] with factor s),
+ *       angle = pos * w_i; the rotated values are rounded to bf16 (the point
+ *       where the GPU rounds before its tensor cores); the indexer tensors get
+ *       no RoPE;
  *   R6  attention over keys j with floor(j/4) selected and j <= t; query head
  *       h reads KV head floor(h/12); softmax scale 1/sqrt(256) unless given;
  *       everything after the bf16 inputs is kept in fp64.
  *
  * All tensors are row-major, bf16 passed as raw uint16 bit patterns.
  */
+#define _GNU_SOURCE
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -111,13 +123,40 @@ void qo_block_keys(int64_t L, const uint16_t *ki, uint16_t *kblk)
 
 /* ---------------------------------------------------------------- RoPE -- */
 
-/* R5, exact part: the 64 rotated values of one head row, in fp64. */
-void qo_rope_exact(const uint16_t *x, double theta, int64_t pos, double *out)
+/* R5: the 32 rotary frequencies w_i = theta^(-2i/64); with a YaRN factor
+ * s > 1, each is rescaled as [YaRN] states: r = L_orig / (2 pi / w_i),
+ * gamma(r) = clamp((r - alpha) / (beta - alpha), 0, 1),
+ * w'_i = (1 - gamma) w_i / s + gamma w_i. */
+void qo_rope_inv_freq(double theta, double s, double l_orig, double alpha, double beta, double *out)
 {
     const int half = QO_RD / 2;
     for (int i = 0; i < half; ++i) {
-        double inv_freq = pow(theta, -2.0 * (double)i / (double)QO_RD);
-        double ang = (double)pos * inv_freq;
+        double w = pow(theta, -2.0 * (double)i / (double)QO_RD);
+        if (s > 1.0) {
+            double lambda = 2.0 * M_PI / w;
+            double r = l_orig / lambda;
+            double gamma = r < alpha ? 0.0 : (r > beta ? 1.0 : (r - alpha) / (beta - alpha));
+            w = (1.0 - gamma) * w / s + gamma * w;
+        }
+        out[i] = w;
+    }
+}
+
+/* [YaRN]: the factor the attention logits are multiplied by, (0.1 ln s + 1)^2
+ * (both query and key carry sqrt(1/t)); 1 without YaRN. */
+double qo_yarn_logit_factor(double s)
+{
+    if (s <= 1.0) return 1.0;
+    double m = 0.1 * log(s) + 1.0;
+    return m * m;
+}
+
+/* R5, exact part: the 64 rotated values of one head row, in fp64. */
+void qo_rope_exact(const uint16_t *x, const double *inv_freq, int64_t pos, double *out)
+{
+    const int half = QO_RD / 2;
+    for (int i = 0; i < half; ++i) {
+        double ang = (double)pos * inv_freq[i];
         double c = cos(ang), s = sin(ang);
         double x1 = qo_bf16_to_f64(x[i]);
         double x2 = qo_bf16_to_f64(x[i + half]);
@@ -128,20 +167,20 @@ void qo_rope_exact(const uint16_t *x, double theta, int64_t pos, double *out)
 
 /* R5: one full head row (256 dims) after RoPE, as the bf16 the tensor cores
  * see: dims [0,64) rotated and rounded, dims [64,256) passed through. */
-void qo_rope_row_bf16(const uint16_t *x, double theta, int64_t pos, uint16_t *out)
+void qo_rope_row_bf16(const uint16_t *x, const double *inv_freq, int64_t pos, uint16_t *out)
 {
     double rot[QO_RD];
-    qo_rope_exact(x, theta, pos, rot);
+    qo_rope_exact(x, inv_freq, pos, rot);
     for (int i = 0; i < QO_RD; ++i) out[i] = qo_f64_to_bf16(rot[i]);
     for (int i = QO_RD; i < QO_D; ++i) out[i] = x[i];
 }
 
 /* K' for a whole [rows, 2, 256] key tensor at positions 0..rows-1. */
-void qo_rope_keys(int64_t rows, double theta, const uint16_t *k, uint16_t *k_rot)
+void qo_rope_keys(int64_t rows, const double *inv_freq, const uint16_t *k, uint16_t *k_rot)
 {
     for (int64_t j = 0; j < rows; ++j)
         for (int g = 0; g < QO_HKV; ++g)
-            qo_rope_row_bf16(k + (j * QO_HKV + g) * QO_D, theta, j,
+            qo_rope_row_bf16(k + (j * QO_HKV + g) * QO_D, inv_freq, j,
                              k_rot + (j * QO_HKV + g) * QO_D);
 }
 
@@ -221,7 +260,7 @@ int qo_select(const double *s, int64_t c, int budget, int32_t *sel, double *sel_
  *   sel   selected blocks (entries < 0 ignored), nsel entries
  *   o     [24,256] output, lse [24] natural-log log-sum-exp of the scaled logits */
 void qo_attend(const uint16_t *q_t, int64_t pos, const uint16_t *k, const uint16_t *v,
-               const int32_t *sel, int nsel, double theta, double scale,
+               const int32_t *sel, int nsel, const double *inv_freq, double scale,
                double *o, double *lse)
 {
     /* gather the attended key positions */
@@ -235,14 +274,14 @@ void qo_attend(const uint16_t *q_t, int64_t pos, const uint16_t *k, const uint16
         }
     }
     uint16_t qrot[QO_HQ][QO_D];
-    for (int h = 0; h < QO_HQ; ++h) qo_rope_row_bf16(q_t + h * QO_D, theta, pos, qrot[h]);
+    for (int h = 0; h < QO_HQ; ++h) qo_rope_row_bf16(q_t + h * QO_D, inv_freq, pos, qrot[h]);
 
     double *z = (double *)malloc(sizeof(double) * (size_t)(QO_HQ * (nkeys > 0 ? nkeys : 1)));
     uint16_t krot[QO_D];
     for (int64_t jj = 0; jj < nkeys; ++jj) {
         int64_t j = keys[jj];
         for (int g = 0; g < QO_HKV; ++g) {
-            qo_rope_row_bf16(k + (j * QO_HKV + g) * QO_D, theta, j, krot);
+            qo_rope_row_bf16(k + (j * QO_HKV + g) * QO_D, inv_freq, j, krot);
             for (int h = g * (QO_HQ / QO_HKV); h < (g + 1) * (QO_HQ / QO_HKV); ++h) {
                 double dot = 0.0;
                 for (int d = 0; d < QO_D; ++d)
@@ -280,7 +319,7 @@ void qo_attend(const uint16_t *q_t, int64_t pos, const uint16_t *k, const uint16
  * If idx_given is non-NULL ([nrows,budget]), the selection step is skipped
  * and attention runs over the given blocks (used to compare attention on
  * one and the same selection). */
-void qo_prefill_rows(int64_t L, int budget, double theta, double scale,
+void qo_prefill_rows(int64_t L, int budget, const double *inv_freq, double scale,
                      const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      const uint16_t *qi, const uint16_t *w, const uint16_t *ki,
                      const int64_t *rows, int64_t nrows, const int32_t *idx_given,
@@ -317,7 +356,7 @@ void qo_prefill_rows(int64_t L, int budget, double theta, double scale,
         if (sel_score) memcpy(sel_score + r * budget, ss, sizeof(double) * (size_t)budget);
         if (o || lse) {
             double ob[QO_HQ * QO_D], lb[QO_HQ];
-            qo_attend(q + t * QO_HQ * QO_D, t, k, v, sel, nsel, theta, scale, ob, lb);
+            qo_attend(q + t * QO_HQ * QO_D, t, k, v, sel, nsel, inv_freq, scale, ob, lb);
             if (o) memcpy(o + r * QO_HQ * QO_D, ob, sizeof ob);
             if (lse) memcpy(lse + r * QO_HQ, lb, sizeof lb);
         }
@@ -355,7 +394,7 @@ void qo_prefill_scores(int64_t L, const uint16_t *qi, const uint16_t *w, const u
  *   k_raw, v [B,Tmax,2,256] (k pre-RoPE), ki_raw [B,Tmax,128]
  *   q [B,24,256] pre-RoPE, qi [B,4,128], w [B,4]
  * Outputs [B,budget] / [B,24,256] / [B,24]; idx_given as for prefill. */
-void qo_decode(int B, int64_t Tmax, const int64_t *seq_lens, int budget, double theta,
+void qo_decode(int B, int64_t Tmax, const int64_t *seq_lens, int budget, const double *inv_freq,
                double scale, const uint16_t *q, const uint16_t *qi, const uint16_t *w,
                const uint16_t *k_raw, const uint16_t *v, const uint16_t *ki_raw,
                const int32_t *idx_given, int32_t *idx, double *sel_score, double *o,
@@ -389,7 +428,7 @@ void qo_decode(int B, int64_t Tmax, const int64_t *seq_lens, int budget, double 
         if (sel_score) memcpy(sel_score + (int64_t)s * budget, ss, sizeof(double) * (size_t)budget);
         if (o || lse) {
             double ob[QO_HQ * QO_D], lb[QO_HQ];
-            qo_attend(q + (int64_t)s * QO_HQ * QO_D, t, ks, vs, sel, budget, theta, scale, ob, lb);
+            qo_attend(q + (int64_t)s * QO_HQ * QO_D, t, ks, vs, sel, budget, inv_freq, scale, ob, lb);
             if (o) memcpy(o + (int64_t)s * QO_HQ * QO_D, ob, sizeof ob);
             if (lse) memcpy(lse + (int64_t)s * QO_HQ, lb, sizeof lb);
         }

@@ -155,3 +155,15 @@ def test_cached_prefix_calls_reject(lib):
     assert at(ctypes.byref(cfg), A, A, A, A, -1, 16, A, None, A, None) == 1
     assert at(ctypes.byref(cfg), A, A, A, A, 16, 0, A, None, A, None) == 1
     assert at(ctypes.byref(cfg), A, A, A, None, 16, 16, A, None, A, None) == 1
+
+
+def test_yarn_config_checked(lib):
+    cfg = Q.default_config(yarn_factor=4.0)
+    cfg.yarn_beta = cfg.yarn_alpha  # empty ramp
+    f = lib.qsa_sparse_attn_prefill
+    assert f(ctypes.byref(cfg), A, A, A, A, 16, A, None, A, None) == 1
+    cfg = Q.default_config(yarn_factor=float("nan"))
+    assert f(ctypes.byref(cfg), A, A, A, A, 16, A, None, A, None) == 1
+    cfg = Q.default_config(yarn_factor=4.0)
+    cfg.yarn_original_max_pos = 0
+    assert f(ctypes.byref(cfg), A, A, A, A, 16, A, None, A, None) == 1

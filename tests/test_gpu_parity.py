@@ -270,3 +270,41 @@ def test_decode_short_sequences():
     ref = O.decode(hd, budget)
     assert np.array_equal(idx.cpu().numpy(), ref["idx"])
     check_outputs(bf16_to_f64(out), ref["o"], "O")
+
+
+# ------------------------------------------------------------------ YaRN --
+
+def test_yarn_prefill_and_decode():
+    """YaRN on (model card: factor 4 over 262,144): RoPE'd keys, prefill and
+    decode attention against the oracle with the same setting; the selection
+    does not depend on it (the indexer has no RoPE)."""
+    L, budget = 4133, 512
+    cfg = Q.default_config(budget=budget, yarn_factor=4.0)
+    t = W.prefill_inputs(L, 51, DEV)
+    hb = W.host_bits(t)
+    res = Q.prefill(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"])
+    torch.cuda.synchronize()
+    Q.check_status(res.status)
+    check_rope(W.to_bits(res.k_rot), O.rope_keys(hb["k"], yarn=O.YARN_CARD), hb["k"])
+    rows = sample_rows(L, 24, 7)
+    idx_g = res.idx.cpu().numpy()[rows]
+    ref = O.prefill_rows(hb, rows, budget, want_o=False)
+    check_selection(idx_g, ref["idx"], O.prefill_scores(hb, rows), rows, budget)
+    att = O.prefill_rows(hb, rows, budget, idx_given=idx_g, yarn=O.YARN_CARD)
+    check_outputs(bf16_to_f64(res.out[torch.as_tensor(rows, device=DEV)]), att["o"], "O")
+    check_outputs(res.lse.cpu().numpy().astype(np.float64)[rows], att["lse"], "LSE")
+    plain = O.prefill_rows(hb, rows[-3:], budget, idx_given=idx_g[-3:])
+    assert not np.allclose(plain["lse"], att["lse"][-3:])  # the setting does reach the kernels
+
+    B, Tmax = 2, 8192
+    lens = [Tmax, 3001]
+    d = W.decode_inputs(B, Tmax, 52, DEV, seq_lens=lens)
+    hd = W.host_bits(d)
+    k_rot = torch.empty_like(d["k"])
+    kblk, _ = Q.kprep(cfg, d["ki"], d["k"], k_rot=k_rot)
+    out, lse, idx, st = Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], k_rot, d["v"], kblk, d["seq_lens"])
+    torch.cuda.synchronize()
+    Q.check_status(st)
+    att = O.decode(hd, budget, idx_given=idx.cpu().numpy(), yarn=O.YARN_CARD)
+    check_outputs(bf16_to_f64(out), att["o"], "O")
+    check_outputs(lse.cpu().numpy().astype(np.float64), att["lse"], "LSE")

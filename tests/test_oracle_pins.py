@@ -142,6 +142,75 @@ def test_rope_norm_and_relative_position():
         assert abs(a - b) < 1e-9 * (1 + abs(a))
 
 
+# ------------------------------------------------------------------ YaRN --
+# YaRN (model card "Processing Ultra-Long Texts": factor 4 over 262,144; the
+# published method): a frequency whose wavelength fits more than beta = 32
+# times into the original context keeps its value; one whose wavelength is
+# longer than the original context (r < alpha = 1) is interpolated by the
+# factor; in between the two are blended.
+
+def _wavelength_ratio(i):
+    return O.YARN_CARD[1] / (2 * math.pi / O.THETA ** (-2.0 * i / 64.0))
+
+
+def test_yarn_off_is_plain_rope():
+    assert np.array_equal(O.rope_inv_freq(O.THETA, None), O.rope_inv_freq(O.THETA, (1.0, 262144.0, 1.0, 32.0)))
+    assert O.yarn_logit_factor(1.0) == 1.0
+
+
+def test_yarn_keeps_fast_dims_and_interpolates_slow_dims():
+    """Fast rotary pairs rotate exactly as without YaRN; slow pairs rotate at
+    position 4p exactly as without YaRN at p (position interpolation by the
+    factor 4).  Checked on the rotation itself, through rope_exact."""
+    g = torch.Generator().manual_seed(41)
+    fast = [i for i in range(32) if _wavelength_ratio(i) > 32.0]
+    slow = [i for i in range(32) if _wavelength_ratio(i) < 1.0]
+    assert fast and slow and max(fast) < min(slow)
+    for _ in range(4):
+        x = bits(torch.randn(O.D, generator=g))
+        p = int(torch.randint(0, 1 << 18, (1,), generator=g))
+        plain_p = O.rope_exact(x, p)
+        yarn_p = O.rope_exact(x, p, yarn=O.YARN_CARD)
+        yarn_4p = O.rope_exact(x, 4 * p, yarn=O.YARN_CARD)
+        plain_4p = O.rope_exact(x, 4 * p)
+        for i in fast:
+            assert yarn_p[i] == plain_p[i] and yarn_p[i + 32] == plain_p[i + 32]
+            assert yarn_4p[i] == plain_4p[i]
+        for i in slow:
+            assert yarn_4p[i] == plain_p[i] and yarn_4p[i + 32] == plain_p[i + 32]
+
+
+def test_yarn_blend_is_between_and_monotone():
+    w = O.rope_inv_freq(O.THETA, None)
+    wy = O.rope_inv_freq(O.THETA, O.YARN_CARD)
+    assert np.all(wy <= w) and np.all(wy >= w / 4.0)
+    assert np.all(np.diff(wy) < 0)  # still strictly decreasing frequencies
+    mid = [i for i in range(32) if 1.0 < _wavelength_ratio(i) < 32.0]
+    assert mid and all(w[i] / 4.0 < wy[i] < w[i] for i in mid)
+
+
+def test_yarn_temperature_scales_logits_only():
+    """With the rotary dims zero, RoPE cannot matter: YaRN attention equals
+    plain attention with the softmax scale times the YaRN logit factor."""
+    g = torch.Generator().manual_seed(43)
+    L = 24
+    q = torch.randn(L, 24, 256, generator=g)
+    k = torch.randn(L, 2, 256, generator=g)
+    q[..., :64] = 0
+    k[..., :64] = 0
+    hb = {"q": bits(q), "k": bits(k), "v": bits(torch.randn(L, 2, 256, generator=g)),
+          "qi": bits(torch.randn(L, 4, 128, generator=g)), "w": bits(torch.rand(L, 4, generator=g)),
+          "ki": bits(torch.randn(L, 128, generator=g))}
+    rows = [3, 11, 23]
+    y = O.prefill_rows(hb, rows, 512, yarn=O.YARN_CARD)
+    f = O.yarn_logit_factor(4.0)
+    assert f > 1.0
+    p = O.prefill_rows(hb, rows, 512, scale=O.SCALE * f)
+    assert np.array_equal(y["idx"], p["idx"])
+    assert np.allclose(y["o"], p["o"], rtol=0, atol=1e-12)
+    assert np.allclose(y["lse"], p["lse"], rtol=0, atol=1e-12)
+
+
 # ---------------------------------------------------------------- scores --
 
 def _kblk_and_q(seed, nb=50, positive=False):
