@@ -240,6 +240,90 @@ def run_prefix_cached(wl: Workload, reps: int, warmup: int, full_prefill_ms: flo
             "speedup_vs_uncached_prefill": full_prefill_ms / ms}
 
 
+# ------------------------------------------------------ dense compare --
+
+def _sdpa_backends():
+    from torch.nn.attention import SDPBackend
+    return [("cudnn", SDPBackend.CUDNN_ATTENTION), ("flash", SDPBackend.FLASH_ATTENTION),
+            ("efficient", SDPBackend.EFFICIENT_ATTENTION)]
+
+
+def run_dense_comparison(wl: Workload, qsa_prefill_ms: float, qsa_decode_ms: float, reps: int = 3) -> dict:
+    """Dense causal GQA attention of the same shapes through torch's fused
+    SDPA kernels (the comparator of the launch post's 7.6x prefill / 4.9x
+    decode kernel speed-ups, "Attention: GDN + QSA").  Prefill: a sample of
+    query rows at the end of the sequence against all earlier keys (their
+    visible-prefix part without a mask plus their own causal square),
+    extrapolated by the number of (query, key) pairs; decode: every cached key
+    of every sequence.  Device time with CUDA events."""
+    import torch.nn.functional as F
+    from torch.nn.attention import sdpa_kernel
+
+    L, dev = wl.L, wl.dev
+    nq = min(16384, L)
+    a = L - nq
+    scale = 1.0 / 16
+    # [1, heads, tokens, 256] layouts (copies: the kernels want them contiguous)
+    kd = wl.k_rot.permute(1, 0, 2).unsqueeze(0).contiguous()
+    vd = wl.p["v"].permute(1, 0, 2).unsqueeze(0).contiguous()
+    qd = wl.p["q"][a:].permute(1, 0, 2).unsqueeze(0).contiguous()
+
+    def prefill_sample():
+        o1 = F.scaled_dot_product_attention(qd, kd[:, :, :a], vd[:, :, :a], scale=scale, enable_gqa=True) \
+            if a > 0 else None
+        o2 = F.scaled_dot_product_attention(qd, kd[:, :, a:], vd[:, :, a:], is_causal=True, scale=scale,
+                                            enable_gqa=True)
+        return o1, o2
+
+    dq = wl.d["q"].unsqueeze(2)                                    # [B, 24, 1, 256]
+    dk = wl.d["k"].permute(0, 2, 1, 3)                             # [B, 2, T, 256] views
+    dv = wl.d["v"].permute(0, 2, 1, 3)
+    dkc, dvc = dk.contiguous(), dv.contiguous()
+
+    def decode_step():
+        return F.scaled_dot_product_attention(dq, dkc, dvc, scale=scale, enable_gqa=True)
+
+    def timed(fn):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    out = {"comparator": "torch.nn.functional.scaled_dot_product_attention (dense causal GQA, bf16)"}
+    for name, be in _sdpa_backends():
+        try:
+            with sdpa_kernel([be]):
+                ms = timed(prefill_sample)
+            pairs_sample = nq * a + nq * (nq + 1) / 2
+            pairs_all = L * (L + 1) / 2
+            out.update({"prefill_backend": name, "prefill_sample": f"{nq} query rows at positions {a}..{L - 1}",
+                        "prefill_sample_ms": ms, "prefill_ms_extrapolated": ms * pairs_all / pairs_sample,
+                        "prefill_speedup_qsa": ms * pairs_all / pairs_sample / qsa_prefill_ms})
+            break
+        except Exception as ex:  # this backend does not take these shapes here
+            out.setdefault("prefill_backend_errors", []).append(f"{name}: {str(ex)[:120]}")
+    for name, be in _sdpa_backends():
+        try:
+            with sdpa_kernel([be]):
+                ms = timed(decode_step)
+            out.update({"decode_backend": name, "decode_ms": ms, "decode_speedup_qsa": ms / qsa_decode_ms})
+            break
+        except Exception as ex:
+            out.setdefault("decode_backend_errors", []).append(f"{name}: {str(ex)[:120]}")
+    del kd, vd, qd, dkc, dvc
+    torch.cuda.empty_cache()
+    out["pages_context"] = "launch post: up to 7.6x prefill, 4.9x decode at 1M (their hardware and baseline)"
+    return out
+
+
 # ----------------------------------------------------------------- e2e --
 
 def run_e2e(wl: Workload, steps: int) -> dict:
@@ -428,6 +512,7 @@ def main():
     ap.add_argument("--workload", default="qsa_1m", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparison")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -524,6 +609,11 @@ def main():
         line["prefix_cached_prefill"] = run_prefix_cached(wl, max(1, min(K, 3)), 2, idx_ms + attn_ms)
     except Exception as ex:  # report, never fake
         line["prefix_cached_prefill"] = {"ms": None, "error": str(ex)[:200]}
+    if rank == 0 and not args.no_dense:
+        try:
+            line["dense_comparison"] = run_dense_comparison(wl, idx_ms + attn_ms, dec_ms)
+        except Exception as ex:
+            line["dense_comparison"] = {"error": str(ex)[:200]}
     if not args.no_e2e:
         try:
             line["e2e"] = run_e2e(wl, max(1, min(K, 3)))
