@@ -45,6 +45,9 @@ WORKLOADS = {
     # profiling cases: inputs larger than L2, a few GB on the device
     "prof_128k": (131072, 512, 2, 1, 65536, 3),
     "prof_256k": (262144, 512, 4, 1, 65536, 3),
+    # NEXT-row workload: topic segments of 8192 tokens (neighbouring queries
+    # select overlapping blocks), same sizes as qsa_1m
+    "qsa_1m_local": (1 << 20, 512, 4, 8, 1 << 20, 4, 8192),
     "prof_decode": (4096, 512, 6, 8, 131072, 6),
 }
 
@@ -120,12 +123,14 @@ class ClockSampler:
 
 class Workload:
     def __init__(self, name: str, dev: str):
-        L, budget, pseed, B, T, dseed = WORKLOADS[name]
+        L, budget, pseed, B, T, dseed, *rest = WORKLOADS[name]
+        locality = rest[0] if rest else 0
+        self.locality = locality
         self.name, self.L, self.budget, self.B, self.T = name, L, budget, B, T
         self.dev = dev
         self.cfg = Q.default_config(budget=budget)
         log(f"[bench] generating {name}: prefill L={L}, decode {B}x{T}")
-        self.p = W.prefill_inputs(L, pseed, dev)
+        self.p = W.prefill_inputs(L, pseed, dev, locality=locality)
         d = W.decode_inputs(B, T, dseed, dev)
         # fill the decode caches once (RoPE'd keys in place, block keys); this
         # is cache state, not part of a step
@@ -376,9 +381,10 @@ def oracle_sample(wl_name: str, target_s: float = 12.0, host_inputs=None) -> dic
     workload's prefill query rows (all steps of the layer per row)."""
     import oracle as O
 
-    L, budget, pseed, B, T, dseed = WORKLOADS[wl_name]
+    L, budget, pseed, B, T, dseed, *rest = WORKLOADS[wl_name]
     if host_inputs is None:
-        t = W.prefill_inputs(L, pseed, "cuda" if torch.cuda.is_available() else "cpu")
+        t = W.prefill_inputs(L, pseed, "cuda" if torch.cuda.is_available() else "cpu",
+                             locality=rest[0] if rest else 0)
     else:
         t = host_inputs
     rng = np.random.default_rng(12345)
@@ -436,7 +442,9 @@ def run_reference(args):
     budget_s = 150.0 / max(1, args.steps + args.warmup)
     vals = []
     res = None
-    t = W.prefill_inputs(L, WORKLOADS[wl_name][2], "cuda" if torch.cuda.is_available() else "cpu")
+    rest = WORKLOADS[wl_name][6:]
+    t = W.prefill_inputs(L, WORKLOADS[wl_name][2], "cuda" if torch.cuda.is_available() else "cpu",
+                         locality=rest[0] if rest else 0)
     for i in range(args.warmup + args.steps):
         res = oracle_sample(wl_name, target_s=min(budget_s, 12.0), host_inputs=t)
         if i >= args.warmup:
@@ -585,6 +593,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "prefill_L": wl.L, "budget_blocks": wl.budget,
+                   "topic_segment_tokens": wl.locality or None,
                    "decode_batch": wl.B, "decode_ctx": wl.T,
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},

@@ -107,26 +107,30 @@ __device__ __forceinline__ void tmem_load16_sync(uint32_t taddr, uint32_t (&r)[1
         : "memory");
 }
 
-// Bounded wait on an mbarrier phase that lets the hardware suspend the
-// thread until the phase completes (up to a microsecond per try) instead of
-// spinning on the issue slots the epilogue warps need.
+// Bounded wait on an mbarrier phase that gives the issue slots away while it
+// waits: after a failed test the warp sleeps (nanosleep takes it off the
+// scheduler), so a waiting warp does not compete with the warps that score.
+// The clock is read only every 64 tries.
+template <int SLEEP_NS>
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity) {
     auto try_once = [&]() {
         uint32_t done;
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done)
-            : "r"(smem_u32(bar)), "r"(parity), "r"(1000u)
+            : "r"(smem_u32(bar)), "r"(parity)
             : "memory");
         return done != 0;
     };
     if (try_once()) return true;
     const unsigned long long t0 = globaltimer();
-    while (!try_once())
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
-    return true;
+    for (unsigned n = 1;; ++n) {
+        __nanosleep(SLEEP_NS);
+        if (try_once()) return true;
+        if ((n & 63u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // Barrier among the 4 warps (128 threads) of one epilogue group that is also a
@@ -462,7 +466,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 tma_load_2d(sQ + SQ_BYTES / 2, &map_q, qfull, 64, q * NCOL);
                 for (int j = 0; j < nbt; ++j) {
                     if (sMisc[1]) { ok = false; break; }
-                    if (!mbar_wait_sleep(&empty[st], ph ^ 1)) { ok = false; break; }
+                    if (!mbar_wait_sleep<256>(&empty[st], ph ^ 1)) { ok = false; break; }
                     uint8_t *dst = sK + st * SK_BYTES;
                     mbar_arrive_expect_tx(&full[st], SK_BYTES);
                     tma_load_2d(dst, &map_k, &full[st], 0, j * TB);
@@ -493,8 +497,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (sMisc[1]) { ok = false; break; }
                     const uint32_t buf = acc & 1;
                     const uint32_t use = acc >> 1;
-                    if (!mbar_wait_sleep(&tempty[buf], (use & 1) ^ 1)) { ok = false; break; }
-                    if (!mbar_wait_sleep(&full[st], ph)) { ok = false; break; }
+                    if (!mbar_wait_sleep<64>(&tempty[buf], (use & 1) ^ 1)) { ok = false; break; }
+                    if (!mbar_wait_sleep<64>(&full[st], ph)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d = tmem_base + buf * NCOL;
 #pragma unroll
@@ -565,7 +569,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // vote also makes sure the whole group goes on to the selection)
                 const bool last = j == nbt - 1;
                 const bool check = !DENSE && (last || (j + 1) % CHK == 0);
-                if (ok && !mbar_wait_sleep(&tfull[buf], use & 1)) ok = false;
+                if (ok && !mbar_wait_sleep<64>(&tfull[buf], use & 1)) ok = false;
                 if (!ok) {  // skip the work, keep taking part in the votes
                     ++acc;
                     if (check && group_sync_fail(bar, true)) break;

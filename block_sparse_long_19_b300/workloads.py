@@ -18,6 +18,10 @@ The workloads (name -> sizes):
   decode_64x256k   64 sequences x 262144 cached tokens, budget 512, seed 3
   prefill_1m       L=1048576, budget 512, seed 4
   decode_8x1m      8 sequences x 1048576 cached tokens, budget 512, seed 4
+
+Locality variant (prefill_inputs(..., locality=S)): neighbouring queries share
+a topic, so their selections overlap -- the structure real long contexts
+have and i.i.d. draws lack (see locality_plant).
 """
 from __future__ import annotations
 
@@ -63,10 +67,11 @@ def _uniform(shape, g, device) -> torch.Tensor:
     return torch.rand(shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16)
 
 
-def prefill_inputs(L: int, seed: int, device="cpu", needle: bool = False) -> dict:
+def prefill_inputs(L: int, seed: int, device="cpu", needle: bool = False, locality: int = 0) -> dict:
     """One sequence of L tokens: q [L,24,256], k/v [L,2,256] (k before RoPE),
     qi [L,4,128], w [L,4], ki [L,128].  With needle=True, also returns
-    'needle_blocks' (int64 [8]) -- see needle_plant."""
+    'needle_blocks' (int64 [8]) -- see needle_plant.  locality=S > 0 plants
+    topic segments of S tokens (see locality_plant)."""
     g = _gen(device, seed)
     t = {
         "q": _normal((L, HQ, D), g, device),
@@ -78,7 +83,30 @@ def prefill_inputs(L: int, seed: int, device="cpu", needle: bool = False) -> dic
     }
     if needle:
         needle_plant(t, seed, device)
+    if locality:
+        locality_plant(t, seed, locality, device)
     return t
+
+
+LOCALITY_GAIN = 3.0
+
+
+def locality_plant(t: dict, seed: int, seg: int, device, chunk_rows: int = 1 << 16) -> None:
+    """Topic segments: tokens [s*seg, (s+1)*seg) share a random unit
+    direction u_s in R^128; every indexer query head of those tokens gets
+    +3.0*u_s and their indexer keys +3.0*sqrt(128)*u_s.  A query's own
+    segment then outscores the rest of the context, so nearby queries select
+    mostly the same blocks.  Values are rounded to bf16."""
+    L = t["ki"].shape[0]
+    g = _gen(device, seed + 2000)
+    nseg = (L + seg - 1) // seg
+    u = torch.randn(nseg, DI, generator=g, device=device, dtype=torch.float32)
+    u = u / u.norm(dim=1, keepdim=True)
+    for r0 in range(0, L, chunk_rows):
+        r1 = min(L, r0 + chunk_rows)
+        us = u[torch.arange(r0, r1, device=device) // seg]          # [rows, 128]
+        t["qi"][r0:r1] = (t["qi"][r0:r1].float() + LOCALITY_GAIN * us[:, None, :]).to(torch.bfloat16)
+        t["ki"][r0:r1] = (t["ki"][r0:r1].float() + LOCALITY_GAIN * math.sqrt(DI) * us).to(torch.bfloat16)
 
 
 def needle_plant(t: dict, seed: int, device) -> None:

@@ -308,3 +308,24 @@ def test_yarn_prefill_and_decode():
     att = O.decode(hd, budget, idx_given=idx.cpu().numpy(), yarn=O.YARN_CARD)
     check_outputs(bf16_to_f64(out), att["o"], "O")
     check_outputs(lse.cpu().numpy().astype(np.float64), att["lse"], "LSE")
+
+
+# ------------------------------------------------ locality-structured input --
+
+def test_locality_workload_selects_own_topic_and_matches_oracle():
+    """Topic segments of 2048 tokens: selection and outputs against the
+    oracle, and most selected past blocks come from the query's own segment
+    (the structure that makes neighbouring selections overlap)."""
+    L, budget, seg = 12288, 512, 2048
+    t = W.prefill_inputs(L, 61, DEV, locality=seg)
+    hb = W.host_bits(t)
+    res = run_prefill(t, budget)
+    rows = sample_rows(L, 32, 8)
+    oracle_compare_prefill(t, hb, res, rows, budget)
+    idx = res.idx.cpu().numpy()
+    late = [r for r in rows if r % seg >= seg // 2 and r >= seg]  # own segment has >= 256 past blocks
+    own = []
+    for r in late:
+        blocks = idx[r][idx[r] >= 0][:-1]
+        own.append(np.mean((blocks * 4) // seg == r // seg))
+    assert own and np.mean(own) > 0.45
