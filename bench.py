@@ -17,6 +17,7 @@ the attention output copied back, inside the timed region.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import math
 import os
@@ -329,6 +330,33 @@ def run_dense_comparison(wl: Workload, qsa_prefill_ms: float, qsa_decode_ms: flo
     return out
 
 
+# -------------------------------------------------------- token level --
+
+def run_token_level(wl: Workload, block_indexer_ms: float, reps: int = 2) -> dict:
+    """The DSA-style token-level indexer on the same inputs (one token per
+    selection unit, budget 512 tokens): the launch post's argument that a
+    token-level indexer costs ~4x more than 4-token micro-blocks
+    ("Attention: GDN + QSA").  Device time with CUDA events."""
+    cfg, p = wl.cfg, wl.p
+    ws = torch.empty(Q.load().qsa_index_topk_tokens_workspace_bytes(ctypes.byref(cfg), wl.L),
+                     dtype=torch.uint8, device=wl.dev)
+    Q.index_topk_tokens(cfg, p["qi"], p["w"], p["ki"], idx=wl.idx, ws=ws, status=wl.status, want_score=False)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        Q.index_topk_tokens(cfg, p["qi"], p["w"], p["ki"], idx=wl.idx, ws=ws, status=wl.status, want_score=False)
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    Q.check_status(wl.status, "token-level indexer")
+    ms = statistics.median(ts)
+    pairs = float(np.sum(np.arange(wl.L, dtype=np.float64)))
+    return {"ms": ms, "units": "tokens", "budget_tokens": wl.budget, "tflops": pairs * 1024 / (ms / 1e3) / 1e12,
+            "vs_block_indexer": ms / block_indexer_ms}
+
+
 # ----------------------------------------------------------------- e2e --
 
 def run_e2e(wl: Workload, steps: int) -> dict:
@@ -521,6 +549,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparison")
+    ap.add_argument("--no-token-level", action="store_true", help="skip the token-level indexer comparison")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -618,6 +647,11 @@ def main():
         line["prefix_cached_prefill"] = run_prefix_cached(wl, max(1, min(K, 3)), 2, idx_ms + attn_ms)
     except Exception as ex:  # report, never fake
         line["prefix_cached_prefill"] = {"ms": None, "error": str(ex)[:200]}
+    if rank == 0 and not args.no_token_level:
+        try:
+            line["token_level_indexer"] = run_token_level(wl, idx_ms)
+        except Exception as ex:
+            line["token_level_indexer"] = {"error": str(ex)[:200]}
     if rank == 0 and not args.no_dense:
         try:
             line["dense_comparison"] = run_dense_comparison(wl, idx_ms + attn_ms, dec_ms)

@@ -80,6 +80,7 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 struct Params {
     int64_t L;          // end position: queries are tokens q_off .. L-1
     int64_t q_off;      // position of the first query row (a cached prefix before it)
+    int bshift;         // log2 of the tokens per selection unit: 2 (4-token blocks) or 0 (tokens)
     int nq;
     int k_sel;          // budget - 1
     int budget;
@@ -155,7 +156,7 @@ __device__ __forceinline__ void group_bar(int id) {
 __device__ __forceinline__ int num_btiles(const Params &p, int q) {
     int64_t t_last = p.q_off + static_cast<int64_t>(q) * TQ + TQ - 1;
     if (t_last > p.L - 1) t_last = p.L - 1;
-    const int64_t cmax = t_last / kBlock;  // blocks 0..cmax-1 are scored
+    const int64_t cmax = t_last >> p.bshift;  // units 0..cmax-1 are scored
     return static_cast<int>((cmax + TB - 1) / TB);
 }
 
@@ -561,7 +562,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (group_sync_fail(bar, false)) { ok = false; break; }
             const bool tile_all_in = (t0 + TQ <= p.L);
-            const int64_t c_min = t0 / kBlock;
+            const int64_t c_min = t0 >> p.bshift;
             for (int j = 0; j < nbt; ++j) {
                 const uint32_t buf = acc & 1;
                 const uint32_t use = acc >> 1;
@@ -609,7 +610,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int tk = 0; tk < 4; ++tk) {
                                 const int64_t t = t0 + tl0 + tk;
-                                const bool valid = !MASKED || ((t < p.L) && (b < (t >> 2)));
+                                const bool valid = !MASKED || ((t < p.L) && (b < (t >> p.bshift)));
                                 if (valid) p.dense[t * p.dense_ld + b] = sv[tk];
                             }
                         } else {
@@ -621,7 +622,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                             for (int tk = 0; tk < 4; ++tk) {
                                 const int64_t t = t0 + tl0 + tk;
-                                const bool valid = !MASKED || ((t < p.L) && (b < (t >> 2)));
+                                const bool valid = !MASKED || ((t < p.L) && (b < (t >> p.bshift)));
                                 pass[tk] = valid && (sv[tk] >= thv[tk]);
                                 m[tk] = __ballot_sync(0xFFFFFFFFu, pass[tk]);
                             }
@@ -707,7 +708,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int tl = g * GTOK + t16;
                     const int64_t t = t0 + tl;
                     if (t >= p.L) break;
-                    const int64_t c = t / kBlock;
+                    const int64_t c = t >> p.bshift;
                     int n[4];
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) n[qq] = min(sCnt[qq * TQ + tl], SUB);
@@ -801,13 +802,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // Budget 1: only the current block, no scoring at all.
-__global__ void fill_current_kernel(int64_t q_off, int64_t Lq, int budget, int32_t *idx, float *score) {
+__global__ void fill_current_kernel(int64_t q_off, int64_t Lq, int bshift, int budget, int32_t *idx, float *score) {
     const int64_t total = Lq * budget;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t tl = i / budget;
         const int r = static_cast<int>(i - tl * budget);
-        idx[i] = r == 0 ? static_cast<int32_t>((q_off + tl) / kBlock) : -1;
+        idx[i] = r == 0 ? static_cast<int32_t>((q_off + tl) >> bshift) : -1;
         if (score) score[i] = r == 0 ? INFINITY : -INFINITY;
     }
 }
@@ -824,13 +825,14 @@ size_t index_cand_bytes(int64_t L, int sms) {
 }
 
 cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t q_off, int64_t Lq,
-                         int budget, const uint16_t *w, int32_t *idx, float *score,
+                         int unit_tokens, int budget, const uint16_t *w, int32_t *idx, float *score,
                          float *dense, void *cand_ws, int32_t *status, int sms,
                          cudaStream_t stream) {
     ix::Params p;
     const int64_t L = q_off + Lq;
     p.L = L;
     p.q_off = q_off;
+    p.bshift = unit_tokens == 1 ? 0 : 2;
     p.nq = static_cast<int>((Lq + ix::TQ - 1) / ix::TQ);
     p.k_sel = budget - 1;
     p.budget = budget;
@@ -857,11 +859,12 @@ cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int
     return cudaGetLastError();
 }
 
-cudaError_t launch_fill_current_only(int64_t q_off, int64_t Lq, int budget, int32_t *idx, float *score,
-                                     cudaStream_t stream) {
+cudaError_t launch_fill_current_only(int64_t q_off, int64_t Lq, int unit_tokens, int budget, int32_t *idx,
+                                     float *score, cudaStream_t stream) {
     int64_t blocks = (Lq * budget + 255) / 256;
     if (blocks > 4096) blocks = 4096;
-    ix::fill_current_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(q_off, Lq, budget, idx, score);
+    ix::fill_current_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(q_off, Lq, unit_tokens == 1 ? 0 : 2,
+                                                                           budget, idx, score);
     return cudaGetLastError();
 }
 

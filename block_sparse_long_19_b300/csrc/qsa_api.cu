@@ -273,7 +273,7 @@ static qsa_status index_common(const qsa_config *cfg, const qsa_bf16 *qi, const 
     cudaError_t e = qsa::launch_kprep(1, 0, L, L, ki, k, k_rot, kblk, freqs_of(cfg), sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "kprep launch");
     if (!dense && cfg->budget_blocks == 1) {
-        e = qsa::launch_fill_current_only(0, L, 1, idx, score, s);
+        e = qsa::launch_fill_current_only(0, L, qsa::kBlock, 1, idx, score, s);
         if (e != cudaSuccess) return cuda_fail(e, "selection launch");
         return ok();
     }
@@ -283,7 +283,7 @@ static qsa_status index_common(const qsa_config *cfg, const qsa_bf16 *qi, const 
     const int64_t nbk = L / qsa::kBlock;
     st = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
     if (st != QSA_OK) return st;
-    e = qsa::launch_index(map_q, map_k, 0, L, cfg->budget_blocks, w, idx, score, dense, cand,
+    e = qsa::launch_index(map_q, map_k, 0, L, qsa::kBlock, cfg->budget_blocks, w, idx, score, dense, cand,
                           dev_status, sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     return ok();
@@ -373,6 +373,45 @@ size_t qsa_index_topk_cached_workspace_bytes(const qsa_config *cfg, int64_t Lq) 
     return align_up(qsa::index_cand_bytes(Lq, sm_count()), 256);
 }
 
+size_t qsa_index_topk_tokens_workspace_bytes(const qsa_config *cfg, int64_t L) {
+    return qsa_index_topk_cached_workspace_bytes(cfg, L);
+}
+
+qsa_status qsa_index_topk_tokens(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                                 const qsa_bf16 *ki, int64_t L, int32_t *idx, float *score, void *ws,
+                                 size_t ws_bytes, int32_t *dev_status, void *stream) {
+    qsa_status st = check_cfg(cfg);
+    if (st != QSA_OK) return st;
+    if (L < 1) return fail(QSA_ERR_INVALID_ARG, "L must be >= 1");
+    if (L > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "L > %lld", static_cast<long long>(kMaxL));
+    REQ_PTR(qi);
+    REQ_PTR(w);
+    REQ_PTR(ki);
+    REQ_PTR(idx);
+    OPT_PTR(score);
+    REQ_PTR(dev_status);
+    const size_t need = qsa_index_topk_tokens_workspace_bytes(cfg, L);
+    if (!ws || ws_bytes < need)
+        return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (cfg->budget_blocks == 1) {
+        e = qsa::launch_fill_current_only(0, L, 1, 1, idx, score, s);
+        if (e != cudaSuccess) return cuda_fail(e, "selection launch");
+        return ok();
+    }
+    CUtensorMap map_q, map_k;
+    st = make_map(&map_q, qi, qsa::kDI, static_cast<uint64_t>(L) * qsa::kHI, 256);
+    if (st != QSA_OK) return st;
+    st = make_map(&map_k, ki, qsa::kDI, static_cast<uint64_t>(L), 128);  // every token is a unit
+    if (st != QSA_OK) return st;
+    e = qsa::launch_index(map_q, map_k, 0, L, 1, cfg->budget_blocks, w, idx, score, nullptr, ws, dev_status,
+                          sm_count(), s);
+    if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+    return ok();
+}
+
 qsa_status qsa_index_topk_cached(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
                                  const qsa_bf16 *kblk, int64_t q_offset, int64_t Lq, int32_t *idx,
                                  float *score, void *ws, size_t ws_bytes, int32_t *dev_status,
@@ -396,7 +435,7 @@ qsa_status qsa_index_topk_cached(const qsa_config *cfg, const qsa_bf16 *qi, cons
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (cfg->budget_blocks == 1) {
-        e = qsa::launch_fill_current_only(q_offset, Lq, 1, idx, score, s);
+        e = qsa::launch_fill_current_only(q_offset, Lq, qsa::kBlock, 1, idx, score, s);
         if (e != cudaSuccess) return cuda_fail(e, "selection launch");
         return ok();
     }
@@ -406,8 +445,8 @@ qsa_status qsa_index_topk_cached(const qsa_config *cfg, const qsa_bf16 *qi, cons
     const int64_t nbk = (q_offset + Lq) / qsa::kBlock;
     st = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
     if (st != QSA_OK) return st;
-    e = qsa::launch_index(map_q, map_k, q_offset, Lq, cfg->budget_blocks, w, idx, score, nullptr, ws,
-                          dev_status, sm_count(), s);
+    e = qsa::launch_index(map_q, map_k, q_offset, Lq, qsa::kBlock, cfg->budget_blocks, w, idx, score, nullptr,
+                          ws, dev_status, sm_count(), s);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     return ok();
 }

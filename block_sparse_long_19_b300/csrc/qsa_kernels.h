@@ -25,13 +25,14 @@ cudaError_t launch_kprep(int batch, int64_t t_begin, int64_t L, int64_t max_ctx,
 int index_grid(int64_t L, int sms);
 size_t index_cand_bytes(int64_t L, int sms);
 // Queries are tokens q_off .. q_off+Lq-1 (qi, w, idx, score hold their Lq
-// rows); block keys cover every complete block before q_off+Lq.
+// rows); the keys (map_k) cover every complete selection unit before
+// q_off+Lq.  unit_tokens: 4 (micro-blocks) or 1 (a token-level indexer).
 cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t q_off, int64_t Lq,
-                         int budget, const uint16_t *w, int32_t *idx, float *score,
+                         int unit_tokens, int budget, const uint16_t *w, int32_t *idx, float *score,
                          float *dense, void *cand_ws, int32_t *status, int sms,
                          cudaStream_t stream);
-cudaError_t launch_fill_current_only(int64_t q_off, int64_t Lq, int budget, int32_t *idx, float *score,
-                                     cudaStream_t stream);
+cudaError_t launch_fill_current_only(int64_t q_off, int64_t Lq, int unit_tokens, int budget, int32_t *idx,
+                                     float *score, cudaStream_t stream);
 
 // ---- block-sparse attention (prefill and decode splits) ----
 struct AttnArgs {

@@ -31,7 +31,8 @@ EXPORTED = [
     "qsa_index_topk_workspace_bytes", "qsa_index_topk", "qsa_index_scores",
     "qsa_sparse_attn_prefill", "qsa_decode_workspace_bytes", "qsa_sparse_attn_decode",
     "qsa_sparse_attn_decode_noalloc", "qsa_kprep_range", "qsa_index_topk_cached_workspace_bytes",
-    "qsa_index_topk_cached", "qsa_sparse_attn_prefill_cached",
+    "qsa_index_topk_cached", "qsa_sparse_attn_prefill_cached", "qsa_index_topk_tokens_workspace_bytes",
+    "qsa_index_topk_tokens",
 ]
 
 
@@ -100,6 +101,10 @@ def load(path: str = LIB_PATH):
     L.qsa_index_topk_cached.restype = c.c_int
     L.qsa_sparse_attn_prefill_cached.argtypes = [cfgp, P, P, P, P, c.c_int64, c.c_int64, P, P, P, P]
     L.qsa_sparse_attn_prefill_cached.restype = c.c_int
+    L.qsa_index_topk_tokens_workspace_bytes.argtypes = [cfgp, c.c_int64]
+    L.qsa_index_topk_tokens_workspace_bytes.restype = c.c_size_t
+    L.qsa_index_topk_tokens.argtypes = [cfgp, P, P, P, c.c_int64, P, P, P, c.c_size_t, P, P]
+    L.qsa_index_topk_tokens.restype = c.c_int
     _lib = L
     return L
 
@@ -311,6 +316,31 @@ def sparse_attn_prefill_cached(cfg: Config, q, k_rot, v, idx, q_offset: int, out
                                                  q_offset, Lq, _ptr(out), _ptr(lse), _ptr(status),
                                                  _stream(stream)), "qsa_sparse_attn_prefill_cached")
     return out, lse, status
+
+
+def index_topk_tokens(cfg: Config, qi, w, ki, idx=None, score=None, ws=None, status=None,
+                      want_score: bool = True, stream=None):
+    """Token-level indexer (one token per selection unit; cfg.budget_blocks
+    counts tokens).  Returns (idx, score, status)."""
+    L = qi.shape[0]
+    dev = qi.device
+    _need(qi, "qi", torch.bfloat16, (L, 4, 128))
+    _need(w, "w", torch.bfloat16, (L, 4))
+    _need(ki, "ki", torch.bfloat16, (L, 128))
+    B = cfg.budget_blocks
+    if idx is None:
+        idx = torch.empty((L, B), dtype=torch.int32, device=dev)
+    if score is None and want_score:
+        score = torch.empty((L, B), dtype=torch.float32, device=dev)
+    need = load().qsa_index_topk_tokens_workspace_bytes(ctypes.byref(cfg), L)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_index_topk_tokens(ctypes.byref(cfg), _ptr(qi), _ptr(w), _ptr(ki), L, _ptr(idx), _ptr(score),
+                                        _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+           "qsa_index_topk_tokens")
+    return idx, score, status
 
 
 def decode_workspace_bytes(cfg: Config, batch: int, max_ctx: int) -> int:

@@ -176,6 +176,23 @@ qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
                                    void *stream);
 
 /* ------------------------------------------------------------------------
+ * Token-level indexer (the DSA-style variant the launch post contrasts QSA
+ * with, "Attention: GDN + QSA": a token-level indexer scores every past
+ * position, so its cost grows 4x against 4-token micro-blocks).  The same
+ * kernel as qsa_index_topk with one token per selection unit: the unit keys
+ * are the indexer keys themselves (no mean), query t sees units 0..t-1 and
+ * always keeps its own token t.
+ *   qi [L, 4, 128], w [L, 4], ki [L, 128]; idx [L, budget] int32 out: the
+ *   selected past tokens ascending, then t, then -1 padding (budget counts
+ *   tokens here, 1..512); score [L, budget] or NULL as for qsa_index_topk.
+ *   ws: at least qsa_index_topk_tokens_workspace_bytes(cfg, L) bytes.
+ * ---------------------------------------------------------------------- */
+size_t qsa_index_topk_tokens_workspace_bytes(const qsa_config *cfg, int64_t L);
+qsa_status qsa_index_topk_tokens(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                                 const qsa_bf16 *ki, int64_t L, int32_t *idx, float *score, void *ws,
+                                 size_t ws_bytes, int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
  * Prefill of a new chunk after a cached prefix (prefix-cache serving: the
  * launch post, "Model Architecture / Attention: GDN + QSA for Efficient
  * Memory and Precise Retrieval", measures prefill at a 90% prefix-cache hit
