@@ -482,7 +482,9 @@ DecodePlan decode_plan(int batch, int64_t max_ctx, int sms) {
     }
     pl.chunk = ch;
     pl.nchunk = static_cast<int>(nchunk < 1 ? 1 : nchunk);
-    int nsplit = (2 * sms + batch - 1) / batch;
+    // attention splits: one wave of CTAs (one per SM: the kernel holds 216 KB
+    // of shared memory), as many splits per sequence as fit, at most 16
+    int nsplit = sms / batch;
     if (nsplit > 16) nsplit = 16;
     if (nsplit < 1) nsplit = 1;
     pl.nsplit = nsplit;
