@@ -360,46 +360,68 @@ def run_token_level(wl: Workload, block_indexer_ms: float, reps: int = 2) -> dic
 # ----------------------------------------------------------------- e2e --
 
 def run_e2e(wl: Workload, steps: int) -> dict:
-    """Step through the public API from pinned host buffers: H2D of every
-    prefill input and of the decode query inputs, compute, D2H of both
-    attention outputs; all inside the timed region."""
+    """A step through the public API from pinned host buffers: every prefill
+    input copied in and the attention output (and LSE) copied back by
+    qsa.HostPrefill (chunked, the copies of one chunk overlapping the compute
+    of the next), then the decode step with its queries copied in and its
+    output copied back; all inside the timed region."""
     p, d = wl.p, wl.d
-    names = ["q", "k", "v", "qi", "w", "ki"]
+    names = Q.HostPrefill.NAMES
     host = {n: torch.empty(p[n].shape, dtype=p[n].dtype, pin_memory=True) for n in names}
     for n in names:
         host[n].copy_(p[n])
-        host[n] = host[n]
     dn = ["q", "qi", "w", "seq_lens"]
     dhost = {n: torch.empty(d[n].shape, dtype=d[n].dtype, pin_memory=True) for n in dn}
     for n in dn:
         dhost[n].copy_(d[n])
     out_h = torch.empty(wl.out.shape, dtype=wl.out.dtype, pin_memory=True)
+    lse_h = torch.empty(wl.lse.shape, dtype=wl.lse.dtype, pin_memory=True)
     dout_h = torch.empty(wl.dout.shape, dtype=wl.dout.dtype, pin_memory=True)
     h2d = sum(host[n].numel() * host[n].element_size() for n in names) + \
         sum(dhost[n].numel() * dhost[n].element_size() for n in dn)
-    d2h = out_h.numel() * out_h.element_size() + dout_h.numel() * dout_h.element_size()
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size() + \
+        dout_h.numel() * dout_h.element_size()
+    # the device buffers of the chunked prefill take the place of the
+    # workload's prefill tensors while this runs
+    saved = {n: p[n] for n in names}
+    for n in names:
+        p[n] = None
+    torch.cuda.empty_cache()
+    hp = Q.HostPrefill(wl.cfg, wl.L, device=wl.dev)
 
     def one():
-        for n in names:
-            p[n].copy_(host[n], non_blocking=True)
+        hp.run(host, out_h, lse_h)
         for n in dn:
             d[n].copy_(dhost[n], non_blocking=True)
-        wl.step()
-        out_h.copy_(wl.out, non_blocking=True)
+        Q.sparse_attn_decode(wl.cfg, d["q"], d["qi"], d["w"], d["k"], d["v"], wl.kblk_cache, d["seq_lens"],
+                             out=wl.dout, lse=wl.dlse, idx_out=None, ws=wl.ws_dec, status=wl.status,
+                             want_idx=False)
         dout_h.copy_(wl.dout, non_blocking=True)
 
-    one()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(steps):
+    try:
         one()
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / steps
-    del host, dhost, out_h, dout_h
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(steps):
+            one()
+        e1.record()
+        torch.cuda.synchronize()
+        Q.check_status(hp.status, "host prefill")
+        Q.check_status(wl.status, "host decode")
+        ms = e0.elapsed_time(e1) / steps
+        # the outputs that came back are the device path's (spot check)
+        ok = bool(torch.equal(out_h[-4:].to(wl.dev), wl.out[-4:]))
+    finally:
+        del hp
+        for n in names:
+            p[n] = saved[n]
+        torch.cuda.empty_cache()
+    del host, dhost, out_h, lse_h, dout_h
     return {"value": (wl.L + wl.B) / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "prefill": "qsa.HostPrefill, 65,536-token chunks, copies overlapped with compute",
+            "output_spot_check": ok}
 
 
 # ---------------------------------------------------------- CPU baseline --

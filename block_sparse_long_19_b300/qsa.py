@@ -425,3 +425,71 @@ def prefill(cfg: Config, q, k, v, qi, w, ki, want_score: bool = False, want_lse:
     out, lse, _ = sparse_attn_prefill(cfg, q, k_rot, v, idx, status=status, want_lse=want_lse,
                                       stream=stream)
     return PrefillResult(idx, score, k_rot, out, lse, status)
+
+
+class HostPrefill:
+    """Prefill of one sequence whose inputs live in pinned host memory.
+
+    The sequence is processed in chunks of query rows with the cached-prefix
+    calls (each chunk's rows against every earlier token), so the host->device
+    copies of chunk c+1 and the device->host copy of chunk c-1's output run on
+    their own streams while chunk c computes.  The results equal those of
+    prefill() on the whole sequence (the per-query computation does not depend
+    on the chunking).  Device buffers are allocated once, here."""
+
+    NAMES = ("q", "k", "v", "qi", "w", "ki")
+
+    def __init__(self, cfg: Config, L: int, chunk_tokens: int = 65536, device="cuda"):
+        self.cfg, self.L, self.dev = cfg, L, device
+        self.chunk = max(64, (chunk_tokens // 64) * 64)
+        shapes = {"q": (L, 24, 256), "k": (L, 2, 256), "v": (L, 2, 256), "qi": (L, 4, 128), "w": (L, 4),
+                  "ki": (L, 128)}
+        self.dev_in = {n: torch.empty(shapes[n], dtype=torch.bfloat16, device=device) for n in self.NAMES}
+        self.k_rot = torch.empty((L, 2, 256), dtype=torch.bfloat16, device=device)
+        self.kblk = torch.zeros((max(L // 4, 1), 128), dtype=torch.bfloat16, device=device)
+        self.idx = torch.empty((L, cfg.budget_blocks), dtype=torch.int32, device=device)
+        self.out = torch.empty((L, 24, 256), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((L, 24), dtype=torch.float32, device=device)
+        self.status = new_status(device)
+        need = load().qsa_index_topk_cached_workspace_bytes(ctypes.byref(cfg), min(self.chunk, L))
+        self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
+        self.h2d = torch.cuda.Stream(device=device)
+        self.d2h = torch.cuda.Stream(device=device)
+        self.bounds = list(range(0, L, self.chunk)) + [L]
+
+    def run(self, host: dict, out_host: torch.Tensor, lse_host: torch.Tensor | None = None):
+        """host: pinned CPU tensors q, k, v, qi, w, ki of the whole sequence;
+        out_host [L, 24, 256] (and lse_host [L, 24]) receive the outputs.
+        Enqueues everything; the caller's current stream waits for the last
+        copy back."""
+        cfg, comp = self.cfg, torch.cuda.current_stream(self.dev)
+        start = torch.cuda.Event()
+        start.record(comp)
+        self.h2d.wait_event(start)
+        self.d2h.wait_event(start)
+        ins, outs = [], []
+        for a, b in zip(self.bounds[:-1], self.bounds[1:]):
+            ev = torch.cuda.Event()
+            with torch.cuda.stream(self.h2d):
+                for n in self.NAMES:
+                    self.dev_in[n][a:b].copy_(host[n][a:b], non_blocking=True)
+                ev.record(self.h2d)
+            ins.append(ev)
+        for (a, b), ev in zip(zip(self.bounds[:-1], self.bounds[1:]), ins):
+            comp.wait_event(ev)
+            d = self.dev_in
+            kprep_range(cfg, d["ki"][:b], self.kblk, a, b, k=d["k"][:b], k_rot=self.k_rot[:b])
+            index_topk_cached(cfg, d["qi"][a:b], d["w"][a:b], self.kblk[: max(b // 4, 1)], a, idx=self.idx[a:b],
+                              score=None, ws=self.ws, status=self.status, want_score=False)
+            sparse_attn_prefill_cached(cfg, d["q"][a:b], self.k_rot[:b], d["v"][:b], self.idx[a:b], a,
+                                       out=self.out[a:b], lse=self.lse[a:b], status=self.status)
+            done = torch.cuda.Event()
+            done.record(comp)
+            self.d2h.wait_event(done)
+            with torch.cuda.stream(self.d2h):
+                out_host[a:b].copy_(self.out[a:b], non_blocking=True)
+                if lse_host is not None:
+                    lse_host[a:b].copy_(self.lse[a:b], non_blocking=True)
+            outs.append(done)
+        comp.wait_stream(self.d2h)
+        return self.status

@@ -128,3 +128,22 @@ def test_prefix90_at_128k():
     check_selection(idx_g, ref["idx"], scores, rows, budget)
     att = O.prefill_rows(hb, rows, budget, idx_given=idx_g)
     check_outputs(bf16_to_f64(out[torch.as_tensor(loc, device=DEV)]), att["o"], "O")
+
+
+def test_host_prefill_pipeline_equals_device_prefill():
+    """qsa.HostPrefill (inputs in pinned host memory, chunked, copies on their
+    own streams) returns exactly the device prefill's output and LSE."""
+    L, budget = 9001, 512
+    t = W.prefill_inputs(L, 44, DEV)
+    full = full_prefill(t, budget)
+    cfg = Q.default_config(budget=budget)
+    host = {n: t[n].cpu().pin_memory() for n in Q.HostPrefill.NAMES}
+    out_h = torch.empty((L, 24, 256), dtype=torch.bfloat16).pin_memory()
+    lse_h = torch.empty((L, 24), dtype=torch.float32).pin_memory()
+    hp = Q.HostPrefill(cfg, L, chunk_tokens=2048)
+    st = hp.run(host, out_h, lse_h)
+    torch.cuda.synchronize()
+    Q.check_status(st)
+    assert torch.equal(out_h, full.out.cpu())
+    assert torch.equal(lse_h, full.lse.cpu())
+    assert torch.equal(hp.idx, full.idx)
