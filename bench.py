@@ -220,6 +220,33 @@ class Workload:
         return self.B * (c * 256 + keys * 2048 + 2 * 24 * 256 * 2)
 
 
+# ------------------------------------------------------ decode stream --
+
+def run_decode_stream(wl: Workload, steps: int = 20) -> dict:
+    """Decode steps back to back, as a serving loop runs them (each step
+    still one full indexer scan + selection + attention per sequence): the
+    device time per step once the pipeline is full."""
+    cfg, d = wl.cfg, wl.d
+
+    def one():
+        Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], d["k"], d["v"], wl.kblk_cache, d["seq_lens"],
+                             out=wl.dout, lse=wl.dlse, idx_out=None, ws=wl.ws_dec, status=wl.status,
+                             want_idx=False)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    Q.check_status(wl.status, "decode stream")
+    us = e0.elapsed_time(e1) * 1e3 / steps
+    return {"steps": steps, "us_per_step": us, "gb_per_s": wl.decode_bytes() / (us / 1e6) / 1e9}
+
+
 # ------------------------------------------------------- prefix cache --
 
 def run_prefix_cached(wl: Workload, reps: int, warmup: int, full_prefill_ms: float) -> dict:
@@ -665,6 +692,10 @@ def main():
         "gpu_launches": wl.launches_per_step() * K,
         "clocks": clk,
     }
+    try:
+        line["decode_back_to_back"] = run_decode_stream(wl)
+    except Exception as ex:
+        line["decode_back_to_back"] = {"us_per_step": None, "error": str(ex)[:200]}
     try:
         line["prefix_cached_prefill"] = run_prefix_cached(wl, max(1, min(K, 3)), 2, idx_ms + attn_ms)
     except Exception as ex:  # report, never fake
