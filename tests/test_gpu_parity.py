@@ -329,3 +329,42 @@ def test_locality_workload_selects_own_topic_and_matches_oracle():
         blocks = idx[r][idx[r] >= 0][:-1]
         own.append(np.mean((blocks * 4) // seg == r // seg))
     assert own and np.mean(own) > 0.45
+
+
+def test_decode_step_replays_as_cuda_graph():
+    """The decode step (scan, filter, merge, split attention, combine, with
+    programmatic dependent launches) captures into a CUDA graph; replays give
+    the eager result bit for bit, with new queries written into the captured
+    input buffers between replays."""
+    B, Tmax, budget = 4, 16384, 512
+    d = W.decode_inputs(B, Tmax, 81, DEV, seq_lens=[Tmax, 9000, 4097, 600])
+    cfg = Q.default_config(budget=budget)
+    kblk, _ = Q.kprep(cfg, d["ki"], d["k"], k_rot=d["k"])
+    ws = torch.empty(Q.decode_workspace_bytes(cfg, B, Tmax), dtype=torch.uint8, device=DEV)
+    out = torch.empty((B, 24, 256), dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty((B, 24), dtype=torch.float32, device=DEV)
+    idx = torch.empty((B, budget), dtype=torch.int32, device=DEV)
+    status = Q.new_status(DEV)
+
+    def step():
+        Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], d["k"], d["v"], kblk, d["seq_lens"], out=out, lse=lse,
+                             idx_out=idx, ws=ws, status=status)
+
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    gen = torch.Generator(device=DEV).manual_seed(82)
+    for _ in range(2):
+        d["q"].copy_(torch.randn(d["q"].shape, generator=gen, device=DEV).to(torch.bfloat16))
+        d["qi"].copy_(torch.randn(d["qi"].shape, generator=gen, device=DEV).to(torch.bfloat16))
+        g.replay()
+        torch.cuda.synchronize()
+        got = (out.clone(), lse.clone(), idx.clone())
+        step()
+        torch.cuda.synchronize()
+        Q.check_status(status)
+        assert torch.equal(got[2], idx)
+        assert torch.equal(got[0], out)
+        assert torch.equal(got[1], lse)
