@@ -49,6 +49,7 @@ WORKLOADS = {
     # NEXT-row workload: topic segments of 8192 tokens (neighbouring queries
     # select overlapping blocks), same sizes as qsa_1m
     "qsa_1m_local": (1 << 20, 512, 4, 8, 1 << 20, 4, 8192),
+    "prof_128k_local": (131072, 512, 2, 1, 65536, 3, 8192),
     "prof_decode": (4096, 512, 6, 8, 131072, 6),
 }
 
