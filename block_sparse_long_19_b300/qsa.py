@@ -20,6 +20,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqsa.so")
 
 QSA_OK = 0
+QSA_ERR_TIMEOUT = 5
 STATUS_NAMES = {
     0: "QSA_OK", 1: "QSA_ERR_INVALID_ARG", 2: "QSA_ERR_UNSUPPORTED", 3: "QSA_ERR_WORKSPACE",
     4: "QSA_ERR_CUDA", 5: "QSA_ERR_TIMEOUT", 6: "QSA_ERR_DEVICE_CHECK",
@@ -32,7 +33,7 @@ EXPORTED = [
     "qsa_sparse_attn_prefill", "qsa_decode_workspace_bytes", "qsa_sparse_attn_decode",
     "qsa_sparse_attn_decode_noalloc", "qsa_kprep_range", "qsa_index_topk_cached_workspace_bytes",
     "qsa_index_topk_cached", "qsa_sparse_attn_prefill_cached", "qsa_index_topk_tokens_workspace_bytes",
-    "qsa_index_topk_tokens",
+    "qsa_index_topk_tokens", "qsa_selftest_bounded_wait",
 ]
 
 
@@ -105,6 +106,8 @@ def load(path: str = LIB_PATH):
     L.qsa_index_topk_tokens_workspace_bytes.restype = c.c_size_t
     L.qsa_index_topk_tokens.argtypes = [cfgp, P, P, P, c.c_int64, P, P, P, c.c_size_t, P, P]
     L.qsa_index_topk_tokens.restype = c.c_int
+    L.qsa_selftest_bounded_wait.argtypes = [c.c_int64, c.c_int, P, P]
+    L.qsa_selftest_bounded_wait.restype = c.c_int
     _lib = L
     return L
 
@@ -341,6 +344,16 @@ def index_topk_tokens(cfg: Config, qi, w, ki, idx=None, score=None, ws=None, sta
                                         _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
            "qsa_index_topk_tokens")
     return idx, score, status
+
+
+def selftest_bounded_wait(limit_ns: int, complete: bool, status=None, stream=None):
+    """Run the bounded-wait self-test kernel; returns the status tensor (its
+    value is QSA_ERR_TIMEOUT after the wait ran out)."""
+    if status is None:
+        status = new_status("cuda")
+    _check(load().qsa_selftest_bounded_wait(int(limit_ns), 1 if complete else 0, _ptr(status), _stream(stream)),
+           "qsa_selftest_bounded_wait")
+    return status
 
 
 def decode_workspace_bytes(cfg: Config, batch: int, max_ctx: int) -> int:

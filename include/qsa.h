@@ -285,6 +285,17 @@ qsa_status qsa_sparse_attn_decode_noalloc(const qsa_config *cfg, int batch, cons
                                           const int32_t *seq_lens, qsa_bf16 *out, float *lse,
                                           int32_t *idx_out, int32_t *dev_status, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Self-test of the failure path: one kernel waits, with the library's bounded
+ * mbarrier wait, on a phase that completes only if `complete` is nonzero.
+ * With complete = 0 the wait runs out after limit_ns (1 ns .. 0.1 s) and the
+ * kernel writes QSA_ERR_TIMEOUT to *dev_status and returns; with complete = 1
+ * it leaves *dev_status untouched.  Every kernel of the library reports a
+ * wait that ran out this way (their limit is 2 s).  Returns QSA_ERR_INVALID_ARG
+ * for a NULL status or a limit out of range.  The pages have no counterpart.
+ * ---------------------------------------------------------------------- */
+qsa_status qsa_selftest_bounded_wait(int64_t limit_ns, int complete, int32_t *dev_status, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -167,3 +167,9 @@ def test_yarn_config_checked(lib):
     cfg = Q.default_config(yarn_factor=4.0)
     cfg.yarn_original_max_pos = 0
     assert f(ctypes.byref(cfg), A, A, A, A, 16, A, None, A, None) == 1
+
+
+def test_selftest_rejects(lib):
+    assert lib.qsa_selftest_bounded_wait(1000, 0, None, None) == 1
+    assert lib.qsa_selftest_bounded_wait(0, 0, A, None) == 1
+    assert lib.qsa_selftest_bounded_wait(200_000_000, 0, A, None) == 1
