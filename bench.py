@@ -154,8 +154,29 @@ class Workload:
         self.kblk_pre = None  # block keys of the whole sequence (prefix-cache measurement)
 
     def step(self, events=None):
-        """One pass of the hot path.  events: optional list of 5 CUDA events
-        recorded at: start, after indexer, after attention, after decode."""
+        """One pass of the hot path as a user runs it: the whole prefill
+        through qsa_prefill_overlapped (K-prep, then the indexer of each chunk
+        of query rows beside the attention of the previous chunk), then the
+        decode step.  events: optional list of 3 CUDA events recorded at:
+        start, after the prefill, after the decode step."""
+        cfg, p, d = self.cfg, self.p, self.d
+        if events:
+            events[0].record()
+        Q.prefill_overlapped(cfg, p["q"], p["k"], p["v"], p["qi"], p["w"], p["ki"], k_rot=self.k_rot, idx=self.idx,
+                             out=self.out, lse=self.lse, ws=self.ws_pre, status=self.status)
+        if events:
+            events[1].record()
+        Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], d["k"], d["v"], self.kblk_cache,
+                             d["seq_lens"], out=self.dout, lse=self.dlse, idx_out=None,
+                             ws=self.ws_dec, status=self.status, want_idx=False)
+        if events:
+            events[2].record()
+
+    def stage_step(self, events=None):
+        """The same pass with the stages one after the other, each on every
+        SM, for the per-stage times and each kernel's roofline.  events:
+        optional list of 4 CUDA events recorded at: start, after indexer,
+        after attention, after decode."""
         cfg, p, d = self.cfg, self.p, self.d
         if events:
             events[0].record()
@@ -192,9 +213,14 @@ class Workload:
         if events:
             events[2].record()
 
+    def overlap_plan(self):
+        sms = torch.cuda.get_device_properties(self.dev).multi_processor_count
+        return Q.prefill_overlap_plan(self.cfg, self.L, sms)
+
     def launches_per_step(self) -> int:
-        n = 2 + 1 + 1      # kprep blocks + kprep rope, indexer, prefill attention
-        n += 3 + 1 + 1     # decode scan, filter, merge; split attention; combine
+        chunks = len(self.overlap_plan()[1])
+        n = 2 + 2 * chunks  # kprep blocks + kprep rope, an indexer and an attention launch per chunk
+        n += 3 + 1 + 1      # decode scan, filter, merge; split attention; combine
         return n
 
     def attn_bytes(self) -> int:
@@ -212,6 +238,14 @@ class Workload:
         """Algorithmic flops of the indexer: 2 * 4 heads * 128 per (query, past block)."""
         t = np.arange(self.L, dtype=np.int64)
         return float((t // 4).sum() * 1024)
+
+    def attn_flops(self) -> float:
+        """Algorithmic flops of the prefill attention: 24 heads x (QK^T + PV)
+        x 2 x 256 per (query, attended key)."""
+        L, B = self.L, self.budget
+        t = np.arange(L, dtype=np.int64)
+        keys = np.minimum(t // 4, B - 1) * 4 + (t % 4) + 1
+        return float(keys.sum() * 24 * 1024)
 
     def decode_bytes(self) -> int:
         """Algorithmic bytes of one decode step: the block-key scan
@@ -585,6 +619,29 @@ def attn_traffic(wl) -> int | None:
     return int(pj["dram_bytes_read"] + pj["dram_bytes_write"])
 
 
+# ------------------------------------------------------ prefill bound --
+
+def prefill_bound(wl, pre_ms: float, tc_tflops: float, hbm_gbs: float) -> dict:
+    """Whole-prefill time against its binding roofline.  The indexer is a
+    dense contraction (tensor-bound); the attention gathers 2 KiB per key at
+    12 flop/B, far below the tensor ridge (HBM-bound).  With perfect overlap
+    of the two the bound is max(flops / P_tc, bytes / BW); run one after the
+    other it is their sum.  `tensor_frac` is all prefill flops over the
+    measured time and the tensor peak: it stays far below 0.5 because the
+    attention's bytes, not its flops, set its time."""
+    f_idx, f_attn = wl.index_flops(), wl.attn_flops()
+    t_idx = f_idx / (tc_tflops * 1e12) * 1e3
+    t_attn_bw = wl.attn_bytes() / (hbm_gbs * 1e9) * 1e3
+    t_attn_tc = f_attn / (tc_tflops * 1e12) * 1e3
+    meas = pre_ms
+    overlap = max(t_idx + t_attn_tc, t_attn_bw)
+    serial = t_idx + t_attn_bw
+    return {"measured_ms": meas, "bound_overlapped_ms": overlap, "frac_overlapped": overlap / meas,
+            "bound_serial_ms": serial, "frac_serial": serial / meas,
+            "flops": f_idx + f_attn, "tensor_frac": (f_idx + f_attn) / (meas / 1e3) / (tc_tflops * 1e12),
+            "attn_tensor_frac_at_hbm_bound": t_attn_tc / t_attn_bw}
+
+
 # ------------------------------------------------------------- ranks --
 
 def job_time_ms(ms: float, pg=None) -> float:
@@ -647,7 +704,7 @@ def main():
     Q.check_status(wl.status, "warm-up")
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     if pg:
@@ -660,15 +717,28 @@ def main():
         wl.step(evs[i])
     e_end.record()
     torch.cuda.synchronize()
-    clk = clocks.stop()
     if pg:
         pg.barrier()
     Q.check_status(wl.status, "timed steps")
     ms = e_start.elapsed_time(e_end) / K
-    idx_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(K))
-    attn_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(K))
-    dec_ms = statistics.mean(evs[i][2].elapsed_time(evs[i][3]) for i in range(K))
+    pre_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(K))
+    dec_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(K))
     ms = job_time_ms(ms, pg)
+
+    # stage breakdown: the same pass with the stages one after the other on
+    # every SM, so that each kernel's time (and roofline) is its own
+    sevs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    wl.stage_step()
+    torch.cuda.synchronize()
+    for i in range(K):
+        wl.stage_step(sevs[i])
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    Q.check_status(wl.status, "stage steps")
+    idx_ms = statistics.mean(sevs[i][0].elapsed_time(sevs[i][1]) for i in range(K))
+    attn_ms = statistics.mean(sevs[i][1].elapsed_time(sevs[i][2]) for i in range(K))
+    dec_serial_ms = statistics.mean(sevs[i][2].elapsed_time(sevs[i][3]) for i in range(K))
+    begin, ctas = wl.overlap_plan()
     value = job_tokens_per_s(wl.L + wl.B, world, ms)
 
     hbm = peaks.get("hbm_gbs")
@@ -691,10 +761,16 @@ def main():
                    "decode_batch": wl.B, "decode_ctx": wl.T,
                    "l2": "inputs larger than L2 (no flush needed)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "prefill_tokens_per_s": wl.L / ((idx_ms + attn_ms) / 1e3),
+        "prefill_tokens_per_s": wl.L / (pre_ms / 1e3),
         "decode_us_per_token": dec_ms * 1e3,
         "decode_us_per_step": dec_ms * 1e3,
-        "stage_ms": {"indexer_topk": idx_ms, "sparse_attn_prefill": attn_ms, "decode_step": dec_ms},
+        "stage_ms": {"prefill_overlapped": pre_ms, "decode_step": dec_ms,
+                     "indexer_topk_alone": idx_ms, "sparse_attn_prefill_alone": attn_ms,
+                     "decode_step_after_serial_prefill": dec_serial_ms},
+        "overlap": {"chunks": len(ctas), "index_ctas": ctas, "serial_prefill_ms": idx_ms + attn_ms,
+                    "speedup_vs_serial": (idx_ms + attn_ms) / pre_ms,
+                    "stage_region": "per-stage times and kernel rooflines come from a second timed region "
+                                    "of the same K steps with the stages one after the other"},
         "roofline": {"bound": "hbm", "achieved": attn_gbs, "peak": hbm, "unit": "GB/s",
                      "frac": attn_gbs / hbm, "traffic": traffic,
                      "kernel": "sparse_attn_prefill", "peak_source": peak_src + " hbm_gbs",
@@ -705,6 +781,7 @@ def main():
             "decode_step": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
                             "frac": dec_gbs / hbm},
         },
+        "prefill_bound": prefill_bound(wl, pre_ms, tc, hbm),
         "gpu_launches": wl.launches_per_step() * K,
         "clocks": clk,
     }
@@ -713,7 +790,7 @@ def main():
     except Exception as ex:
         line["decode_back_to_back"] = {"us_per_step": None, "error": str(ex)[:200]}
     try:
-        line["prefix_cached_prefill"] = run_prefix_cached(wl, max(1, min(K, 3)), 2, idx_ms + attn_ms)
+        line["prefix_cached_prefill"] = run_prefix_cached(wl, max(1, min(K, 3)), 2, pre_ms)
     except Exception as ex:  # report, never fake
         line["prefix_cached_prefill"] = {"ms": None, "error": str(ex)[:200]}
     if rank == 0 and not args.no_token_level:
@@ -723,7 +800,7 @@ def main():
             line["token_level_indexer"] = {"error": str(ex)[:200]}
     if rank == 0 and not args.no_dense:
         try:
-            line["dense_comparison"] = run_dense_comparison(wl, idx_ms + attn_ms, dec_ms)
+            line["dense_comparison"] = run_dense_comparison(wl, pre_ms, dec_ms)
         except Exception as ex:
             line["dense_comparison"] = {"error": str(ex)[:200]}
     if not args.no_e2e:

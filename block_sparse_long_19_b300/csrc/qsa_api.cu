@@ -173,6 +173,52 @@ namespace qsa {
 void set_error_detail(const char *msg) { g_detail = msg; }
 }  // namespace qsa
 
+// ------------------------------------------------- overlapped prefill --
+// The indexer is bound by its epilogue's instruction issue and the
+// attention by HBM bytes, so the two can share the GPU: the query rows are
+// cut into chunks, and while the attention of chunk j-1 runs on part of the
+// SMs, the indexer of chunk j runs as a persistent grid on the others (a
+// second, higher-priority stream).  The split balances the two stages' time
+// per chunk from per-SM costs fitted to B300 runs of both kernels, side by
+// side, at 128K and 1M tokens: the indexer takes 2.14e-10 SM-seconds per
+// (query, past block) pair plus 8.2e-6 per query row (its list start-up and
+// final selection); the attention consumes 65 GB/s of gathered K/V per SM
+// (2 KiB per attended key) and cannot go below 6.9 TB/s for the whole GPU.
+// Below 256K tokens the attention's K/V mostly sits in L2 and the attention
+// is bound by its SMs rather than by HBM, so there is nothing to hand to the
+// indexer: shorter prefills run the two stages one after the other.
+namespace {
+
+constexpr int64_t kOverlapMinL = 262144;
+
+constexpr double kIdxPairSm = 2.14e-10;
+constexpr double kIdxRowSm = 8.2e-6;
+constexpr double kAttnKeySm = 2048.0 / 65e9;
+constexpr double kAttnKeyFloor = 2048.0 / 6.9e12;
+
+// sum over t in [r0, r1) of floor(t/4): the pairs the indexer scores
+double pairs_in(int64_t r0, int64_t r1) {
+    auto upto = [](int64_t n) {  // sum over t < n of floor(t/4)
+        const int64_t q = n / 4, r = n % 4;
+        return 4.0 * (static_cast<double>(q) * (q - 1) / 2.0) + static_cast<double>(r) * q;
+    };
+    return upto(r1) - upto(r0);
+}
+
+// sum over t in [r0, r1) of the keys query t attends: t+1 while its block
+// is below the budget, 4(budget-1) + t%4 + 1 after that
+double keys_in(int64_t r0, int64_t r1, int budget) {
+    const int64_t t0 = 4 * static_cast<int64_t>(budget - 1);
+    double s = 0.0;
+    const int64_t a1 = r1 < t0 ? r1 : t0;
+    if (r0 < a1) s += (static_cast<double>(a1) * (a1 + 1) - static_cast<double>(r0) * (r0 + 1)) / 2.0;
+    const int64_t b0 = r0 > t0 ? r0 : t0;
+    if (b0 < r1) s += static_cast<double>(r1 - b0) * (4.0 * (budget - 1) + 2.5);
+    return s;
+}
+
+}  // namespace
+
 extern "C" {
 
 void qsa_default_config(qsa_config *cfg) {
@@ -350,6 +396,168 @@ qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
     return qsa_sparse_attn_prefill_cached(cfg, q, k_rot, v, idx, 0, L, out, lse, dev_status, stream);
 }
 
+int qsa_prefill_overlap_plan(const qsa_config *cfg, int64_t L, int sms, int max_chunks,
+                             int64_t *chunk_begin, int *index_ctas) {
+    if (check_cfg(cfg) != QSA_OK || L < 1 || L > kMaxL || sms < 2 || max_chunks < 1 || !chunk_begin ||
+        !index_ctas)
+        return 0;
+    const int64_t tq = 64;  // query rows per indexer tile
+    int64_t rows = ((L + 15) / 16 + tq - 1) / tq * tq;
+    if (rows < 16384) rows = 16384;
+    // equal chunks; a remainder under half a chunk joins the last one
+    int64_t n = (L + rows / 2) / rows;
+    if (n < 1) n = 1;
+    if (n > max_chunks) {
+        rows = ((L + max_chunks - 1) / max_chunks + tq - 1) / tq * tq;
+        n = (L + rows - 1) / rows;
+    }
+    if (cfg->budget_blocks <= 1 || L < kOverlapMinL) n = 1;
+    if (n <= 1) {
+        chunk_begin[0] = 0;
+        chunk_begin[1] = L;
+        index_ctas[0] = sms;
+        return 1;
+    }
+    for (int64_t j = 0; j < n; ++j) chunk_begin[j] = j * rows;
+    chunk_begin[n] = L;
+    index_ctas[0] = sms;  // the first chunk's indexer runs alone
+    for (int64_t j = 1; j < n; ++j) {
+        const double w = pairs_in(chunk_begin[j], chunk_begin[j + 1]) * kIdxPairSm +
+                         static_cast<double>(chunk_begin[j + 1] - chunk_begin[j]) * kIdxRowSm;
+        const double keys = keys_in(chunk_begin[j - 1], chunk_begin[j], cfg->budget_blocks);
+        const double a = keys * kAttnKeySm, fl = keys * kAttnKeyFloor;
+        int best = 1;
+        double best_t = 1e300;
+        for (int x = 1; x < sms; ++x) {
+            const double ta = a / (sms - x) > fl ? a / (sms - x) : fl;
+            const double t = w / x > ta ? w / x : ta;
+            if (t < best_t) {
+                best_t = t;
+                best = x;
+            }
+        }
+        index_ctas[j] = best;
+    }
+    return static_cast<int>(n);
+}
+
+size_t qsa_prefill_overlapped_workspace_bytes(const qsa_config *cfg, int64_t L) {
+    return qsa_index_topk_workspace_bytes(cfg, L);
+}
+
+qsa_status qsa_prefill_overlapped(const qsa_config *cfg, const qsa_bf16 *q, const qsa_bf16 *qi,
+                                  const qsa_bf16 *w, const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot,
+                                  const qsa_bf16 *v, int64_t L, int32_t *idx, float *score, qsa_bf16 *out,
+                                  float *lse, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream) {
+    qsa_status st = check_cfg(cfg);
+    if (st != QSA_OK) return st;
+    if (L < 1) return fail(QSA_ERR_INVALID_ARG, "L must be >= 1");
+    if (L > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "L > %lld", static_cast<long long>(kMaxL));
+    REQ_PTR(q);
+    REQ_PTR(qi);
+    REQ_PTR(w);
+    REQ_PTR(ki);
+    REQ_PTR(k);
+    REQ_PTR(k_rot);
+    REQ_PTR(v);
+    REQ_PTR(idx);
+    OPT_PTR(score);
+    REQ_PTR(out);
+    OPT_PTR(lse);
+    REQ_PTR(dev_status);
+    const size_t need = index_ws(L);
+    if (!ws || ws_bytes < need)
+        return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
+    if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");
+
+    const int sms = sm_count();
+    constexpr int kMaxChunks = 64;
+    int64_t begin[kMaxChunks + 1];
+    int ctas[kMaxChunks];
+    const int n = qsa_prefill_overlap_plan(cfg, L, sms, kMaxChunks, begin, ctas);
+    if (n < 1) return fail(QSA_ERR_INVALID_ARG, "no chunk plan");
+    if (n == 1) {  // nothing to overlap: the two stages one after the other
+        st = index_common(cfg, qi, w, ki, k, k_rot, L, idx, score, nullptr, ws, ws_bytes, dev_status, stream);
+        if (st != QSA_OK) return st;
+        return qsa_sparse_attn_prefill_cached(cfg, q, k_rot, v, idx, 0, L, out, lse, dev_status, stream);
+    }
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *wsb = static_cast<uint8_t *>(ws);
+    uint16_t *kblk = reinterpret_cast<uint16_t *>(wsb);
+    const size_t kblk_bytes = align_up(static_cast<size_t>(L / qsa::kBlock) * qsa::kDI * 2 + 16, 1024);
+    void *cand = wsb + kblk_bytes;
+    const int budget = cfg->budget_blocks;
+    const qsa::RopeFreqs freqs = freqs_of(cfg);
+
+    // the side stream and the events live until their work is done (CUDA
+    // releases a destroyed stream or event once its pending work completes)
+    int lo = 0, hi = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e != cudaSuccess) return cuda_fail(e, "stream priority range");
+    cudaStream_t side = nullptr;
+    e = cudaStreamCreateWithPriority(&side, cudaStreamNonBlocking, hi);
+    if (e != cudaSuccess) return cuda_fail(e, "side stream");
+    cudaEvent_t ev[kMaxChunks + 1];
+    int nev = 0;
+    auto cleanup = [&]() {
+        for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);
+        cudaStreamDestroy(side);
+    };
+    for (; nev < n + 1; ++nev) {
+        e = cudaEventCreateWithFlags(&ev[nev], cudaEventDisableTiming);
+        if (e != cudaSuccess) {
+            cleanup();
+            return cuda_fail(e, "event");
+        }
+    }
+    auto run = [&]() -> qsa_status {
+        cudaError_t e2 = qsa::launch_kprep(1, 0, L, L, ki, k, k_rot, kblk, freqs, sms, s);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "kprep launch");
+        if ((e2 = cudaEventRecord(ev[n], s)) != cudaSuccess) return cuda_fail(e2, "event record");
+        if ((e2 = cudaStreamWaitEvent(side, ev[n], 0)) != cudaSuccess) return cuda_fail(e2, "stream wait");
+        for (int j = 0; j < n; ++j) {
+            const int64_t r0 = begin[j], nr = begin[j + 1] - begin[j];
+            CUtensorMap map_q, map_k;
+            qsa_status st2 = make_map(&map_q, qi + r0 * qsa::kHI * qsa::kDI, qsa::kDI,
+                                      static_cast<uint64_t>(nr) * qsa::kHI, 256);
+            if (st2 != QSA_OK) return st2;
+            const int64_t nbk = (r0 + nr) / qsa::kBlock;
+            st2 = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
+            if (st2 != QSA_OK) return st2;
+            e2 = qsa::launch_index(map_q, map_k, r0, nr, qsa::kBlock, budget, w + r0 * qsa::kHI,
+                                   idx + r0 * budget, score ? score + r0 * budget : nullptr, nullptr, cand,
+                                   dev_status, ctas[j], side);
+            if (e2 != cudaSuccess) return cuda_fail(e2, "indexer launch");
+            if ((e2 = cudaEventRecord(ev[j], side)) != cudaSuccess) return cuda_fail(e2, "event record");
+        }
+        for (int j = 0; j < n; ++j) {
+            const int64_t r0 = begin[j], nr = begin[j + 1] - begin[j];
+            if ((e2 = cudaStreamWaitEvent(s, ev[j], 0)) != cudaSuccess) return cuda_fail(e2, "stream wait");
+            qsa::AttnArgs a{};
+            a.q = q + r0 * qsa::kHQ * qsa::kD;
+            a.k = k_rot;
+            a.v = v;
+            a.idx = idx + r0 * budget;
+            a.budget = budget;
+            a.L = nr;
+            a.q_off = r0;
+            a.out = out + r0 * qsa::kHQ * qsa::kD;
+            a.lse = lse ? lse + r0 * qsa::kHQ : nullptr;
+            a.nsplit = 1;
+            a.scale_log2 = scale_log2_of(cfg);
+            a.status = dev_status;
+            e2 = qsa::launch_attn_prefill(a, freqs, s);
+            if (e2 != cudaSuccess) return cuda_fail(e2, "attention launch");
+        }
+        return QSA_OK;
+    };
+    st = run();
+    cleanup();
+    if (st != QSA_OK) return st;
+    return ok();
+}
+
 qsa_status qsa_kprep_range(const qsa_config *cfg, const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot,
                            qsa_bf16 *kblk, int64_t t_begin, int64_t t_end, void *stream) {
     qsa_status st = check_cfg(cfg);
@@ -416,8 +624,17 @@ qsa_status qsa_index_topk_cached(const qsa_config *cfg, const qsa_bf16 *qi, cons
                                  const qsa_bf16 *kblk, int64_t q_offset, int64_t Lq, int32_t *idx,
                                  float *score, void *ws, size_t ws_bytes, int32_t *dev_status,
                                  void *stream) {
+    return qsa_index_topk_cached_ctas(cfg, qi, w, kblk, q_offset, Lq, idx, score, 0, ws, ws_bytes, dev_status,
+                                      stream);
+}
+
+qsa_status qsa_index_topk_cached_ctas(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                                      const qsa_bf16 *kblk, int64_t q_offset, int64_t Lq, int32_t *idx,
+                                      float *score, int max_ctas, void *ws, size_t ws_bytes,
+                                      int32_t *dev_status, void *stream) {
     qsa_status st = check_cfg(cfg);
     if (st != QSA_OK) return st;
+    if (max_ctas < 0) return fail(QSA_ERR_INVALID_ARG, "max_ctas must be >= 0");
     if (Lq < 1) return fail(QSA_ERR_INVALID_ARG, "the number of query rows must be >= 1");
     if (q_offset < 0) return fail(QSA_ERR_INVALID_ARG, "q_offset must be >= 0");
     if (q_offset + Lq > kMaxL) return fail(QSA_ERR_UNSUPPORTED, "more than %lld positions", static_cast<long long>(kMaxL));
@@ -445,8 +662,9 @@ qsa_status qsa_index_topk_cached(const qsa_config *cfg, const qsa_bf16 *qi, cons
     const int64_t nbk = (q_offset + Lq) / qsa::kBlock;
     st = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
     if (st != QSA_OK) return st;
+    const int sms = sm_count();
     e = qsa::launch_index(map_q, map_k, q_offset, Lq, qsa::kBlock, cfg->budget_blocks, w, idx, score, nullptr,
-                          ws, dev_status, sm_count(), s);
+                          ws, dev_status, max_ctas > 0 && max_ctas < sms ? max_ctas : sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     return ok();
 }

@@ -33,7 +33,8 @@ EXPORTED = [
     "qsa_sparse_attn_prefill", "qsa_decode_workspace_bytes", "qsa_sparse_attn_decode",
     "qsa_sparse_attn_decode_noalloc", "qsa_kprep_range", "qsa_index_topk_cached_workspace_bytes",
     "qsa_index_topk_cached", "qsa_sparse_attn_prefill_cached", "qsa_index_topk_tokens_workspace_bytes",
-    "qsa_index_topk_tokens", "qsa_selftest_bounded_wait",
+    "qsa_index_topk_tokens", "qsa_selftest_bounded_wait", "qsa_prefill_overlapped_workspace_bytes",
+    "qsa_prefill_overlapped", "qsa_prefill_overlap_plan", "qsa_index_topk_cached_ctas",
 ]
 
 
@@ -100,6 +101,9 @@ def load(path: str = LIB_PATH):
     L.qsa_index_topk_cached_workspace_bytes.restype = c.c_size_t
     L.qsa_index_topk_cached.argtypes = [cfgp, P, P, P, c.c_int64, c.c_int64, P, P, P, c.c_size_t, P, P]
     L.qsa_index_topk_cached.restype = c.c_int
+    L.qsa_index_topk_cached_ctas.argtypes = [cfgp, P, P, P, c.c_int64, c.c_int64, P, P, c.c_int, P, c.c_size_t,
+                                             P, P]
+    L.qsa_index_topk_cached_ctas.restype = c.c_int
     L.qsa_sparse_attn_prefill_cached.argtypes = [cfgp, P, P, P, P, c.c_int64, c.c_int64, P, P, P, P]
     L.qsa_sparse_attn_prefill_cached.restype = c.c_int
     L.qsa_index_topk_tokens_workspace_bytes.argtypes = [cfgp, c.c_int64]
@@ -108,6 +112,13 @@ def load(path: str = LIB_PATH):
     L.qsa_index_topk_tokens.restype = c.c_int
     L.qsa_selftest_bounded_wait.argtypes = [c.c_int64, c.c_int, P, P]
     L.qsa_selftest_bounded_wait.restype = c.c_int
+    L.qsa_prefill_overlapped_workspace_bytes.argtypes = [cfgp, c.c_int64]
+    L.qsa_prefill_overlapped_workspace_bytes.restype = c.c_size_t
+    L.qsa_prefill_overlapped.argtypes = [cfgp, P, P, P, P, P, P, P, c.c_int64, P, P, P, P, P, c.c_size_t, P, P]
+    L.qsa_prefill_overlapped.restype = c.c_int
+    L.qsa_prefill_overlap_plan.argtypes = [cfgp, c.c_int64, c.c_int, c.c_int, c.POINTER(c.c_int64),
+                                           c.POINTER(c.c_int)]
+    L.qsa_prefill_overlap_plan.restype = c.c_int
     _lib = L
     return L
 
@@ -273,9 +284,10 @@ def kprep_range(cfg: Config, ki, kblk, t_begin: int, t_end: int, k=None, k_rot=N
 
 
 def index_topk_cached(cfg: Config, qi, w, kblk, q_offset: int, idx=None, score=None, ws=None, status=None,
-                      want_score: bool = True, stream=None):
+                      want_score: bool = True, stream=None, max_ctas: int = 0):
     """Indexer + selection for the query rows q_offset .. q_offset+Lq-1 of a
-    sequence whose block keys so far are kblk.  Returns (idx, score, status)."""
+    sequence whose block keys so far are kblk.  max_ctas > 0 limits the
+    persistent grid to that many SMs.  Returns (idx, score, status)."""
     Lq = qi.shape[0]
     dev = qi.device
     _need(qi, "qi", torch.bfloat16, (Lq, 4, 128))
@@ -293,9 +305,9 @@ def index_topk_cached(cfg: Config, qi, w, kblk, q_offset: int, idx=None, score=N
         ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
     if status is None:
         status = new_status(dev)
-    _check(load().qsa_index_topk_cached(ctypes.byref(cfg), _ptr(qi), _ptr(w), _ptr(kblk), q_offset, Lq,
-                                        _ptr(idx), _ptr(score), _ptr(ws), ws.numel(), _ptr(status),
-                                        _stream(stream)), "qsa_index_topk_cached")
+    _check(load().qsa_index_topk_cached_ctas(ctypes.byref(cfg), _ptr(qi), _ptr(w), _ptr(kblk), q_offset, Lq,
+                                             _ptr(idx), _ptr(score), max_ctas, _ptr(ws), ws.numel(), _ptr(status),
+                                             _stream(stream)), "qsa_index_topk_cached_ctas")
     return idx, score, status
 
 
@@ -440,15 +452,71 @@ def prefill(cfg: Config, q, k, v, qi, w, ki, want_score: bool = False, want_lse:
     return PrefillResult(idx, score, k_rot, out, lse, status)
 
 
+def prefill_overlapped_workspace_bytes(cfg: Config, L: int) -> int:
+    return int(load().qsa_prefill_overlapped_workspace_bytes(ctypes.byref(cfg), L))
+
+
+def prefill_overlap_plan(cfg: Config, L: int, sms: int, max_chunks: int = 64):
+    """Chunk starts (n+1 values, the last = L) and indexer grid sizes (n
+    values) that prefill_overlapped uses on a GPU with `sms` SMs."""
+    begin = (ctypes.c_int64 * (max_chunks + 1))()
+    ctas = (ctypes.c_int * max_chunks)()
+    n = load().qsa_prefill_overlap_plan(ctypes.byref(cfg), L, sms, max_chunks, begin, ctas)
+    if n < 1:
+        raise QsaError(1, "qsa_prefill_overlap_plan: invalid arguments")
+    return [int(begin[i]) for i in range(n + 1)], [int(ctas[i]) for i in range(n)]
+
+
+def prefill_overlapped(cfg: Config, q, k, v, qi, w, ki, k_rot=None, idx=None, score=None, out=None, lse=None,
+                       ws=None, status=None, want_score: bool = False, want_lse: bool = True,
+                       stream=None) -> PrefillResult:
+    """The whole prefill layer with the indexer of one chunk of query rows
+    running beside the attention of the previous chunk (same results as
+    prefill())."""
+    L = q.shape[0]
+    dev = q.device
+    _need(q, "q", torch.bfloat16, (L, 24, 256))
+    _need(k, "k", torch.bfloat16, (L, 2, 256))
+    _need(v, "v", torch.bfloat16, (L, 2, 256))
+    _need(qi, "qi", torch.bfloat16, (L, 4, 128))
+    _need(w, "w", torch.bfloat16, (L, 4))
+    _need(ki, "ki", torch.bfloat16, (L, 128))
+    B = cfg.budget_blocks
+    if k_rot is None:
+        k_rot = torch.empty_like(k)
+    if idx is None:
+        idx = torch.empty((L, B), dtype=torch.int32, device=dev)
+    if score is None and want_score:
+        score = torch.empty((L, B), dtype=torch.float32, device=dev)
+    if out is None:
+        out = torch.empty((L, 24, 256), dtype=torch.bfloat16, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty((L, 24), dtype=torch.float32, device=dev)
+    need = prefill_overlapped_workspace_bytes(cfg, L)
+    if ws is None:
+        ws = torch.empty(max(need, 16), dtype=torch.uint8, device=dev)
+    if status is None:
+        status = new_status(dev)
+    _check(load().qsa_prefill_overlapped(ctypes.byref(cfg), _ptr(q), _ptr(qi), _ptr(w), _ptr(ki), _ptr(k),
+                                         _ptr(k_rot), _ptr(v), L, _ptr(idx), _ptr(score), _ptr(out), _ptr(lse),
+                                         _ptr(ws), ws.numel(), _ptr(status), _stream(stream)),
+           "qsa_prefill_overlapped")
+    return PrefillResult(idx, score, k_rot, out, lse, status)
+
+
 class HostPrefill:
     """Prefill of one sequence whose inputs live in pinned host memory.
 
     The sequence is processed in chunks of query rows with the cached-prefix
     calls (each chunk's rows against every earlier token), so the host->device
     copies of chunk c+1 and the device->host copy of chunk c-1's output run on
-    their own streams while chunk c computes.  The results equal those of
-    prefill() on the whole sequence (the per-query computation does not depend
-    on the chunking).  Device buffers are allocated once, here."""
+    their own streams while chunk c computes.  For long prefills the chunks
+    and indexer grid sizes are those of prefill_overlapped(): the K-prep and
+    indexer of a chunk run on a higher-priority stream on a share of the SMs
+    while the attention of the previous chunk runs on the rest.  The results
+    equal those of prefill() on the whole sequence (the per-query computation
+    does not depend on the chunking).  Device buffers are allocated once,
+    here."""
 
     NAMES = ("q", "k", "v", "qi", "w", "ki")
 
@@ -464,11 +532,19 @@ class HostPrefill:
         self.out = torch.empty((L, 24, 256), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty((L, 24), dtype=torch.float32, device=device)
         self.status = new_status(device)
-        need = load().qsa_index_topk_cached_workspace_bytes(ctypes.byref(cfg), min(self.chunk, L))
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        begin, ctas = prefill_overlap_plan(cfg, L, sms)
+        if len(ctas) > 1:
+            self.bounds, self.ctas = begin, ctas
+        else:
+            self.bounds = list(range(0, L, self.chunk)) + [L]
+            self.ctas = None
+        longest = max(b - a for a, b in zip(self.bounds[:-1], self.bounds[1:]))
+        need = load().qsa_index_topk_cached_workspace_bytes(ctypes.byref(cfg), longest)
         self.ws = torch.empty(max(need, 16), dtype=torch.uint8, device=device)
         self.h2d = torch.cuda.Stream(device=device)
         self.d2h = torch.cuda.Stream(device=device)
-        self.bounds = list(range(0, L, self.chunk)) + [L]
+        self.side = torch.cuda.Stream(device=device, priority=-8) if self.ctas else None
 
     def run(self, host: dict, out_host: torch.Tensor, lse_host: torch.Tensor | None = None):
         """host: pinned CPU tensors q, k, v, qi, w, ki of the whole sequence;
@@ -476,26 +552,33 @@ class HostPrefill:
         Enqueues everything; the caller's current stream waits for the last
         copy back."""
         cfg, comp = self.cfg, torch.cuda.current_stream(self.dev)
+        ixs = self.side if self.ctas else comp  # stream of K-prep + indexer
         start = torch.cuda.Event()
         start.record(comp)
-        self.h2d.wait_event(start)
-        self.d2h.wait_event(start)
-        ins, outs = [], []
-        for a, b in zip(self.bounds[:-1], self.bounds[1:]):
+        for st in (self.h2d, self.d2h) + ((self.side,) if self.side else ()):
+            st.wait_event(start)
+        chunks = list(zip(self.bounds[:-1], self.bounds[1:]))
+        ins = []
+        for a, b in chunks:
             ev = torch.cuda.Event()
             with torch.cuda.stream(self.h2d):
                 for n in self.NAMES:
                     self.dev_in[n][a:b].copy_(host[n][a:b], non_blocking=True)
                 ev.record(self.h2d)
             ins.append(ev)
-        for (a, b), ev in zip(zip(self.bounds[:-1], self.bounds[1:]), ins):
-            comp.wait_event(ev)
-            d = self.dev_in
-            kprep_range(cfg, d["ki"][:b], self.kblk, a, b, k=d["k"][:b], k_rot=self.k_rot[:b])
+        d = self.dev_in
+        for j, ((a, b), ev) in enumerate(zip(chunks, ins)):
+            ixs.wait_event(ev)
+            kprep_range(cfg, d["ki"][:b], self.kblk, a, b, k=d["k"][:b], k_rot=self.k_rot[:b], stream=ixs)
             index_topk_cached(cfg, d["qi"][a:b], d["w"][a:b], self.kblk[: max(b // 4, 1)], a, idx=self.idx[a:b],
-                              score=None, ws=self.ws, status=self.status, want_score=False)
+                              score=None, ws=self.ws, status=self.status, want_score=False, stream=ixs,
+                              max_ctas=self.ctas[j] if self.ctas else 0)
+            if self.ctas:
+                sel = torch.cuda.Event()
+                sel.record(ixs)
+                comp.wait_event(sel)
             sparse_attn_prefill_cached(cfg, d["q"][a:b], self.k_rot[:b], d["v"][:b], self.idx[a:b], a,
-                                       out=self.out[a:b], lse=self.lse[a:b], status=self.status)
+                                       out=self.out[a:b], lse=self.lse[a:b], status=self.status, stream=comp)
             done = torch.cuda.Event()
             done.record(comp)
             self.d2h.wait_event(done)
@@ -503,6 +586,5 @@ class HostPrefill:
                 out_host[a:b].copy_(self.out[a:b], non_blocking=True)
                 if lse_host is not None:
                     lse_host[a:b].copy_(self.lse[a:b], non_blocking=True)
-            outs.append(done)
         comp.wait_stream(self.d2h)
         return self.status

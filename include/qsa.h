@@ -224,10 +224,58 @@ qsa_status qsa_index_topk_cached(const qsa_config *cfg, const qsa_bf16 *qi, cons
                                  const qsa_bf16 *kblk, int64_t q_offset, int64_t Lq, int32_t *idx,
                                  float *score, void *ws, size_t ws_bytes, int32_t *dev_status,
                                  void *stream);
+/* qsa_index_topk_cached_ctas: qsa_index_topk_cached with the indexer's
+ * persistent grid limited to max_ctas CTAs (one per SM; 0 or more than the
+ * SM count = every SM), so that other work can run beside it on the other
+ * SMs.  Same results for every max_ctas; INVALID_ARG if max_ctas < 0. */
+qsa_status qsa_index_topk_cached_ctas(const qsa_config *cfg, const qsa_bf16 *qi, const qsa_bf16 *w,
+                                      const qsa_bf16 *kblk, int64_t q_offset, int64_t Lq, int32_t *idx,
+                                      float *score, int max_ctas, void *ws, size_t ws_bytes,
+                                      int32_t *dev_status, void *stream);
 qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 *q,
                                           const qsa_bf16 *k_rot, const qsa_bf16 *v, const int32_t *idx,
                                           int64_t q_offset, int64_t Lq, qsa_bf16 *out, float *lse,
                                           int32_t *dev_status, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Whole prefill of one sequence with the indexer and the attention running
+ * side by side (the launch post, "Attention: GDN + QSA": indexer, selection
+ * and attention over the selected regions, with the same definitions as
+ * qsa_index_topk followed by qsa_sparse_attn_prefill, and bit-identical
+ * results).  The indexer's time goes to instruction issue and the
+ * attention's to HBM bytes, so the query rows are cut into chunks and the
+ * indexer of chunk j runs on a share of the SMs while the attention of chunk
+ * j-1 runs on the rest.
+ *   q [L, 24, 256], qi [L, 4, 128], w [L, 4], ki [L, 128], k [L, 2, 256]
+ *   (before RoPE), k_rot [L, 2, 256] out (may equal k), v [L, 2, 256];
+ *   idx [L, budget] and score [L, budget] (or NULL) as for qsa_index_topk;
+ *   out [L, 24, 256], lse [L, 24] (or NULL) as for qsa_sparse_attn_prefill.
+ *   ws: at least qsa_prefill_overlapped_workspace_bytes(cfg, L) bytes,
+ *   16-byte aligned.
+ * The call enqueues on `stream`; internally it forks a higher-priority
+ * stream for the indexer and joins it back before the last attention chunk,
+ * so work enqueued on `stream` afterwards sees every output.  Errors as for
+ * the two calls it combines; QSA_ERR_CUDA if the helper stream or its
+ * events cannot be created.
+ *
+ * Prefills shorter than 262,144 tokens (whose K/V mostly stays in L2, so the
+ * attention is bound by its SMs, not by HBM) and budget 1 run the two stages
+ * one after the other on `stream`.
+ *
+ * qsa_prefill_overlap_plan: the chunking this call uses on a GPU with `sms`
+ *   SMs (host only, no GPU needed).  Writes n+1 chunk starts
+ *   (chunk_begin[0] = 0, chunk_begin[n] = L; every inner start a multiple of
+ *   64) and n indexer grid sizes (index_ctas[0] = sms: the first chunk's
+ *   indexer runs alone), and returns n (1 <= n <= max_chunks), or 0 on
+ *   invalid arguments.  chunk_begin needs max_chunks + 1 entries.
+ * ---------------------------------------------------------------------- */
+size_t qsa_prefill_overlapped_workspace_bytes(const qsa_config *cfg, int64_t L);
+qsa_status qsa_prefill_overlapped(const qsa_config *cfg, const qsa_bf16 *q, const qsa_bf16 *qi,
+                                  const qsa_bf16 *w, const qsa_bf16 *ki, const qsa_bf16 *k, qsa_bf16 *k_rot,
+                                  const qsa_bf16 *v, int64_t L, int32_t *idx, float *score, qsa_bf16 *out,
+                                  float *lse, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream);
+int qsa_prefill_overlap_plan(const qsa_config *cfg, int64_t L, int sms, int max_chunks,
+                             int64_t *chunk_begin, int *index_ctas);
 
 /* ------------------------------------------------------------------------
  * Decode: one new token for each of `batch` sequences.  Sequence s holds

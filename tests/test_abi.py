@@ -151,6 +151,9 @@ def test_cached_prefix_calls_reject(lib):
     assert call(kb=None) == 1
     assert call(kb=MIS) == 1
     assert call(ws_bytes=16) == 3
+    ixc = lib.qsa_index_topk_cached_ctas
+    assert ixc(ctypes.byref(cfg), A, A, A, 64, 64, A, None, -1, A, 1 << 40, A, None) == 1  # negative grid
+    assert ixc(ctypes.byref(cfg), A, A, A, 64, 0, A, None, 8, A, 1 << 40, A, None) == 1
     at = lib.qsa_sparse_attn_prefill_cached
     assert at(ctypes.byref(cfg), A, A, A, A, -1, 16, A, None, A, None) == 1
     assert at(ctypes.byref(cfg), A, A, A, A, 16, 0, A, None, A, None) == 1
@@ -173,3 +176,65 @@ def test_selftest_rejects(lib):
     assert lib.qsa_selftest_bounded_wait(1000, 0, None, None) == 1
     assert lib.qsa_selftest_bounded_wait(0, 0, A, None) == 1
     assert lib.qsa_selftest_bounded_wait(200_000_000, 0, A, None) == 1
+
+
+def test_overlapped_prefill_rejects(lib):
+    """The overlapped prefill validates before it creates a stream or
+    launches anything."""
+    cfg = Q.default_config()
+    f = lib.qsa_prefill_overlapped
+    need = lib.qsa_prefill_overlapped_workspace_bytes(ctypes.byref(cfg), 1 << 16)
+    assert need == lib.qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 1 << 16) > 0
+
+    def call(L=1 << 16, ws_bytes=1 << 40, **kw):
+        a = dict(q=A, qi=A, w=A, ki=A, k=A, kr=A, v=A, idx=A, sc=None, out=A, lse=None, ws=A, st=A)
+        a.update(kw)
+        return f(ctypes.byref(cfg), a["q"], a["qi"], a["w"], a["ki"], a["k"], a["kr"], a["v"], L, a["idx"],
+                 a["sc"], a["out"], a["lse"], a["ws"], ws_bytes, a["st"], None)
+
+    assert call(L=0) == 1
+    assert call(L=(1 << 24) + 4) == 2
+    for name in ("q", "qi", "w", "ki", "k", "kr", "v", "idx", "out", "st"):
+        assert call(**{name: None}) == 1, name
+    assert call(q=MIS) == 1
+    assert call(ws_bytes=16) == 3
+    assert call(ws=MIS) == 1
+
+
+@pytest.mark.parametrize("L", [1, 1000, 16384, 70001, 262143, 262144, 266277, 1 << 20, 3_000_001, 1 << 24])
+@pytest.mark.parametrize("sms", [148, 132, 8])
+def test_overlap_plan_invariants(L, sms):
+    """Chunks tile [0, L) in order with inner starts on 64-row tiles; the
+    first indexer grid has every SM and the others leave SMs to the
+    attention; long prefills are cut into several chunks."""
+    cfg = Q.default_config()
+    begin, ctas = Q.prefill_overlap_plan(cfg, L, sms)
+    n = len(ctas)
+    assert 1 <= n <= 64 and len(begin) == n + 1
+    assert begin[0] == 0 and begin[-1] == L
+    assert all(a < b for a, b in zip(begin[:-1], begin[1:]))
+    assert all(b % 64 == 0 for b in begin[1:-1])
+    assert ctas[0] == sms
+    assert all(1 <= c < sms for c in ctas[1:])
+    if L >= 262144:
+        assert n >= 4
+    else:
+        assert n == 1  # short prefills: nothing to overlap
+    # a later chunk's indexer has more past blocks per query: never fewer SMs
+    # (the last chunk may be longer or shorter than the others)
+    assert all(a <= b for a, b in zip(ctas[1:-2], ctas[2:-1]))
+    # no stub of a chunk at the end
+    if n > 1:
+        assert begin[-1] - begin[-2] >= (begin[1] - begin[0]) // 2
+
+
+def test_overlap_plan_rejects_and_small_budget():
+    cfg = Q.default_config()
+    with pytest.raises(Q.QsaError):
+        Q.prefill_overlap_plan(cfg, 0, 148)
+    with pytest.raises(Q.QsaError):
+        Q.prefill_overlap_plan(cfg, 1 << 20, 1)
+    begin, ctas = Q.prefill_overlap_plan(Q.default_config(budget=1), 1 << 20, 148)
+    assert begin == [0, 1 << 20] and ctas == [148]  # nothing to overlap without an indexer
+    begin, ctas = Q.prefill_overlap_plan(cfg, 1 << 20, 148, max_chunks=3)
+    assert len(ctas) <= 3 and begin[-1] == 1 << 20

@@ -130,20 +130,56 @@ def test_prefix90_at_128k():
     check_outputs(bf16_to_f64(out[torch.as_tensor(loc, device=DEV)]), att["o"], "O")
 
 
-def test_host_prefill_pipeline_equals_device_prefill():
+@pytest.mark.parametrize("L,chunk", [(9001, 2048), (266277, 65536)])
+def test_host_prefill_pipeline_equals_device_prefill(L, chunk):
     """qsa.HostPrefill (inputs in pinned host memory, chunked, copies on their
-    own streams) returns exactly the device prefill's output and LSE."""
-    L, budget = 9001, 512
+    own streams; at 266,277 tokens also the indexer beside the attention on
+    two compute streams) returns exactly the device prefill's output and LSE."""
+    budget = 512
     t = W.prefill_inputs(L, 44, DEV)
     full = full_prefill(t, budget)
     cfg = Q.default_config(budget=budget)
     host = {n: t[n].cpu().pin_memory() for n in Q.HostPrefill.NAMES}
     out_h = torch.empty((L, 24, 256), dtype=torch.bfloat16).pin_memory()
     lse_h = torch.empty((L, 24), dtype=torch.float32).pin_memory()
-    hp = Q.HostPrefill(cfg, L, chunk_tokens=2048)
+    hp = Q.HostPrefill(cfg, L, chunk_tokens=chunk)
+    assert (hp.ctas is not None) == (L >= 262144)
     st = hp.run(host, out_h, lse_h)
     torch.cuda.synchronize()
     Q.check_status(st)
     assert torch.equal(out_h, full.out.cpu())
     assert torch.equal(lse_h, full.lse.cpu())
     assert torch.equal(hp.idx, full.idx)
+
+
+@pytest.mark.parametrize("L,budget", [
+    (266277, 512),  # 16 chunks, the last one ragged
+    (262144, 32),   # 16 chunks, small budget
+    (70001, 512),   # short: the two stages one after the other
+    (65536, 1),     # no indexer work: the current block only
+])
+def test_overlapped_prefill_equals_serial_prefill(L, budget):
+    """qsa_prefill_overlapped (the indexer of chunk j beside the attention of
+    chunk j-1, on two streams) writes exactly what the serial prefill writes:
+    selection, scores, RoPE'd keys, output and LSE; sampled rows of the last
+    chunk also against the oracle."""
+    t = W.prefill_inputs(L, 45, DEV)
+    full = full_prefill(t, budget)
+    cfg = Q.default_config(budget=budget)
+    res = Q.prefill_overlapped(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"], want_score=True)
+    torch.cuda.synchronize()
+    Q.check_status(res.status)
+    assert torch.equal(res.idx, full.idx)
+    assert torch.equal(res.score, full.score)
+    assert torch.equal(res.k_rot, full.k_rot)
+    assert torch.equal(res.out, full.out)
+    assert torch.equal(res.lse, full.lse)
+    if budget > 1 and L >= 262144:
+        hb = W.host_bits(t)
+        begin, _ = Q.prefill_overlap_plan(cfg, L, torch.cuda.get_device_properties(0).multi_processor_count)
+        rows = rows_from(L, begin[-2], 16, 7)
+        idx_g = res.idx.cpu().numpy()[rows]
+        ref = O.prefill_rows(hb, rows, budget, want_o=False)
+        check_selection(idx_g, ref["idx"], O.prefill_scores(hb, rows), rows, budget)
+        att = O.prefill_rows(hb, rows, budget, idx_given=idx_g)
+        check_outputs(bf16_to_f64(res.out[torch.as_tensor(rows, device=DEV)]), att["o"], "O")
