@@ -35,7 +35,10 @@
  *     entry point (qsa_sparse_attn_decode_noalloc, at the end, is the one
  *     call that uses a built-in scratch array instead of a workspace).
  *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL = the legacy
- *     default stream) and return without synchronising.
+ *     default stream) and return without synchronising.  One call,
+ *     qsa_prefill_overlapped, also forks a helper stream and events of its
+ *     own (released by CUDA once their work is done) and joins them back
+ *     into `stream` before it returns.
  *   - Argument errors are reported synchronously by the return value, and
  *     then NOTHING is launched and no output is written.  A failed launch
  *     returns QSA_ERR_CUDA (qsa_last_error_detail() says which).
