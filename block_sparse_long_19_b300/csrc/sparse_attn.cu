@@ -23,7 +23,9 @@
 //   * four consumer warps (KV head x key half of every stage) run QK^T and PV
 //     with the warp-level MMA (m16n8k16, bf16 in, fp32 out) and an fp32 online
 //     softmax in the log2 domain with a lazy rescale; the two halves merge at
-//     the end.  Every consumer waits on every stage: with an odd ring depth,
+//     the end.  A warp keeps its KV head's query fragments in registers for
+//     the whole key loop, so per stage shared memory is read only for K and
+//     V.  Every consumer waits on every stage: with an odd ring depth,
 //     consumers that skipped stages could wait on a slot two fills ahead,
 //     which a one-bit phase parity cannot tell apart.
 // Decode runs the same kernel over a slice of the selected blocks per CTA
@@ -262,6 +264,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     // of slots 0-7, lanes 16-31 -> dims +8
     const uint32_t v_lane = (lane & 7) * SLOTB + (2 * kh + ((lane >> 3) & 1)) * ROWB + (lane >> 4) * 16;
     bool ok = true;
+    // the query's A fragments stay in registers for the whole key loop
+    uint32_t qf[kD / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < kD / 16; ++kk) ldsm_x4(q_addr + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
 
     for (int st = st_begin; st < st_end; ++st) {
         const int local = st - st_begin;
@@ -277,11 +283,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
         for (int n = 0; n < 2; ++n) S[n][0] = S[n][1] = S[n][2] = S[n][3] = 0.f;
 #pragma unroll
         for (int kk = 0; kk < kD / 16; ++kk) {
-            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
-            ldsm_x4(q_addr + kk * 32, a0, a1, a2, a3);
+            uint32_t b0, b1, b2, b3;
             ldsm_x4(kb + k_lane + kk * 32, b0, b1, b2, b3);
-            mma_bf16_16816(S[0], a0, a1, a2, a3, b0, b1);
-            mma_bf16_16816(S[1], a0, a1, a2, a3, b2, b3);
+            mma_bf16_16816(S[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+            mma_bf16_16816(S[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
         }
         bool need_mask = false;
 #pragma unroll
