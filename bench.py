@@ -465,6 +465,7 @@ def run_e2e(wl: Workload, steps: int) -> dict:
         p[n] = None
     torch.cuda.empty_cache()
     hp = Q.HostPrefill(wl.cfg, wl.L, device=wl.dev)
+    hp_ctas = hp.ctas is not None
 
     def one():
         hp.run(host, out_h, lse_h)
@@ -497,7 +498,9 @@ def run_e2e(wl: Workload, steps: int) -> dict:
     del host, dhost, out_h, lse_h, dout_h
     return {"value": (wl.L + wl.B) / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "prefill": "qsa.HostPrefill, 65,536-token chunks, copies overlapped with compute",
+            "prefill": ("qsa.HostPrefill: the overlapped prefill's chunks (first and last in 4 parts), "
+                        "host copies on their own streams beside the compute"
+                        if hp_ctas else "qsa.HostPrefill, 65,536-token chunks, copies overlapped with compute"),
             "output_spot_check": ok}
 
 

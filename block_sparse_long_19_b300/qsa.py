@@ -511,16 +511,18 @@ class HostPrefill:
     calls (each chunk's rows against every earlier token), so the host->device
     copies of chunk c+1 and the device->host copy of chunk c-1's output run on
     their own streams while chunk c computes.  For long prefills the chunks
-    and indexer grid sizes are those of prefill_overlapped(): the K-prep and
-    indexer of a chunk run on a higher-priority stream on a share of the SMs
-    while the attention of the previous chunk runs on the rest.  The results
+    and indexer grid sizes are those of prefill_overlapped() (its first and
+    last chunk split into `edge_parts` parts, to shorten the pipeline's fill
+    and drain): the K-prep and indexer of a chunk run on a higher-priority
+    stream on a share of the SMs while the attention of the previous chunk
+    runs on the rest.  The results
     equal those of prefill() on the whole sequence (the per-query computation
     does not depend on the chunking).  Device buffers are allocated once,
     here."""
 
     NAMES = ("q", "k", "v", "qi", "w", "ki")
 
-    def __init__(self, cfg: Config, L: int, chunk_tokens: int = 65536, device="cuda"):
+    def __init__(self, cfg: Config, L: int, chunk_tokens: int = 65536, device="cuda", edge_parts: int = 4):
         self.cfg, self.L, self.dev = cfg, L, device
         self.chunk = max(64, (chunk_tokens // 64) * 64)
         shapes = {"q": (L, 24, 256), "k": (L, 2, 256), "v": (L, 2, 256), "qi": (L, 4, 128), "w": (L, 4),
@@ -535,7 +537,17 @@ class HostPrefill:
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         begin, ctas = prefill_overlap_plan(cfg, L, sms)
         if len(ctas) > 1:
-            self.bounds, self.ctas = begin, ctas
+            # the first and the last chunk go in smaller parts (same indexer
+            # grid each): the first computes as soon as its part has arrived
+            # and the last part's copy back is short
+            self.bounds, self.ctas = [0], []
+            for j, (a, b) in enumerate(zip(begin[:-1], begin[1:])):
+                parts = edge_parts if j in (0, len(ctas) - 1) else 1
+                step = max(64, ((b - a) // parts) // 64 * 64)
+                cuts = [c for c in range(a + step, b, step)][: parts - 1]
+                for c in cuts + [b]:
+                    self.bounds.append(c)
+                    self.ctas.append(ctas[j])
         else:
             self.bounds = list(range(0, L, self.chunk)) + [L]
             self.ctas = None
