@@ -771,6 +771,7 @@ def main():
                      "indexer_topk_alone": idx_ms, "sparse_attn_prefill_alone": attn_ms,
                      "decode_step_after_serial_prefill": dec_serial_ms},
         "overlap": {"chunks": len(ctas), "index_ctas": ctas, "serial_prefill_ms": idx_ms + attn_ms,
+                    "stage_region_launches": 9 * K,
                     "speedup_vs_serial": (idx_ms + attn_ms) / pre_ms,
                     "stage_region": "per-stage times and kernel rooflines come from a second timed region "
                                     "of the same K steps with the stages one after the other"},

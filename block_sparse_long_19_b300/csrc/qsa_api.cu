@@ -474,8 +474,14 @@ qsa_status qsa_prefill_overlapped(const qsa_config *cfg, const qsa_bf16 *q, cons
     constexpr int kMaxChunks = 64;
     int64_t begin[kMaxChunks + 1];
     int ctas[kMaxChunks];
-    const int n = qsa_prefill_overlap_plan(cfg, L, sms, kMaxChunks, begin, ctas);
+    int n = qsa_prefill_overlap_plan(cfg, L, sms, kMaxChunks, begin, ctas);
     if (n < 1) return fail(QSA_ERR_INVALID_ARG, "no chunk plan");
+    // a stream being captured into a CUDA graph gets the serial schedule (no
+    // helper stream is created while a capture is open)
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t ce = cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cap);
+    if (ce != cudaSuccess) return cuda_fail(ce, "stream capture query");
+    if (cap != cudaStreamCaptureStatusNone) n = 1;
     if (n == 1) {  // nothing to overlap: the two stages one after the other
         st = index_common(cfg, qi, w, ki, k, k_rot, L, idx, score, nullptr, ws, ws_bytes, dev_status, stream);
         if (st != QSA_OK) return st;

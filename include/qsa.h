@@ -262,8 +262,9 @@ qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 
  * events cannot be created.
  *
  * Prefills shorter than 262,144 tokens (whose K/V mostly stays in L2, so the
- * attention is bound by its SMs, not by HBM) and budget 1 run the two stages
- * one after the other on `stream`.
+ * attention is bound by its SMs, not by HBM), budget 1, and calls on a stream
+ * that is being captured into a CUDA graph run the two stages one after the
+ * other on `stream`.
  *
  * qsa_prefill_overlap_plan: the chunking this call uses on a GPU with `sms`
  *   SMs (host only, no GPU needed).  Writes n+1 chunk starts

@@ -183,3 +183,30 @@ def test_overlapped_prefill_equals_serial_prefill(L, budget):
         check_selection(idx_g, ref["idx"], O.prefill_scores(hb, rows), rows, budget)
         att = O.prefill_rows(hb, rows, budget, idx_given=idx_g)
         check_outputs(bf16_to_f64(res.out[torch.as_tensor(rows, device=DEV)]), att["o"], "O")
+
+
+def test_overlapped_prefill_under_graph_capture():
+    """Captured into a CUDA graph, the overlapped prefill takes its serial
+    schedule on the captured stream; a replay writes the serial results."""
+    L, budget = 262144, 512
+    t = W.prefill_inputs(L, 46, DEV)
+    full = full_prefill(t, budget)
+    cfg = Q.default_config(budget=budget)
+    k_rot = torch.empty_like(t["k"])
+    idx = torch.full((L, budget), -7, dtype=torch.int32, device=DEV)
+    out = torch.zeros_like(t["q"])
+    lse = torch.zeros((L, 24), dtype=torch.float32, device=DEV)
+    ws = torch.empty(Q.prefill_overlapped_workspace_bytes(cfg, L), dtype=torch.uint8, device=DEV)
+    status = Q.new_status(DEV)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        Q.prefill_overlapped(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"], k_rot=k_rot, idx=idx,
+                             out=out, lse=lse, ws=ws, status=status)
+    g.replay()
+    torch.cuda.synchronize()
+    Q.check_status(status)
+    assert torch.equal(idx, full.idx)
+    assert torch.equal(out, full.out)
+    assert torch.equal(lse, full.lse)
