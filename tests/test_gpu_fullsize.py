@@ -35,7 +35,9 @@ def prefill_check(name, nrows, needle=False):
     L, budget, seed = spec["L"], spec["budget"], spec["seed"]
     t = W.prefill_inputs(L, seed, DEV, needle=needle)
     cfg = Q.default_config(budget=budget)
-    res = Q.prefill(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"], want_score=False)
+    # the benchmark's prefill call: at 1M the indexer of each chunk runs
+    # beside the attention of the previous one; shorter prefills run serially
+    res = Q.prefill_overlapped(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"], want_score=False)
     torch.cuda.synchronize()
     Q.check_status(res.status, name)
     rows = sample_rows(L, nrows, seed=seed)
