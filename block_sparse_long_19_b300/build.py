@@ -1,9 +1,12 @@
 """Build libqsa.so in-tree with nvcc for sm_103a (B300).
 
-    python -m block_sparse_long_19_b300.build
+    python -m block_sparse_long_19_b300.build [--debug] [--force] [-v]
 
 Each .cu under csrc/ is compiled in parallel, then linked into one shared
-library next to this file (the CUDA runtime is linked statically).
+library next to this file (the CUDA runtime is linked statically).  --debug
+builds libqsa_debug.so instead: the same kernels with QSA_DEBUG_CHECKS=1,
+which range-check the indices they are given or compute and report a
+violation in the caller's status word.
 """
 from __future__ import annotations
 
@@ -18,6 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "libqsa.so")
 OBJ_DIR = os.path.join(HERE, "_build")
+OUT_DEBUG = os.path.join(HERE, "libqsa_debug.so")
+OBJ_DIR_DEBUG = os.path.join(HERE, "_build_debug")
 
 NVCC = os.environ.get("NVCC", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -32,21 +37,24 @@ def _deps():
     return [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(INCLUDE, "qsa.h")]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(OUT):
+def up_to_date(out: str = OUT) -> bool:
+    if not os.path.exists(out):
         return False
-    t = os.path.getmtime(OUT)
+    t = os.path.getmtime(out)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    if not force and up_to_date():
-        return OUT
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    out = OUT_DEBUG if debug else OUT
+    obj_dir = OBJ_DIR_DEBUG if debug else OBJ_DIR
+    flags = FLAGS + (["-DQSA_DEBUG_CHECKS=1"] if debug else [])
+    if not force and up_to_date(out):
+        return out
+    os.makedirs(obj_dir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [NVCC, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
+        cmd = [NVCC, *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -58,14 +66,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = OUT + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, OUT)
-    return OUT
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -440,6 +440,12 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
             v[r] = e < m ? sortb[512 + e] : 0xFFFFFFFFu;
         }
         group_sort512(v, sortb, threadIdx.x, 1);
+#if QSA_DEBUG_CHECKS
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+            if (4 * threadIdx.x + r < m)
+                debug_check(p.status, v[r] < static_cast<uint64_t>(c) && (r == 0 || v[r - 1] < v[r]));
+#endif
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int e = 4 * threadIdx.x + r;

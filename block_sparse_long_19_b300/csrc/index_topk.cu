@@ -79,6 +79,7 @@ static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
 struct Params {
     int64_t L;          // end position: queries are tokens q_off .. L-1
+    int64_t unit_rows;  // rows of the unit-key tensor map (debug checks)
     int64_t q_off;      // position of the first query row (a cached prefix before it)
     int bshift;         // log2 of the tokens per selection unit: 2 (4-token blocks) or 0 (tokens)
     int nq;
@@ -469,6 +470,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (sMisc[1]) { ok = false; break; }
                     if (!mbar_wait_sleep<256>(&empty[st], ph ^ 1)) { ok = false; break; }
                     uint8_t *dst = sK + st * SK_BYTES;
+                    debug_check(p.status, static_cast<int64_t>(j) * TB < p.unit_rows);  // tile starts inside the map
                     mbar_arrive_expect_tx(&full[st], SK_BYTES);
                     tma_load_2d(dst, &map_k, &full[st], 0, j * TB);
                     tma_load_2d(dst + SK_BYTES / 2, &map_k, &full[st], 64, j * TB);
@@ -754,6 +756,14 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int r = 0; r < 4; ++r) v[r] = 4 * tg + r < m ? sort64[512 + 4 * tg + r] : ~0ull;
                         group_sort512(v, sort64, tg, bar);
+#if QSA_DEBUG_CHECKS
+                        debug_check(p.status, m == static_cast<int>(c < p.k_sel ? c : p.k_sel));
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            if (4 * tg + r < m)
+                                debug_check(p.status, (v[r] >> 32) < static_cast<uint64_t>(c) &&
+                                                          (r == 0 || (v[r - 1] >> 32) < (v[r] >> 32)));
+#endif
 #pragma unroll
                         for (int r = 0; r < 4; ++r)
                             emit(4 * tg + r, static_cast<uint32_t>(v[r] >> 32),
@@ -775,6 +785,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                         for (int r = 0; r < 4; ++r) v[r] = 4 * tg + r < m ? sort32[512 + 4 * tg + r] : 0xFFFFFFFFu;
                         group_sort512(v, sort32, tg, bar);
                         const int e0 = 4 * tg;
+#if QSA_DEBUG_CHECKS
+                        debug_check(p.status, m == static_cast<int>(c < p.k_sel ? c : p.k_sel));
+#pragma unroll
+                        for (int r = 0; r < 4; ++r)
+                            if (e0 + r < m)
+                                debug_check(p.status, v[r] < static_cast<uint64_t>(c) && (r == 0 || v[r - 1] < v[r]));
+#endif
                         if ((p.budget & 3) == 0 && e0 + 3 < m) {
                             *reinterpret_cast<int4 *>(row + e0) = make_int4(
                                 static_cast<int>(v[0]), static_cast<int>(v[1]), static_cast<int>(v[2]),
@@ -831,6 +848,7 @@ cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int
     ix::Params p;
     const int64_t L = q_off + Lq;
     p.L = L;
+    p.unit_rows = unit_tokens == 1 ? L : L / kBlock;
     p.q_off = q_off;
     p.bshift = unit_tokens == 1 ? 0 : 2;
     p.nq = static_cast<int>((Lq + ix::TQ - 1) / ix::TQ);

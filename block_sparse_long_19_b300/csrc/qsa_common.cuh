@@ -38,6 +38,24 @@ __device__ __forceinline__ void report(int32_t *status, int code) {
     if (status) atomicCAS(status, 0, code);
 }
 
+// Debug builds (libqsa_debug.so, compiled with QSA_DEBUG_CHECKS=1) check the
+// indices every kernel is given or computes -- selection rows, TMA tile
+// coordinates, emitted rows -- and report a violation as
+// QSA_ERR_DEVICE_CHECK in the caller's status word (no trap, no assert: the
+// kernel carries on and leaves normally).  In the normal build the checks
+// compile to nothing.
+#ifndef QSA_DEBUG_CHECKS
+#define QSA_DEBUG_CHECKS 0
+#endif
+__device__ __forceinline__ void debug_check(int32_t *status, bool holds) {
+#if QSA_DEBUG_CHECKS
+    if (!holds) report(status, QSA_ERR_DEVICE_CHECK);
+#else
+    (void)status;
+    (void)holds;
+#endif
+}
+
 __device__ __forceinline__ unsigned long long globaltimer() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -126,6 +126,15 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     }
     for (int i = threadIdx.x; i < a.budget; i += THREADS) {
         int b = irow[i];
+#if QSA_DEBUG_CHECKS
+        {  // a row as the indexer writes it: past blocks ascending, block c last, -1 padding
+            const int nxt = i + 1 < a.budget ? irow[i + 1] : -1;
+            bool row_ok = b >= -1 && b <= c && (i > 0 || b >= 0);
+            if (b >= 0) row_ok = row_ok && (nxt < 0 ? b == c : b < nxt);
+            else row_ok = row_ok && nxt < 0;
+            debug_check(a.status, row_ok);
+        }
+#endif
         if (b < 0 || b > c) b = -1;  // out-of-range entries are ignored
         sIdx[i] = b;
     }

@@ -10,6 +10,7 @@ Function names follow the C ABI in include/qsa.h (without the qsa_ prefix).
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from dataclasses import dataclass
@@ -18,6 +19,8 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libqsa.so")
+# the same kernels built with QSA_DEBUG_CHECKS=1 (python -m block_sparse_long_19_b300.build --debug)
+DEBUG_LIB_PATH = os.path.join(_HERE, "libqsa_debug.so")
 
 QSA_OK = 0
 QSA_ERR_TIMEOUT = 5
@@ -63,6 +66,24 @@ def load(path: str = LIB_PATH):
     global _lib
     if _lib is not None:
         return _lib
+    _lib = _open(path)
+    return _lib
+
+
+@contextlib.contextmanager
+def using_library(path: str):
+    """Route every call of this module to another build of the library (e.g.
+    DEBUG_LIB_PATH) inside the `with` block."""
+    global _lib
+    saved = _lib
+    _lib = _open(path)
+    try:
+        yield _lib
+    finally:
+        _lib = saved
+
+
+def _open(path: str):
     if not os.path.exists(path):
         raise RuntimeError(
             f"{path} is missing: build it with `python -m block_sparse_long_19_b300.build` "
@@ -119,7 +140,6 @@ def load(path: str = LIB_PATH):
     L.qsa_prefill_overlap_plan.argtypes = [cfgp, c.c_int64, c.c_int, c.c_int, c.POINTER(c.c_int64),
                                            c.POINTER(c.c_int)]
     L.qsa_prefill_overlap_plan.restype = c.c_int
-    _lib = L
     return L
 
 

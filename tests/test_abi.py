@@ -238,3 +238,16 @@ def test_overlap_plan_rejects_and_small_budget():
     assert begin == [0, 1 << 20] and ctas == [148]  # nothing to overlap without an indexer
     begin, ctas = Q.prefill_overlap_plan(cfg, 1 << 20, 148, max_chunks=3)
     assert len(ctas) <= 3 and begin[-1] == 1 << 20
+
+
+def test_debug_library_builds_and_exports_every_symbol():
+    """libqsa_debug.so (QSA_DEBUG_CHECKS=1) is the same ABI."""
+    path = B.build(debug=True)
+    assert path == Q.DEBUG_LIB_PATH
+    dbg = ctypes.CDLL(path)
+    for n in declared_functions():
+        assert hasattr(dbg, n), n
+    with Q.using_library(path) as L:
+        cfg = Q.default_config()
+        assert L.qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 1 << 16) == \
+            Q.load().qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 1 << 16)
