@@ -417,17 +417,20 @@ def run_token_level(wl: Workload, block_indexer_ms: float, reps: int = 2) -> dic
     cfg, p = wl.cfg, wl.p
     ws = torch.empty(Q.load().qsa_index_topk_tokens_workspace_bytes(ctypes.byref(cfg), wl.L),
                      dtype=torch.uint8, device=wl.dev)
-    Q.index_topk_tokens(cfg, p["qi"], p["w"], p["ki"], idx=wl.idx, ws=ws, status=wl.status, want_score=False)
+    tidx = torch.empty_like(wl.idx)  # the block-level selection in wl.idx stays for the parity check
+    Q.index_topk_tokens(cfg, p["qi"], p["w"], p["ki"], idx=tidx, ws=ws, status=wl.status, want_score=False)
     torch.cuda.synchronize()
     ts = []
     for _ in range(reps):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        Q.index_topk_tokens(cfg, p["qi"], p["w"], p["ki"], idx=wl.idx, ws=ws, status=wl.status, want_score=False)
+        Q.index_topk_tokens(cfg, p["qi"], p["w"], p["ki"], idx=tidx, ws=ws, status=wl.status, want_score=False)
         e1.record()
         torch.cuda.synchronize()
         ts.append(e0.elapsed_time(e1))
     Q.check_status(wl.status, "token-level indexer")
+    del tidx, ws
+    torch.cuda.empty_cache()
     ms = statistics.median(ts)
     pairs = float(np.sum(np.arange(wl.L, dtype=np.float64)))
     return {"ms": ms, "units": "tokens", "budget_tokens": wl.budget, "tflops": pairs * 1024 / (ms / 1e3) / 1e12,
@@ -506,9 +509,13 @@ def run_e2e(wl: Workload, steps: int) -> dict:
 
 # ---------------------------------------------------------- CPU baseline --
 
-def oracle_sample(wl_name: str, target_s: float = 12.0, host_inputs=None) -> dict:
+def oracle_sample(wl_name: str, target_s: float = 12.0, host_inputs=None, gpu=None) -> dict:
     """The oracle as it stands, on the host cores, on a bounded sample of the
-    workload's prefill query rows (all steps of the layer per row)."""
+    workload's prefill query rows (all steps of the layer per row).  With
+    `gpu` (the benchmark's idx / out / lse tensors) the sampled rows are also
+    compared with the GPU's, after the timed oracle call: a parity summary
+    under the rules of the tests (same selected set; O and LSE within
+    2e-2 + 1e-2 |ref| on that set)."""
     import oracle as O
 
     L, budget, pseed, B, T, dseed, *rest = WORKLOADS[wl_name]
@@ -550,12 +557,26 @@ def oracle_sample(wl_name: str, target_s: float = 12.0, host_inputs=None) -> dic
     rows1 = np.sort(pool[2 * n0:2 * n0 + n1])
     fill(rows1)
     t1 = time.perf_counter()
-    O.prefill_rows(hb, rows1, budget)
+    ref = O.prefill_rows(hb, rows1, budget)
     dt1 = time.perf_counter() - t1
-    return {"value": len(rows1) / dt1, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{len(rows1)} uniformly drawn query rows (positions >= {lo}) of the "
-                      f"L={L} prefill, full layer per row (scores over every past block, "
-                      f"selection, RoPE, attention), fp64, {dt1:.1f} s"}
+    res = {"value": len(rows1) / dt1, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+           "sample": f"{len(rows1)} uniformly drawn query rows (positions >= {lo}) of the "
+                     f"L={L} prefill, full layer per row (scores over every past block, "
+                     f"selection, RoPE, attention), fp64, {dt1:.1f} s"}
+    if gpu is not None:
+        ri = torch.as_tensor(rows1, device=gpu["idx"].device)
+        idx_g = gpu["idx"][ri].cpu().numpy()
+        o_g = gpu["out"][ri].double().cpu().numpy()
+        lse_g = gpu["lse"][ri].double().cpu().numpy()
+        same = np.array([set(a[a >= 0].tolist()) == set(b[b >= 0].tolist()) for a, b in zip(idx_g, ref["idx"])])
+        o_ok = np.abs(o_g - ref["o"]) <= 2e-2 + 1e-2 * np.abs(ref["o"])
+        l_ok = np.abs(lse_g - ref["lse"]) <= 2e-2 + 1e-2 * np.abs(ref["lse"])
+        ok_rows = same & o_ok.reshape(len(rows1), -1).all(axis=1) & l_ok.all(axis=1)
+        res["parity"] = {"rows": int(len(rows1)), "selection_identical_rows": int(same.sum()),
+                         "rows_within_tolerance": int(ok_rows.sum()),
+                         "o_max_abs_err": float(np.abs(o_g - ref["o"])[same].max()) if same.any() else None,
+                         "rule": "same selected set; O and LSE within 2e-2 + 1e-2 |oracle|"}
+    return res
 
 
 def run_reference(args):
@@ -815,7 +836,8 @@ def main():
             line["e2e"] = {"value": None, "unit": "tokens/s", "error": str(ex)[:200]}
     if rank == 0 and not args.no_cpu_baseline:
         try:
-            line["cpu_baseline"] = oracle_sample(args.workload, host_inputs=wl.p)
+            line["cpu_baseline"] = oracle_sample(args.workload, host_inputs=wl.p,
+                                                 gpu={"idx": wl.idx, "out": wl.out, "lse": wl.lse})
         except Exception as ex:
             line["cpu_baseline"] = {"value": None, "error": str(ex)[:200]}
     if rank == 0:
