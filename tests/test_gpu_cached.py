@@ -152,20 +152,23 @@ def test_host_prefill_pipeline_equals_device_prefill(L, chunk):
     assert torch.equal(hp.idx, full.idx)
 
 
-@pytest.mark.parametrize("L,budget", [
-    (266277, 512),  # 16 chunks, the last one ragged
-    (262144, 32),   # 16 chunks, small budget
-    (70001, 512),   # short: the two stages one after the other
-    (65536, 1),     # no indexer work: the current block only
+@pytest.mark.parametrize("L,budget,yarn", [
+    (266277, 512, 1.0),  # 16 chunks, the last one ragged
+    (262144, 32, 1.0),   # 16 chunks, small budget
+    (262144, 512, 4.0),  # 16 chunks, YaRN on (the model card's factor 4)
+    (70001, 512, 1.0),   # short: the two stages one after the other
+    (65536, 1, 1.0),     # no indexer work: the current block only
 ])
-def test_overlapped_prefill_equals_serial_prefill(L, budget):
+def test_overlapped_prefill_equals_serial_prefill(L, budget, yarn):
     """qsa_prefill_overlapped (the indexer of chunk j beside the attention of
     chunk j-1, on two streams) writes exactly what the serial prefill writes:
     selection, scores, RoPE'd keys, output and LSE; sampled rows of the last
     chunk also against the oracle."""
     t = W.prefill_inputs(L, 45, DEV)
-    full = full_prefill(t, budget)
-    cfg = Q.default_config(budget=budget)
+    cfg = Q.default_config(budget=budget, yarn_factor=yarn)
+    full = Q.prefill(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"], want_score=True)
+    torch.cuda.synchronize()
+    Q.check_status(full.status)
     res = Q.prefill_overlapped(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"], want_score=True)
     torch.cuda.synchronize()
     Q.check_status(res.status)
@@ -181,7 +184,7 @@ def test_overlapped_prefill_equals_serial_prefill(L, budget):
         idx_g = res.idx.cpu().numpy()[rows]
         ref = O.prefill_rows(hb, rows, budget, want_o=False)
         check_selection(idx_g, ref["idx"], O.prefill_scores(hb, rows), rows, budget)
-        att = O.prefill_rows(hb, rows, budget, idx_given=idx_g)
+        att = O.prefill_rows(hb, rows, budget, idx_given=idx_g, yarn=O.YARN_CARD if yarn > 1 else None)
         check_outputs(bf16_to_f64(res.out[torch.as_tensor(rows, device=DEV)]), att["o"], "O")
 
 
