@@ -1,8 +1,8 @@
 """The checked build, libqsa_debug.so (the same kernels compiled with
 QSA_DEBUG_CHECKS=1).  Its kernels range-check the selection rows they are
 given or write and the TMA tile coordinates they compute, and report a
-violation as QSA_ERR_DEVICE_CHECK in the status word.  It stands in for a
-memory checker on this GPU pool.
+violation as QSA_ERR_DEVICE_CHECK in the status word, in place of a memory
+checker.
 
 * On valid inputs it reports nothing and writes exactly what the normal
   build writes.
