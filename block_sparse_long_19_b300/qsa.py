@@ -524,6 +524,23 @@ def prefill_overlapped(cfg: Config, q, k, v, qi, w, ki, k_rot=None, idx=None, sc
     return PrefillResult(idx, score, k_rot, out, lse, status)
 
 
+def split_edge_chunks(begin, ctas, parts: int = 4):
+    """Chunk starts and indexer grids of prefill_overlap_plan() with the first
+    and the last chunk split into `parts` parts on 64-row tiles (each part
+    keeps its chunk's indexer grid): HostPrefill's first part computes as soon
+    as it has arrived, and its last part's copy back is short.  Returns
+    (bounds, ctas) with len(bounds) == len(ctas) + 1."""
+    bounds, out = [0], []
+    for j, (a, b) in enumerate(zip(begin[:-1], begin[1:])):
+        n = parts if j in (0, len(ctas) - 1) else 1
+        step = max(64, ((b - a) // n) // 64 * 64)
+        cuts = [c for c in range(a + step, b, step)][: n - 1]
+        for c in cuts + [b]:
+            bounds.append(c)
+            out.append(ctas[j])
+    return bounds, out
+
+
 class HostPrefill:
     """Prefill of one sequence whose inputs live in pinned host memory.
 
@@ -557,17 +574,7 @@ class HostPrefill:
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         begin, ctas = prefill_overlap_plan(cfg, L, sms)
         if len(ctas) > 1:
-            # the first and the last chunk go in smaller parts (same indexer
-            # grid each): the first computes as soon as its part has arrived
-            # and the last part's copy back is short
-            self.bounds, self.ctas = [0], []
-            for j, (a, b) in enumerate(zip(begin[:-1], begin[1:])):
-                parts = edge_parts if j in (0, len(ctas) - 1) else 1
-                step = max(64, ((b - a) // parts) // 64 * 64)
-                cuts = [c for c in range(a + step, b, step)][: parts - 1]
-                for c in cuts + [b]:
-                    self.bounds.append(c)
-                    self.ctas.append(ctas[j])
+            self.bounds, self.ctas = split_edge_chunks(begin, ctas, edge_parts)
         else:
             self.bounds = list(range(0, L, self.chunk)) + [L]
             self.ctas = None

@@ -251,3 +251,21 @@ def test_debug_library_builds_and_exports_every_symbol():
         cfg = Q.default_config()
         assert L.qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 1 << 16) == \
             Q.load().qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 1 << 16)
+
+
+@pytest.mark.parametrize("L", [262144, 266277, 1 << 20, 3_000_001])
+def test_host_prefill_edge_split(L):
+    """HostPrefill's chunks: the overlap plan's, with the first and last chunk
+    in parts on 64-row tiles that keep their chunk's indexer grid."""
+    cfg = Q.default_config()
+    begin, ctas = Q.prefill_overlap_plan(cfg, L, 148)
+    bounds, parts = Q.split_edge_chunks(begin, ctas, 4)
+    assert len(bounds) == len(parts) + 1
+    assert bounds[0] == 0 and bounds[-1] == L
+    assert all(a < b for a, b in zip(bounds[:-1], bounds[1:]))
+    assert all(b % 64 == 0 for b in bounds[1:-1])
+    assert set(begin) <= set(bounds)          # every chunk start is kept
+    assert len(parts) == len(ctas) + 6       # 3 extra parts at each end
+    for a, b, x in zip(bounds[:-1], bounds[1:], parts):
+        j = max(i for i in range(len(ctas)) if begin[i] <= a)
+        assert b <= begin[j + 1] and x == ctas[j]
