@@ -322,7 +322,8 @@ qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf
  *     present on every GPU that loads the library until it is unloaded.
  *     batch x max_ctx combinations whose workspace
  *     (qsa_decode_workspace_bytes) exceeds it return QSA_ERR_UNSUPPORTED and
- *     launch nothing (8 x 1,048,576 and 64 x 262,144 fit).
+ *     launch nothing (8 x 1,048,576 fits, 12.1 MB; 64 x 262,144, 24.3 MB,
+ *     does not).
  *   - The first call on each device (that device current) resolves the
  *     array's device address; make that first call before any stream
  *     capture.
