@@ -34,6 +34,8 @@
  *     other than a cached per-device property query and a resolved driver
  *     entry point (qsa_sparse_attn_decode_noalloc, at the end, is the one
  *     call that uses a built-in scratch array instead of a workspace).
+ *   - Calls run on the current CUDA device: `stream` and every pointer must
+ *     belong to it.
  *   - Calls only enqueue work on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and return without synchronising.  One call,
  *     qsa_prefill_overlapped, also forks a helper stream and events of its
