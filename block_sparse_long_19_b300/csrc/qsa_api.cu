@@ -707,6 +707,9 @@ qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf
     REQ_PTR(dev_status);
     const int sms = sm_count();
     const size_t need = qsa::decode_ws_bytes(batch, max_ctx, cfg->budget_blocks, sms);
+    // the workspace is checked after every other argument:
+    // qsa_sparse_attn_decode_noalloc relies on this order to report argument
+    // errors with the statuses of this call
     if (!ws || ws_bytes < need)
         return fail(QSA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, ws_bytes);
     if (!aligned16(ws)) return fail(QSA_ERR_INVALID_ARG, "ws is not 16-byte aligned");

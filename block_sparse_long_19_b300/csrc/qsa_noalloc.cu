@@ -12,10 +12,13 @@
 // scratch area that lives in this file as a statically sized device array:
 //   * the array (kNoAllocScratchBytes = 16 MiB) exists on every GPU that
 //     loads this library, for as long as the library stays loaded;
-//   * host code cannot use the array's name as a device address, so the
-//     first call on each device (with that device current) looks up the
-//     array's address with cudaGetSymbolAddress and caches it; make that
-//     first call before any stream capture;
+//   * host code cannot use the array's name as a device address, so every
+//     call looks the address up with cudaGetSymbolAddress in the current
+//     context (a lookup, not an allocation).  Nothing is cached: after a
+//     cudaDeviceReset, or with a non-primary context current, the next call
+//     finds the array where that context has it.  The first call in a
+//     context may load the library's device code there, so make it before
+//     any stream capture;
 //   * every call shares the one array and finds the previous call's data in
 //     it.  Nothing in it has to start at zero: each region the decode kernels
 //     read is written earlier in the same call.  Two calls whose work
@@ -24,8 +27,6 @@
 //   * sizes whose workspace would not fit are rejected with
 //     QSA_ERR_UNSUPPORTED before anything is launched;
 //   * nothing here calls cudaMalloc, cudaFree or any allocating routine.
-#include <mutex>
-
 #include "qsa_common.cuh"
 #include "qsa_kernels.h"
 
@@ -36,31 +37,15 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) uint8_t g_decode_scratch[kNoAllocScratchBytes];
 
 namespace {
-std::mutex g_scratch_mu;
-void *g_scratch_addr[64] = {};  // device address of g_decode_scratch, per device
-
+// The device address of g_decode_scratch in the current context.
 qsa_status scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) {
-        qsa::set_error_detail("cudaGetDevice failed");
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+        qsa::set_error_detail("cudaGetSymbolAddress of the decode scratch array failed");
         return QSA_ERR_CUDA;
     }
-    if (dev < 0 || dev >= 64) {
-        qsa::set_error_detail("device ordinal out of range");
-        return QSA_ERR_UNSUPPORTED;
-    }
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_decode_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            qsa::set_error_detail("cudaGetSymbolAddress of the decode scratch array failed");
-            return QSA_ERR_CUDA;
-        }
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return QSA_OK;
 }
 }  // namespace
@@ -70,6 +55,14 @@ extern "C" qsa_status qsa_sparse_attn_decode_noalloc(
     const qsa_bf16 *k_cache, const qsa_bf16 *v_cache, const qsa_bf16 *kblk_cache, int64_t max_ctx,
     const int32_t *seq_lens, qsa_bf16 *out, float *lse, int32_t *idx_out, int32_t *dev_status,
     void *stream) {
+    // Validate every argument first, exactly as the decode with a workspace
+    // does: given no workspace it returns the first argument error, or
+    // QSA_ERR_WORKSPACE once every other argument is valid (its workspace
+    // check comes last), and launches nothing either way.
+    const qsa_status arg = qsa_sparse_attn_decode(cfg, batch, q, qi, w, k_cache, v_cache, kblk_cache,
+                                                  max_ctx, seq_lens, out, lse, idx_out, nullptr, 0,
+                                                  dev_status, stream);
+    if (arg != QSA_ERR_WORKSPACE) return arg == QSA_OK ? QSA_ERR_INVALID_ARG : arg;
     const size_t need = qsa_decode_workspace_bytes(cfg, batch, max_ctx);
     if (need > kNoAllocScratchBytes) {
         qsa::set_error_detail(
@@ -78,12 +71,9 @@ extern "C" qsa_status qsa_sparse_attn_decode_noalloc(
         return QSA_ERR_UNSUPPORTED;
     }
     void *scratch = nullptr;
-    if (need > 0) {
-        const qsa_status st = scratch_address(&scratch);
-        if (st != QSA_OK) return st;
-    }
-    // need == 0 means the arguments are invalid: the call below reports why
+    const qsa_status st = scratch_address(&scratch);
+    if (st != QSA_OK) return st;
     return qsa_sparse_attn_decode(cfg, batch, q, qi, w, k_cache, v_cache, kblk_cache, max_ctx,
-                                  seq_lens, out, lse, idx_out, scratch,
-                                  scratch ? kNoAllocScratchBytes : 0, dev_status, stream);
+                                  seq_lens, out, lse, idx_out, scratch, kNoAllocScratchBytes,
+                                  dev_status, stream);
 }

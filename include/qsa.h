@@ -326,9 +326,14 @@ qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf
  *     (qsa_decode_workspace_bytes) exceeds it return QSA_ERR_UNSUPPORTED and
  *     launch nothing (8 x 1,048,576 fits, 12.1 MB; 64 x 262,144, 24.3 MB,
  *     does not).
- *   - The first call on each device (that device current) resolves the
- *     array's device address; make that first call before any stream
- *     capture.
+ *   - Every call looks up the array's device address in the current
+ *     context (cudaGetSymbolAddress: a lookup, not an allocation), so a
+ *     cudaDeviceReset or a non-primary context is followed correctly.  The
+ *     first call in a context may load the library's device code there:
+ *     make it before any stream capture.
+ *   - Arguments are checked as qsa_sparse_attn_decode checks them, with
+ *     the same statuses (batch < 1: QSA_ERR_INVALID_ARG; max_ctx beyond
+ *     3,080,192: QSA_ERR_UNSUPPORTED).
  *   - All calls share the array: calls whose GPU work overlaps (other
  *     streams, unordered host threads) race.  Nothing in it needs zeroing.
  *   - Allocates nothing (no cudaMalloc, cudaFree or allocating library call).

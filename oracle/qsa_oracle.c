@@ -50,7 +50,20 @@
  *       no RoPE;
  *   R6  attention over keys j with floor(j/4) selected and j <= t; query head
  *       h reads KV head floor(h/12); softmax scale 1/sqrt(256) unless given;
- *       everything after the bf16 inputs is kept in fp64.
+ *       everything after the bf16 inputs is kept in fp64;
+ *   R7  with YaRN on, the temperature multiplies the whole attention logit
+ *       (all 256 dims), as [YaRN] defines it: a temperature on the softmax of
+ *       q.k.  Implementations written for fully rotary models fold
+ *       sqrt(1/t) into the cos/sin tables, which here, with only 64 of 256
+ *       dims rotary, would scale the rotary part of the logit alone; the
+ *       method's definition is followed rather than that folding.
+ *
+ * Parity unpinned: qo_yarn_logit_factor.  Its constant (0.1 ln s + 1,
+ * squared) is [YaRN]'s recommended fit; the pages print no value of it, and
+ * no property of the method fixes it, so the tests pin only how it is used
+ * (the temperature scales the logits and nothing else), not its value.
+ * Every other function here is pinned by the tests against closed forms,
+ * invariants, library routines or brute force.
  *
  * All tensors are row-major, bf16 passed as raw uint16 bit patterns.
  */
@@ -143,7 +156,8 @@ void qo_rope_inv_freq(double theta, double s, double l_orig, double alpha, doubl
 }
 
 /* [YaRN]: the factor the attention logits are multiplied by, (0.1 ln s + 1)^2
- * (both query and key carry sqrt(1/t)); 1 without YaRN. */
+ * (both query and key carry sqrt(1/t)); 1 without YaRN.  Parity unpinned:
+ * the constant is the method's fitted value, printed on none of the pages. */
 double qo_yarn_logit_factor(double s)
 {
     if (s <= 1.0) return 1.0;

@@ -87,3 +87,19 @@ def sample_rows(L: int, n: int, seed: int = 0, extra=()) -> np.ndarray:
     base |= set(int(x) for x in extra if 0 <= x < L)
     base |= set(int(x) for x in rng.integers(0, L, size=n))
     return np.array(sorted(base), dtype=np.int64)
+
+
+def check_rope(got_bits, ref_bits, x_bits):
+    """RoPE'd keys: the GPU rotates in fp32 (angle reduced in fp64), the
+    oracle in fp64, both then round to bf16.  Allowed: one bf16 ulp of the
+    result (2^-7 relative) plus the fp32 rounding error of the rotation, which
+    dominates when x1 cos a and x2 sin a nearly cancel."""
+    g = \
+        torch.from_numpy(got_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
+    r = torch.from_numpy(ref_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
+    x = torch.from_numpy(x_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
+    mag = np.abs(x[..., :32]) + np.abs(x[..., 32:])
+    mag = np.concatenate([mag, mag], axis=-1)
+    bound = 2.0 ** -7 * np.abs(r) + 2.0 ** -20 * mag
+    assert np.all(np.abs(g - r) <= bound), float(np.max(np.abs(g - r) - bound))
+    assert np.mean(got_bits[..., :64] != ref_bits[..., :64]) < 1e-3

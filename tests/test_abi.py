@@ -47,8 +47,28 @@ def test_default_config(lib):
 
 
 P = ctypes.c_void_p
-A = P(0x10000)   # aligned, never dereferenced on the rejected paths
-MIS = P(0x10008)  # 8-byte aligned only
+
+
+def _pointers():
+    """The pointers the rejected calls below are given.  Nothing is launched
+    on these paths, but where a GPU is present they still point at a real
+    device buffer (64 MiB, covering every size the calls name up to the
+    ones that are rejected for size), so that a validation step that ever
+    moved behind a launch could not make a kernel read a made-up address.
+    Without a GPU nothing can be launched at all, and any aligned value
+    serves."""
+    try:
+        import torch
+
+        if torch.cuda.is_available():
+            buf = torch.empty(64 << 20, dtype=torch.uint8, device="cuda")
+            return buf, P(buf.data_ptr()), P(buf.data_ptr() + 8)
+    except Exception:  # pragma: no cover
+        pass
+    return None, P(0x10000), P(0x10008)
+
+
+_BUF, A, MIS = _pointers()  # A 256-byte aligned; MIS 8-byte aligned only
 
 
 def call_topk(lib, cfg, L=64, qi=A, w=A, ki=A, k=None, k_rot=None, idx=A, score=None, ws=A,
@@ -76,7 +96,7 @@ def test_index_topk_rejects(lib):
     assert call_topk(lib, bad) == 2
     bad = Q.default_config(rope_theta=-1.0)
     assert call_topk(lib, bad) == 1
-    assert b"workspace" in lib.qsa_last_error_detail() or True
+    assert b"rope_theta" in lib.qsa_last_error_detail()
 
 
 def test_workspace_sizes(lib):
@@ -112,6 +132,34 @@ def test_decode_rejects(lib):
     assert call(max_ctx=1 << 23) == 2
     assert call(sl=None) == 1
     assert call(ws_bytes=64) == 3
+    assert call(kb=MIS) == 1
+
+
+def test_decode_noalloc_rejects(lib):
+    """The decode without a workspace argument reports argument errors with
+    the statuses of the decode with one, and refuses sizes whose workspace
+    exceeds its built-in scratch; nothing is launched on these paths."""
+    cfg = Q.default_config()
+    f = lib.qsa_sparse_attn_decode_noalloc
+
+    def call(batch=2, max_ctx=1024, cfgp=ctypes.byref(cfg), **kw):
+        a = dict(q=A, qi=A, w=A, kc=A, vc=A, kb=A, sl=A, out=A, lse=None, idx=None, st=A)
+        a.update(kw)
+        return f(cfgp, batch, a["q"], a["qi"], a["w"], a["kc"], a["vc"], a["kb"], max_ctx, a["sl"], a["out"],
+                 a["lse"], a["idx"], a["st"], None)
+
+    assert call(batch=0) == 1
+    assert call(batch=-3) == 1
+    assert call(max_ctx=0) == 1
+    assert call(max_ctx=3_080_192 + 4) == 2
+    assert call(cfgp=None) == 1
+    bad = Q.default_config()
+    bad.head_dim = 128
+    assert call(cfgp=ctypes.byref(bad)) == 2
+    assert call(batch=256, max_ctx=1 << 20) == 2  # workspace beyond the 16 MiB scratch
+    assert b"16 MiB" in lib.qsa_last_error_detail()
+    assert call(max_ctx=1022) == 1
+    assert call(sl=None) == 1
     assert call(kb=MIS) == 1
 
 

@@ -1,7 +1,8 @@
-"""Parity at the full workload sizes (32K, 128K + needles, 64 x 256K decode,
-1M prefill, 8 x 1M decode), run in the launch configuration the benchmark
-times, checked against the oracle on sampled query rows / sequences that
-the oracle computes one by one.  Rules are in tests/parity.py."""
+"""Parity at the full workload sizes (512 tokens at budget 32, 32K, 128K with
+and without needles, 64 x 256K decode, 1M prefill, 8 x 1M decode), run in
+the launch configuration the benchmark times, checked against the oracle on
+sampled query rows / sequences that the oracle computes one by one (every
+row at 512 tokens).  Rules are in tests/parity.py."""
 import numpy as np
 import pytest
 import torch
@@ -10,7 +11,7 @@ import oracle as O
 from block_sparse_long_19_b300 import qsa as Q
 from block_sparse_long_19_b300 import workloads as W
 
-from .parity import bf16_to_f64, check_outputs, check_selection, sample_rows
+from .parity import bf16_to_f64, check_outputs, check_rope, check_selection, sample_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -30,7 +31,18 @@ def host_for_rows(t, rows):
     return hb
 
 
-def prefill_check(name, nrows, needle=False):
+def check_k_rot_tail(t, res, n):
+    """RoPE'd keys of the last n positions (the largest angles of the
+    workload) against the oracle's rotation, row by row."""
+    L = t["k"].shape[0]
+    raw = W.to_bits(t["k"][L - n:])
+    got = W.to_bits(res.k_rot[L - n:])
+    ref = np.stack([np.stack([O.rope_row_bf16(raw[i, g], L - n + i) for g in range(2)]) for i in range(n)])
+    assert np.array_equal(got[:, :, 64:], raw[:, :, 64:])
+    check_rope(got, ref, raw)
+
+
+def prefill_check(name, nrows, needle=False, all_rows=False, k_rot_tail=0):
     spec = W.WORKLOADS[name]
     L, budget, seed = spec["L"], spec["budget"], spec["seed"]
     t = W.prefill_inputs(L, seed, DEV, needle=needle)
@@ -40,7 +52,9 @@ def prefill_check(name, nrows, needle=False):
     res = Q.prefill_overlapped(cfg, t["q"], t["k"], t["v"], t["qi"], t["w"], t["ki"], want_score=False)
     torch.cuda.synchronize()
     Q.check_status(res.status, name)
-    rows = sample_rows(L, nrows, seed=seed)
+    if k_rot_tail:
+        check_k_rot_tail(t, res, k_rot_tail)
+    rows = np.arange(L, dtype=np.int64) if all_rows else sample_rows(L, nrows, seed=seed)
     hb = host_for_rows(t, rows)
     idx_gpu = res.idx[torch.as_tensor(rows, device=DEV)].cpu().numpy()
     ref = O.prefill_rows(hb, rows, budget, want_o=False)
@@ -53,8 +67,18 @@ def prefill_check(name, nrows, needle=False):
     return t, res
 
 
+def test_prefill_512_every_row():
+    """512 tokens at budget 32 from seed 0, every query row."""
+    prefill_check("prefill_512", 0, all_rows=True, k_rot_tail=512)
+
+
 def test_prefill_32k():
     prefill_check("prefill_32k", 64)
+
+
+def test_prefill_128k_plain():
+    """The 128K input without planted blocks (i.i.d. draws only)."""
+    prefill_check("prefill_128k", 32)
 
 
 def test_prefill_128k_with_needles():
@@ -70,10 +94,10 @@ def test_prefill_128k_with_needles():
 
 
 def test_prefill_1m():
-    prefill_check("prefill_1m", 12)
+    prefill_check("prefill_1m", 12, k_rot_tail=2048)
 
 
-def decode_check(name, nseq):
+def decode_check(name, nseq, noalloc=False):
     spec = W.WORKLOADS[name]
     B, T, budget, seed = spec["B"], spec["T"], spec["budget"], spec["seed"]
     d = W.decode_inputs(B, T, seed, DEV)
@@ -89,6 +113,14 @@ def decode_check(name, nseq):
                                              d["seq_lens"])
     torch.cuda.synchronize()
     Q.check_status(st, name)
+    if noalloc:
+        # the same step through the entry point that uses the library's
+        # built-in scratch array: the same kernels, so the same bits
+        o2, l2, i2, st2 = Q.sparse_attn_decode_noalloc(cfg, d["q"], d["qi"], d["w"], d["k"], d["v"], kblk,
+                                                       d["seq_lens"])
+        torch.cuda.synchronize()
+        Q.check_status(st2, name + " (no-alloc)")
+        assert torch.equal(i2, idx) and torch.equal(o2, out) and torch.equal(l2, lse)
     for j, s in enumerate(seqs):
         one = {
             "q": W.to_bits(d["q"][s:s + 1]), "qi": W.to_bits(d["qi"][s:s + 1]),
@@ -112,4 +144,4 @@ def test_decode_64x256k():
 
 
 def test_decode_8x1m():
-    decode_check("decode_8x1m", 2)
+    decode_check("decode_8x1m", 2, noalloc=True)

@@ -8,8 +8,8 @@ import oracle as O
 from block_sparse_long_19_b300 import qsa as Q
 from block_sparse_long_19_b300 import workloads as W
 
-from .parity import (bf16_to_f64, check_outputs, check_row_format, check_scores, check_selection,
-                     sample_rows)
+from .parity import (bf16_to_f64, check_outputs, check_rope, check_row_format, check_scores,
+                     check_selection, sample_rows)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -36,22 +36,6 @@ def oracle_compare_prefill(t, hb, res, rows, budget, check_attn=True):
 
 
 # ------------------------------------------------------------------ K-prep --
-
-def check_rope(got_bits, ref_bits, x_bits):
-    """RoPE'd keys: the GPU rotates in fp32 (angle reduced in fp64), the
-    oracle in fp64, both then round to bf16.  Allowed: one bf16 ulp of the
-    result (2^-7 relative) plus the fp32 rounding error of the rotation, which
-    dominates when x1 cos a and x2 sin a nearly cancel."""
-    g = \
-        torch.from_numpy(got_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
-    r = torch.from_numpy(ref_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
-    x = torch.from_numpy(x_bits[..., :64].astype(np.int32) << 16).view(torch.float32).double().numpy()
-    mag = np.abs(x[..., :32]) + np.abs(x[..., 32:])
-    mag = np.concatenate([mag, mag], axis=-1)
-    bound = 2.0 ** -7 * np.abs(r) + 2.0 ** -20 * mag
-    assert np.all(np.abs(g - r) <= bound), float(np.max(np.abs(g - r) - bound))
-    assert np.mean(got_bits[..., :64] != ref_bits[..., :64]) < 1e-3
-
 
 @pytest.mark.parametrize("L", [5, 1003, 4096])
 def test_kprep_block_keys_bit_exact_and_rope(L):
