@@ -4,6 +4,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -83,6 +84,55 @@ qsa_status make_map(CUtensorMap *m, const void *base, uint64_t inner, uint64_t r
                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return QSA_OK;
+}
+
+// 5-D bf16 map of K' or V laid out [nseq][rows][2 heads][256 dims]: dims
+// {64 dims, rows, 2 heads, 4 dim chunks, nseq} (strides 1024, 512, 128,
+// rows * 1024 bytes), box {64, 4, 2, 4, 1} = one 4-token block of both heads,
+// dim chunk outermost, 128-byte swizzle; rows past the end read as zeros.
+qsa_status make_kv_map(CUtensorMap *m, const void *base, uint64_t rows, uint64_t nseq) {
+    auto fn = encode_fn();
+    if (!fn) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    cuuint64_t dims[5] = {64, rows, 2, 4, nseq};
+    cuuint64_t strides[4] = {1024, 512, 128, rows * 1024};
+    cuuint32_t box[5] = {64, 4, 2, 4, 1};
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(QSA_ERR_CUDA, "cuTensorMapEncodeTiled (K/V) failed (%d)", static_cast<int>(r));
+    return QSA_OK;
+}
+
+// Which attention kernel runs: the warp-MMA kernel (default: the faster of
+// the two as measured) or, with the environment variable
+// QSA_ATTENTION_KERNEL=tc set when the library is first used, the tcgen05
+// kernel (sparse_attn_tc.cu).  Both compute the same attention.
+bool use_tc_attention() {
+    static const bool tc = [] {
+        const char *v = std::getenv("QSA_ATTENTION_KERNEL");
+        return v && std::strcmp(v, "tc") == 0;
+    }();
+    return tc;
+}
+
+// Prefill attention of a.L query rows at positions a.q_off.., keys from the
+// first key_rows rows of a.k / a.v.
+qsa_status attention_prefill(const qsa::AttnArgs &a, const qsa::RopeFreqs &freqs, int64_t key_rows,
+                             cudaStream_t s) {
+    cudaError_t e;
+    if (use_tc_attention()) {
+        CUtensorMap mk, mv;
+        qsa_status st = make_kv_map(&mk, a.k, static_cast<uint64_t>(key_rows), 1);
+        if (st != QSA_OK) return st;
+        st = make_kv_map(&mv, a.v, static_cast<uint64_t>(key_rows), 1);
+        if (st != QSA_OK) return st;
+        e = qsa::launch_attn_prefill_tc(a, freqs, mk, mv, key_rows, s);
+    } else {
+        e = qsa::launch_attn_prefill(a, freqs, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
     return QSA_OK;
 }
 
@@ -384,8 +434,8 @@ qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 
     a.nsplit = 1;
     a.scale_log2 = scale_log2_of(cfg);
     a.status = dev_status;
-    cudaError_t e = qsa::launch_attn_prefill(a, freqs_of(cfg), static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "attention launch");
+    st = attention_prefill(a, freqs_of(cfg), q_offset + Lq, static_cast<cudaStream_t>(stream));
+    if (st != QSA_OK) return st;
     return ok();
 }
 
@@ -553,8 +603,8 @@ qsa_status qsa_prefill_overlapped(const qsa_config *cfg, const qsa_bf16 *q, cons
             a.nsplit = 1;
             a.scale_log2 = scale_log2_of(cfg);
             a.status = dev_status;
-            e2 = qsa::launch_attn_prefill(a, freqs, s);
-            if (e2 != cudaSuccess) return cuda_fail(e2, "attention launch");
+            qsa_status st3 = attention_prefill(a, freqs, L, s);
+            if (st3 != QSA_OK) return st3;
         }
         return QSA_OK;
     };
@@ -748,7 +798,16 @@ qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf
     a.nsplit = plan.nsplit;
     a.scale_log2 = scale_log2_of(cfg);
     a.status = dev_status;
-    e = qsa::launch_attn_decode(a, batch, freqs_of(cfg), s);
+    if (use_tc_attention()) {
+        CUtensorMap mk, mv;
+        qsa_status st2 = make_kv_map(&mk, k_cache, static_cast<uint64_t>(max_ctx), static_cast<uint64_t>(batch));
+        if (st2 != QSA_OK) return st2;
+        st2 = make_kv_map(&mv, v_cache, static_cast<uint64_t>(max_ctx), static_cast<uint64_t>(batch));
+        if (st2 != QSA_OK) return st2;
+        e = qsa::launch_attn_decode_tc(a, batch, freqs_of(cfg), mk, mv, s);
+    } else {
+        e = qsa::launch_attn_decode(a, batch, freqs_of(cfg), s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "decode attention launch");
     if (plan.nsplit > 1) {
         e = qsa::launch_attn_combine(part_o, part_lse, batch, plan.nsplit, out, lse, s);

@@ -58,6 +58,15 @@ cudaError_t launch_attn_decode(const AttnArgs &a, int batch, const RopeFreqs &f,
                                cudaStream_t stream);
 cudaError_t launch_attn_combine(const float *part_o, const float *part_lse, int batch,
                                 int nsplit, uint16_t *out, float *lse, cudaStream_t stream);
+// The same attention on the tcgen05 tensor cores (sparse_attn_tc.cu).  map_k
+// and map_v are 5-D maps {64 dims, rows per sequence, 2 KV heads, 4 dim
+// chunks, sequences} of K' and V with boxes {64, 4, 2, 4, 1} (one block,
+// 128-byte swizzle); key_rows = rows per sequence (the coordinate of an
+// unused slot, read as zeros).
+cudaError_t launch_attn_prefill_tc(const AttnArgs &a, const RopeFreqs &f, const CUtensorMap &map_k,
+                                   const CUtensorMap &map_v, int64_t key_rows, cudaStream_t stream);
+cudaError_t launch_attn_decode_tc(const AttnArgs &a, int batch, const RopeFreqs &f, const CUtensorMap &map_k,
+                                  const CUtensorMap &map_v, cudaStream_t stream);
 
 // ---- decode indexer ----
 struct DecodePlan {
