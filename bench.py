@@ -297,6 +297,115 @@ def run_decode_stream(wl: Workload, steps: int = 20) -> dict:
     return {"steps": steps, "mode": mode, "us_per_step": us, "gb_per_s": wl.decode_bytes() / (us / 1e6) / 1e9}
 
 
+# ----------------------------------------------------- per config --
+
+def _timed_ms(fn, reps: int, warmup: int = 1) -> float:
+    """Mean device time of fn() over reps calls (CUDA events on the current
+    stream, after warm-up, synchronised on both sides)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in evs:
+        a.record()
+        fn()
+        b.record()
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in evs)
+
+
+def _attn_bytes(L: int, budget: int) -> int:
+    t = np.arange(L, dtype=np.int64)
+    keys = np.minimum(t // 4, budget - 1) * 4 + (t % 4) + 1
+    return int((keys * 2048).sum() + L * (2 * 24 * 256 * 2 + budget * 4 + 24 * 4))
+
+
+def _prefill_config(dev, L, seed, hbm, locality=0, reps=3) -> dict:
+    """One prefill workload measured the way the main step runs it (the
+    whole layer through qsa_prefill_overlapped) and stage by stage."""
+    cfg = Q.default_config(budget=512)
+    p = W.prefill_inputs(L, seed, dev, locality=locality)
+    k_rot = torch.empty_like(p["k"])
+    idx = torch.empty((L, 512), dtype=torch.int32, device=dev)
+    out = torch.empty((L, 24, 256), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((L, 24), dtype=torch.float32, device=dev)
+    ws = torch.empty(Q.index_topk_workspace_bytes(cfg, L), dtype=torch.uint8, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    whole = _timed_ms(lambda: Q.prefill_overlapped(cfg, p["q"], p["k"], p["v"], p["qi"], p["w"], p["ki"], k_rot=k_rot,
+                                                   idx=idx, out=out, lse=lse, ws=ws, status=st), reps)
+    ix = _timed_ms(lambda: Q.index_topk(cfg, p["qi"], p["w"], p["ki"], k=p["k"], k_rot=k_rot, idx=idx, score=None,
+                                        ws=ws, status=st, want_score=False), reps)
+    at = _timed_ms(lambda: Q.sparse_attn_prefill(cfg, p["q"], k_rot, p["v"], idx, out=out, lse=lse, status=st), reps)
+    torch.cuda.synchronize()
+    Q.check_status(st, f"prefill {L}")
+    gbs = _attn_bytes(L, 512) / (at / 1e3) / 1e9
+    t = np.arange(L, dtype=np.int64)
+    idx_tflops = float((t // 4).sum() * 1024) / (ix / 1e3) / 1e12
+    r = {"L": L, "seed": seed, "ms": whole, "tokens_per_s": L / (whole / 1e3), "indexer_ms": ix,
+         "indexer_tflops": idx_tflops, "attn_ms": at, "attn_gbs": gbs, "attn_frac_hbm": gbs / hbm,
+         "attn_over_whole": at / whole}
+    if locality:
+        r["topic_segment_tokens"] = locality
+    return r
+
+
+def _decode_config(dev, B, T, seed, hbm, reps=5) -> dict:
+    """One decode workload: a single step (device time of one call) and
+    steps back to back as replays of one CUDA graph of the step."""
+    cfg = Q.default_config(budget=512)
+    d = W.decode_inputs(B, T, seed, dev)
+    kblk, _ = Q.kprep(cfg, d["ki"], d["k"], k_rot=d["k"])
+    del d["ki"]
+    ws = torch.empty(Q.decode_workspace_bytes(cfg, B, T), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, 24, 256), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, 24), dtype=torch.float32, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def one():
+        Q.sparse_attn_decode(cfg, d["q"], d["qi"], d["w"], d["k"], d["v"], kblk, d["seq_lens"], out=out, lse=lse,
+                             idx_out=None, ws=ws, status=st, want_idx=False)
+
+    single = _timed_ms(one, reps, warmup=3) * 1e3
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        one()
+    g.replay()
+    torch.cuda.synchronize()
+    steps = 20
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    Q.check_status(st, f"decode {B}x{T}")
+    b2b = a.elapsed_time(b) * 1e3 / steps
+    c = (T - 1) // 4
+    keys = min(c, 511) * 4 + ((T - 1) % 4) + 1
+    nbytes = B * (c * 256 + keys * 2048 + 2 * 24 * 256 * 2)
+    return {"B": B, "T": T, "seed": seed, "us_per_step": single, "back_to_back_us_per_step": b2b,
+            "gb_per_s": nbytes / (single / 1e6) / 1e9, "frac_hbm": nbytes / (single / 1e6) / 1e9 / hbm,
+            "back_to_back_frac_hbm": nbytes / (b2b / 1e6) / 1e9 / hbm, "bytes_per_step": nbytes}
+
+
+def run_per_config(dev, hbm) -> dict:
+    """The 128K-256K range of the metric and the locality workload, each on
+    its own inputs (freed after use): the 131,072-token prefill (seed 2),
+    the 64 x 262,144 decode (seed 3), and the 1M prefill with topic
+    segments of 8,192 tokens (seed 4)."""
+    res = {}
+    for name, fn in (("prefill_128k", lambda: _prefill_config(dev, 131072, 2, hbm)),
+                     ("decode_64x256k", lambda: _decode_config(dev, 64, 262144, 3, hbm)),
+                     ("prefill_1m_local", lambda: _prefill_config(dev, 1 << 20, 4, hbm, locality=8192, reps=2))):
+        try:
+            res[name] = fn()
+        except Exception as ex:  # report, never fake
+            res[name] = {"error": str(ex)[:200]}
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
 # ------------------------------------------------------- prefix cache --
 
 def run_prefix_cached(wl: Workload, reps: int, warmup: int, full_prefill_ms: float) -> dict:
@@ -696,6 +805,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-dense", action="store_true", help="skip the dense-attention comparison")
     ap.add_argument("--no-token-level", action="store_true", help="skip the token-level indexer comparison")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the 128K / 64x256K / locality measurements")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -806,7 +916,8 @@ def main():
             "decode_step": {"bound": "hbm", "achieved": dec_gbs, "peak": hbm, "unit": "GB/s",
                             "frac": dec_gbs / hbm},
         },
-        "prefill_bound": prefill_bound(wl, pre_ms, tc, hbm),
+        "prefill_bound": dict(prefill_bound(wl, pre_ms, tc, hbm), attention_alone_ms=attn_ms,
+                              frac_of_attention_alone=attn_ms / pre_ms),
         "gpu_launches": wl.launches_per_step() * K,
         "clocks": clk,
     }
@@ -823,6 +934,8 @@ def main():
             line["token_level_indexer"] = run_token_level(wl, idx_ms)
         except Exception as ex:
             line["token_level_indexer"] = {"error": str(ex)[:200]}
+    if rank == 0 and not args.no_per_config:
+        line["per_config"] = run_per_config(dev, hbm)
     if rank == 0 and not args.no_dense:
         try:
             line["dense_comparison"] = run_dense_comparison(wl, pre_ms, dec_ms)
