@@ -54,6 +54,8 @@ constexpr int GT = 128;              // threads per group
 constexpr int THREADS = (4 + NEPI) * 32;
 constexpr int CHK = 2;               // tiles between list checks
 constexpr int FLAG_AT = SUB - 32 * CHK;  // a sub-list longer than this is cut back at a check
+constexpr int FIRST_AT = 160;         // before the first prediction: cut back a sub-list beyond this
+constexpr int R_MIN = 64;             // smallest rank a threshold is predicted from
 constexpr int HIST_INTS = 3 * 256;   // per group: 3 rotating histogram slots
 constexpr int CTL_INTS = 3 * 16;     // per group: 3 rotating control slots
 
@@ -71,7 +73,8 @@ constexpr int OFF_W = OFF_SORT + NGRP * 1024 * 8;
 constexpr int OFF_THETA = OFF_W + TQ * 4 * 4;
 constexpr int OFF_CNT = OFF_THETA + TQ * 4;      // [4 quarters][TQ] sub-list counts
 constexpr int OFF_FLAG = OFF_CNT + 4 * TQ * 4;   // [NGRP groups][2 parities] token masks
-constexpr int OFF_BAR = OFF_FLAG + NGRP * 2 * 4;
+constexpr int OFF_PRED = OFF_FLAG + NGRP * 2 * 4;  // [TQ] predicted threshold per token (-inf: none)
+constexpr int OFF_BAR = OFF_PRED + TQ * 4;
 constexpr int NBAR = 2 * NSTAGE + 2 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -92,7 +95,15 @@ struct Params {
     int64_t dense_ld;
     uint2 *cand;        // [grid, TQ, CAP] {score bits, block}
     int32_t *status;
+    int predict;        // raise thresholds by prediction (with the exactness check below)
+    uint8_t *redo;      // [nq, 4 groups] set where a prediction failed its check (or null)
+    int redo_pass;      // 1: process only the query tiles flagged in redo, without prediction
 };
+
+// In the pass after a predicting launch only the flagged query tiles run.
+__device__ __forceinline__ bool tile_skipped(const Params &p, int q) {
+    return p.redo_pass && *reinterpret_cast<const uint32_t *>(p.redo + 4 * static_cast<int64_t>(q)) == 0u;
+}
 
 // One TMEM load of 16 columns and its completion wait in a single statement:
 // the chunk's values are ordinary outputs, so nothing can read them early
@@ -387,6 +398,23 @@ __device__ __forceinline__ int group_ranks_apply(const uint2 (&it)[IPL], int n, 
     return cw.x + cw.y + cw.z + cw.w;
 }
 
+// Number of the group's items for which keep(item) holds.  One step.
+template <typename Keep>
+__device__ __forceinline__ int group_count(const uint2 (&it)[IPL], int n, Keep keep, Group &G) {
+    int mine = 0;
+#pragma unroll
+    for (int i = 0; i < IPL; ++i) {
+        if (32 * i >= n) break;
+        mine += __popc(__ballot_sync(0xFFFFFFFFu, G.lane + 32 * i < n && keep(it[i])));
+    }
+    const int s = group_step_begin(G);
+    int *c = G.ctl + s * 16;
+    if (G.lane == 0) c[G.gw] = mine;
+    group_step_end(G);
+    const int4 cw = *reinterpret_cast<const int4 *>(c);
+    return cw.x + cw.y + cw.z + cw.w;
+}
+
 // Store only where pred holds, as a predicated instruction (no branch).  No
 // "memory" clobber: the compiler may move other loads across it (ordering
 // against the list readers comes from the group barrier).
@@ -413,6 +441,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     unsigned long long *sSort = reinterpret_cast<unsigned long long *>(smem + OFF_SORT);
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sTheta = reinterpret_cast<float *>(smem + OFF_THETA);
+    float *sPred = reinterpret_cast<float *>(smem + OFF_PRED);
     int *sCnt = reinterpret_cast<int *>(smem + OFF_CNT);  // sCnt[q * TQ + tl]
     unsigned *sFlag = reinterpret_cast<unsigned *>(smem + OFF_FLAG);  // sFlag[group * 2 + parity]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
@@ -460,7 +489,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kk = blockIdx.x; kk < p.nq && ok; kk += gridDim.x) {
                 const int q = p.nq - 1 - kk;
                 const int nbt = num_btiles(p, q);
-                if (nbt == 0) continue;
+                if (nbt == 0 || tile_skipped(p, q)) continue;
                 if (!mbar_wait(qempty, qph ^ 1)) { ok = false; break; }
                 qph ^= 1;
                 mbar_arrive_expect_tx(qfull, SQ_BYTES);
@@ -492,7 +521,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int kk = blockIdx.x; kk < p.nq && ok; kk += gridDim.x) {
                 const int q = p.nq - 1 - kk;
                 const int nbt = num_btiles(p, q);
-                if (nbt == 0) continue;
+                if (nbt == 0 || tile_skipped(p, q)) continue;
                 if (!mbar_wait(qfull, qph)) { ok = false; break; }
                 qph ^= 1;
                 tc_fence_after();
@@ -548,6 +577,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int q = p.nq - 1 - kk;
             const int64_t t0 = p.q_off + static_cast<int64_t>(q) * TQ;
             const int nbt = num_btiles(p, q);
+            if (tile_skipped(p, q)) continue;
             if (group_sync_fail(bar, !ok || sMisc[1] != 0)) { ok = false; break; }
             if (tg < GTOK) {
                 const int tl = g * GTOK + tg;
@@ -555,6 +585,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) sCnt[qq * TQ + tl] = 0;
                 sTheta[tl] = -INFINITY;
+                sPred[tl] = -INFINITY;
 #pragma unroll
                 for (int h = 0; h < kHI; ++h) {
                     float wv = 0.f;
@@ -659,7 +690,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int par = static_cast<int>(nchk & 1);
                 ++nchk;
                 if (!last) {
-                    const bool full_soon = lane < GTOK && sCnt[quarter * TQ + g * GTOK + lane] > FLAG_AT;
+                    // a token with many blocks still waiting for its first
+                    // prediction is cut back early, so that its threshold
+                    // rises before most of its blocks stream past
+                    const int tln = g * GTOK + (lane & (GTOK - 1));
+                    const bool early = p.predict && sPred[tln] == -INFINITY &&
+                                       ((t0 + tln) >> p.bshift) > 8 * static_cast<int64_t>(p.k_sel);
+                    const bool full_soon = lane < GTOK && sCnt[quarter * TQ + tln] > (early ? FIRST_AT : FLAG_AT);
                     const unsigned fl = __ballot_sync(0xFFFFFFFFu, full_soon);
                     if (fl && lane == 0) atomicOr(&sFlag[g * 2 + par], fl);
                 }
@@ -677,6 +714,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         report(p.status, QSA_ERR_DEVICE_CHECK);
 #pragma unroll
                     for (int qq = 0; qq < 4; ++qq) n[qq] = min(n[qq], SUB);
+                    if (n[0] + n[1] + n[2] + n[3] <= p.k_sel) continue;  // nothing to cut (the group agrees)
                     uint2 *lst = p.cand + (static_cast<int64_t>(blockIdx.x) * TQ + tl) * CAP;
                     const int nown = min(sCnt[quarter * TQ + tl], SUB);  // this warp's sub-list
                     uint2 it[IPL];
@@ -699,6 +737,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                         G);
                     if (tg < 4) sCnt[tg * TQ + tl] = (kept + 3 - tg) / 4;
                     if (tg == 0) sTheta[tl] = th;
+                    if (p.predict) {
+                        // Predicted threshold: the rp-th best score seen so far,
+                        // rp = 2 (budget-1) seen / c, is expected to keep about
+                        // twice the budget of the token's c blocks above it.  It
+                        // holds a later block back only if the token's final
+                        // (budget-1)-th best reaches it, which finalize checks.
+                        const int64_t ct = (t0 + tl) >> p.bshift;
+                        const int64_t seen = min(static_cast<int64_t>(j + 1) * TB, ct);
+                        int64_t rp = (2 * static_cast<int64_t>(p.k_sel) * seen + ct - 1) / ct;
+                        if (rp < R_MIN) rp = R_MIN;
+                        if (rp < p.k_sel && kept >= rp) {
+                            const RadixOut rq = group_radix<false, false>(it, nown, 0u, static_cast<int>(rp), 2, G);
+                            const float thp = key2f(rq.thr);  // at or below the rp-th best key
+                            if (tg == 0) {
+                                sPred[tl] = thp;
+                                sTheta[tl] = fmaxf(th, thp);
+                            }
+                        }
+                    }
                 }
                 if (group_sync_fail(bar, false)) { ok = false; break; }
                 if (tg == 0) sFlag[g * 2 + par] = 0u;  // next written two checks from now
@@ -706,6 +763,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) continue;  // the next tile-start barrier takes everyone out
             if constexpr (!DENSE) {
                 // ---- finalize: the group's 16 tokens one after the other
+                bool pred_failed = false;
                 for (int t16 = 0; t16 < GTOK; ++t16) {
                     const int tl = g * GTOK + t16;
                     const int64_t t = t0 + tl;
@@ -723,6 +781,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (ntot > p.k_sel) {
                         float th;
                         rule = group_select_exact(it, nown, p.k_sel, G, &th);
+                    }
+                    const float pred = sPred[tl];
+                    if (pred != -INFINITY) {
+                        // exact only if (budget-1) candidates reach the predicted threshold
+                        const uint32_t pk = f2key(pred);
+                        const int reach = group_count(it, nown, [&](uint2 e) { return e.x >= pk; }, G);
+                        pred_failed |= reach < p.k_sel;
                     }
                     auto keep = [&](uint2 e) { return staged_keep(rule, e); };
                     // order by block (blocks are distinct): a group sort of 512 keys,
@@ -802,6 +867,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 }
+                // this group's tokens of the tile: redone without prediction if one failed
+                if (p.redo && !p.redo_pass && tg == 0) p.redo[4 * static_cast<int64_t>(q) + g] = pred_failed ? 1 : 0;
             }
         }
         if (!ok) {
@@ -837,8 +904,12 @@ int index_grid(int64_t L, int sms) {
     return static_cast<int>(nq < sms ? nq : sms);
 }
 
+// Candidate lists of the persistent grid, then the per-(query tile, group)
+// flags of the predicting pass.
 size_t index_cand_bytes(int64_t L, int sms) {
-    return static_cast<size_t>(index_grid(L, sms)) * ix::TQ * ix::CAP * sizeof(uint2);
+    const int64_t nq = (L + ix::TQ - 1) / ix::TQ;
+    const size_t lists = static_cast<size_t>(index_grid(L, sms)) * ix::TQ * ix::CAP * sizeof(uint2);
+    return lists + ((static_cast<size_t>(nq) * 4 + 255) / 256) * 256;
 }
 
 cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t q_off, int64_t Lq,
@@ -862,6 +933,13 @@ cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int
     p.cand = reinterpret_cast<uint2 *>(cand_ws);
     p.status = status;
     const int grid = index_grid(Lq, sms);
+    // selection launches predict thresholds; a second launch redoes, without
+    // prediction, the query tiles whose prediction failed its check (it finds
+    // no flag set and leaves at once in all but rare cases)
+    p.predict = dense ? 0 : 1;
+    p.redo = dense ? nullptr
+                   : reinterpret_cast<uint8_t *>(cand_ws) + static_cast<size_t>(grid) * ix::TQ * ix::CAP * sizeof(uint2);
+    p.redo_pass = 0;
     cudaError_t e;
     if (dense) {
         e = cudaFuncSetAttribute(ix::index_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -872,6 +950,11 @@ cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int
         e = cudaFuncSetAttribute(ix::index_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  ix::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        ix::index_kernel<false><<<grid, ix::THREADS, ix::SMEM_BYTES, stream>>>(map_q, map_k, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        p.predict = 0;
+        p.redo_pass = 1;
         ix::index_kernel<false><<<grid, ix::THREADS, ix::SMEM_BYTES, stream>>>(map_q, map_k, p);
     }
     return cudaGetLastError();
