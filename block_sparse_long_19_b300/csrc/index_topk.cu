@@ -52,10 +52,23 @@ constexpr int GTOK = TQ / NGRP;      // 16 tokens (64 TMEM columns) per group
 constexpr int NEPI = 4 * NGRP;       // 16 epilogue warps: group x TMEM lane quarter
 constexpr int GT = 128;              // threads per group
 constexpr int THREADS = (4 + NEPI) * 32;
-constexpr int CHK = 2;               // tiles between list checks
+#ifndef QSA_IX_CHK
+#define QSA_IX_CHK 2
+#endif
+#ifndef QSA_IX_FIRST_AT
+#define QSA_IX_FIRST_AT 160
+#endif
+#ifndef QSA_IX_R_MIN
+#define QSA_IX_R_MIN 64
+#endif
+#ifndef QSA_IX_MARGIN
+#define QSA_IX_MARGIN 2
+#endif
+constexpr int CHK = QSA_IX_CHK;      // tiles between list checks
 constexpr int FLAG_AT = SUB - 32 * CHK;  // a sub-list longer than this is cut back at a check
-constexpr int FIRST_AT = 160;         // before the first prediction: cut back a sub-list beyond this
-constexpr int R_MIN = 64;             // smallest rank a threshold is predicted from
+constexpr int FIRST_AT = QSA_IX_FIRST_AT;  // before the first prediction: cut back a sub-list beyond this
+constexpr int R_MIN = QSA_IX_R_MIN;        // smallest rank a threshold is predicted from
+constexpr int MARGIN = QSA_IX_MARGIN;      // predicted thresholds keep MARGIN x (budget-1) blocks
 constexpr int HIST_INTS = 3 * 256;   // per group: 3 rotating histogram slots
 constexpr int CTL_INTS = 3 * 16;     // per group: 3 rotating control slots
 
@@ -74,7 +87,8 @@ constexpr int OFF_THETA = OFF_W + TQ * 4 * 4;
 constexpr int OFF_CNT = OFF_THETA + TQ * 4;      // [4 quarters][TQ] sub-list counts
 constexpr int OFF_FLAG = OFF_CNT + 4 * TQ * 4;   // [NGRP groups][2 parities] token masks
 constexpr int OFF_PRED = OFF_FLAG + NGRP * 2 * 4;  // [TQ] predicted threshold per token (-inf: none)
-constexpr int OFF_BAR = OFF_PRED + TQ * 4;
+constexpr int OFF_GPRED = OFF_PRED + TQ * 4;     // [NGRP] this tile's prediction switch per group
+constexpr int OFF_BAR = OFF_GPRED + NGRP * 4;
 constexpr int NBAR = 2 * NSTAGE + 2 + 4;
 constexpr int OFF_MISC = OFF_BAR + NBAR * 8;
 constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
@@ -98,6 +112,7 @@ struct Params {
     int predict;        // raise thresholds by prediction (with the exactness check below)
     uint8_t *redo;      // [nq, 4 groups] set where a prediction failed its check (or null)
     int redo_pass;      // 1: process only the query tiles flagged in redo, without prediction
+    int *stop;          // set once a prediction failed anywhere in the call: no more predictions
 };
 
 // In the pass after a predicting launch only the flagged query tiles run.
@@ -442,6 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     float *sW = reinterpret_cast<float *>(smem + OFF_W);
     float *sTheta = reinterpret_cast<float *>(smem + OFF_THETA);
     float *sPred = reinterpret_cast<float *>(smem + OFF_PRED);
+    volatile int *sGPred = reinterpret_cast<volatile int *>(smem + OFF_GPRED);
     int *sCnt = reinterpret_cast<int *>(smem + OFF_CNT);  // sCnt[q * TQ + tl]
     unsigned *sFlag = reinterpret_cast<unsigned *>(smem + OFF_FLAG);  // sFlag[group * 2 + parity]
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
@@ -469,6 +485,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(&tempty[i], NEPI);
         }
         sMisc[1] = 0;
+        sMisc[2] = 0;  // set once a group's prediction failed: the CTA stops predicting
         for (int i = 0; i < NGRP * 2; ++i) sFlag[i] = 0u;
         fence_barrier_init();
     }
@@ -573,6 +590,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint2 *sub = p.cand + static_cast<int64_t>(blockIdx.x) * TQ * CAP + quarter * SUB;
         uint32_t acc = 0, nchk = 0;
         bool ok = true;
+        // thresholds are predicted until a prediction fails its check anywhere
+        // in the CTA or the call: rows whose scores are not spread alike over
+        // their blocks (a structured context) then run the plain streaming
+        // selection, and few query tiles are redone.  The switch is read once
+        // per tile for the whole group (group-uniform).
+        bool predict_on = p.predict != 0;
         for (int kk = blockIdx.x; kk < p.nq; kk += gridDim.x) {
             const int q = p.nq - 1 - kk;
             const int64_t t0 = p.q_off + static_cast<int64_t>(q) * TQ;
@@ -586,6 +609,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int qq = 0; qq < 4; ++qq) sCnt[qq * TQ + tl] = 0;
                 sTheta[tl] = -INFINITY;
                 sPred[tl] = -INFINITY;
+                if (tg == 0)
+                    sGPred[g] = predict_on && sMisc[2] == 0u &&
+                                (p.stop == nullptr || *reinterpret_cast<volatile int *>(p.stop) == 0);
 #pragma unroll
                 for (int h = 0; h < kHI; ++h) {
                     float wv = 0.f;
@@ -594,6 +620,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
             if (group_sync_fail(bar, false)) { ok = false; break; }
+            predict_on = sGPred[g] != 0;
             const bool tile_all_in = (t0 + TQ <= p.L);
             const int64_t c_min = t0 >> p.bshift;
             for (int j = 0; j < nbt; ++j) {
@@ -694,7 +721,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // prediction is cut back early, so that its threshold
                     // rises before most of its blocks stream past
                     const int tln = g * GTOK + (lane & (GTOK - 1));
-                    const bool early = p.predict && sPred[tln] == -INFINITY &&
+                    const bool early = predict_on && sPred[tln] == -INFINITY &&
                                        ((t0 + tln) >> p.bshift) > 8 * static_cast<int64_t>(p.k_sel);
                     const bool full_soon = lane < GTOK && sCnt[quarter * TQ + tln] > (early ? FIRST_AT : FLAG_AT);
                     const unsigned fl = __ballot_sync(0xFFFFFFFFu, full_soon);
@@ -737,7 +764,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         G);
                     if (tg < 4) sCnt[tg * TQ + tl] = (kept + 3 - tg) / 4;
                     if (tg == 0) sTheta[tl] = th;
-                    if (p.predict) {
+                    if (predict_on) {
                         // Predicted threshold: the rp-th best score seen so far,
                         // rp = 2 (budget-1) seen / c, is expected to keep about
                         // twice the budget of the token's c blocks above it.  It
@@ -745,7 +772,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // (budget-1)-th best reaches it, which finalize checks.
                         const int64_t ct = (t0 + tl) >> p.bshift;
                         const int64_t seen = min(static_cast<int64_t>(j + 1) * TB, ct);
-                        int64_t rp = (2 * static_cast<int64_t>(p.k_sel) * seen + ct - 1) / ct;
+                        int64_t rp = (MARGIN * static_cast<int64_t>(p.k_sel) * seen + ct - 1) / ct;
                         if (rp < R_MIN) rp = R_MIN;
                         if (rp < p.k_sel && kept >= rp) {
                             const RadixOut rq = group_radix<false, false>(it, nown, 0u, static_cast<int>(rp), 2, G);
@@ -869,6 +896,13 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 // this group's tokens of the tile: redone without prediction if one failed
                 if (p.redo && !p.redo_pass && tg == 0) p.redo[4 * static_cast<int64_t>(q) + g] = pred_failed ? 1 : 0;
+                if (pred_failed) {
+                    predict_on = false;
+                    if (tg == 0) {
+                        sMisc[2] = 1u;
+                        if (p.stop) *reinterpret_cast<volatile int *>(p.stop) = 1;
+                    }
+                }
             }
         }
         if (!ok) {
@@ -909,12 +943,12 @@ int index_grid(int64_t L, int sms) {
 size_t index_cand_bytes(int64_t L, int sms) {
     const int64_t nq = (L + ix::TQ - 1) / ix::TQ;
     const size_t lists = static_cast<size_t>(index_grid(L, sms)) * ix::TQ * ix::CAP * sizeof(uint2);
-    return lists + ((static_cast<size_t>(nq) * 4 + 255) / 256) * 256;
+    return lists + ((static_cast<size_t>(nq) * 4 + 255) / 256) * 256 + 256;  // + the call's stop word
 }
 
 cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t q_off, int64_t Lq,
                          int unit_tokens, int budget, const uint16_t *w, int32_t *idx, float *score,
-                         float *dense, void *cand_ws, int32_t *status, int sms,
+                         float *dense, void *cand_ws, int32_t *status, int sms, int *stop,
                          cudaStream_t stream) {
     ix::Params p;
     const int64_t L = q_off + Lq;
@@ -940,6 +974,7 @@ cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int
     p.redo = dense ? nullptr
                    : reinterpret_cast<uint8_t *>(cand_ws) + static_cast<size_t>(grid) * ix::TQ * ix::CAP * sizeof(uint2);
     p.redo_pass = 0;
+    p.stop = stop;
     cudaError_t e;
     if (dense) {
         e = cudaFuncSetAttribute(ix::index_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,

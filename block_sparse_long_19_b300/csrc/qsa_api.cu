@@ -379,8 +379,11 @@ static qsa_status index_common(const qsa_config *cfg, const qsa_bf16 *qi, const 
     const int64_t nbk = L / qsa::kBlock;
     st = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
     if (st != QSA_OK) return st;
+    int *stop = qsa::index_stop_word(cand, qsa::index_cand_bytes(L, sms));
+    e = cudaMemsetAsync(stop, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "memset");
     e = qsa::launch_index(map_q, map_k, 0, L, qsa::kBlock, cfg->budget_blocks, w, idx, score, dense, cand,
-                          dev_status, sms, s);
+                          dev_status, sms, stop, s);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     return ok();
 }
@@ -567,9 +570,11 @@ qsa_status qsa_prefill_overlapped(const qsa_config *cfg, const qsa_bf16 *q, cons
             return cuda_fail(e, "event");
         }
     }
+    int *stop = qsa::index_stop_word(cand, qsa::index_cand_bytes(L, sms));
     auto run = [&]() -> qsa_status {
         cudaError_t e2 = qsa::launch_kprep(1, 0, L, L, ki, k, k_rot, kblk, freqs, sms, s);
         if (e2 != cudaSuccess) return cuda_fail(e2, "kprep launch");
+        if ((e2 = cudaMemsetAsync(stop, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e2, "memset");
         if ((e2 = cudaEventRecord(ev[n], s)) != cudaSuccess) return cuda_fail(e2, "event record");
         if ((e2 = cudaStreamWaitEvent(side, ev[n], 0)) != cudaSuccess) return cuda_fail(e2, "stream wait");
         for (int j = 0; j < n; ++j) {
@@ -583,7 +588,7 @@ qsa_status qsa_prefill_overlapped(const qsa_config *cfg, const qsa_bf16 *q, cons
             if (st2 != QSA_OK) return st2;
             e2 = qsa::launch_index(map_q, map_k, r0, nr, qsa::kBlock, budget, w + r0 * qsa::kHI,
                                    idx + r0 * budget, score ? score + r0 * budget : nullptr, nullptr, cand,
-                                   dev_status, ctas[j], side);
+                                   dev_status, ctas[j], stop, side);
             if (e2 != cudaSuccess) return cuda_fail(e2, "indexer launch");
             if ((e2 = cudaEventRecord(ev[j], side)) != cudaSuccess) return cuda_fail(e2, "event record");
         }
@@ -670,8 +675,11 @@ qsa_status qsa_index_topk_tokens(const qsa_config *cfg, const qsa_bf16 *qi, cons
     if (st != QSA_OK) return st;
     st = make_map(&map_k, ki, qsa::kDI, static_cast<uint64_t>(L), 128);  // every token is a unit
     if (st != QSA_OK) return st;
+    int *stop = qsa::index_stop_word(ws, qsa::index_cand_bytes(L, sm_count()));
+    e = cudaMemsetAsync(stop, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "memset");
     e = qsa::launch_index(map_q, map_k, 0, L, 1, cfg->budget_blocks, w, idx, score, nullptr, ws, dev_status,
-                          sm_count(), s);
+                          sm_count(), stop, s);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     return ok();
 }
@@ -719,8 +727,11 @@ qsa_status qsa_index_topk_cached_ctas(const qsa_config *cfg, const qsa_bf16 *qi,
     st = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
     if (st != QSA_OK) return st;
     const int sms = sm_count();
+    int *stop = qsa::index_stop_word(ws, qsa::index_cand_bytes(Lq, sms));
+    e = cudaMemsetAsync(stop, 0, sizeof(int), s);
+    if (e != cudaSuccess) return cuda_fail(e, "memset");
     e = qsa::launch_index(map_q, map_k, q_offset, Lq, qsa::kBlock, cfg->budget_blocks, w, idx, score, nullptr,
-                          ws, dev_status, max_ctas > 0 && max_ctas < sms ? max_ctas : sms, s);
+                          ws, dev_status, max_ctas > 0 && max_ctas < sms ? max_ctas : sms, stop, s);
     if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
     return ok();
 }

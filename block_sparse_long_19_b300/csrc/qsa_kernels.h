@@ -29,8 +29,13 @@ size_t index_cand_bytes(int64_t L, int sms);
 // q_off+Lq.  unit_tokens: 4 (micro-blocks) or 1 (a token-level indexer).
 cudaError_t launch_index(const CUtensorMap &map_q, const CUtensorMap &map_k, int64_t q_off, int64_t Lq,
                          int unit_tokens, int budget, const uint16_t *w, int32_t *idx, float *score,
-                         float *dense, void *cand_ws, int32_t *status, int sms,
+                         float *dense, void *cand_ws, int32_t *status, int sms, int *stop,
                          cudaStream_t stream);
+// The prediction stop word of a call: the last 256 bytes of a candidate
+// workspace of index_cand_bytes(L, sms) bytes (zeroed by the caller once per call).
+inline int *index_stop_word(void *cand_ws, size_t cand_bytes) {
+    return reinterpret_cast<int *>(static_cast<uint8_t *>(cand_ws) + cand_bytes - 256);
+}
 cudaError_t launch_fill_current_only(int64_t q_off, int64_t Lq, int unit_tokens, int budget, int32_t *idx,
                                      float *score, cudaStream_t stream);
 

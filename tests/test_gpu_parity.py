@@ -352,3 +352,39 @@ def test_decode_step_replays_as_cuda_graph():
         assert torch.equal(got[2], idx)
         assert torch.equal(got[0], out)
         assert torch.equal(got[1], lse)
+
+
+def test_failed_threshold_prediction_is_redone_exactly():
+    """Blocks 0..767 score far above every later block, so the threshold the
+    indexer predicts from the first tiles of a long row (the rp-th best of
+    the first 768 blocks) overshoots the row's final (budget-1)-th best: the
+    exactness check fails, the query tile is redone without prediction, and
+    the selection still equals the oracle's.  The per-(query tile, group)
+    flags of the predicting launch sit after the candidate lists in the
+    workspace; some must be set here, which shows the redo launch had work."""
+    L, budget = 32768, 512
+    t = W.prefill_inputs(L, 57, DEV)
+    g = torch.Generator(device=DEV)
+    g.manual_seed(58)
+    u = torch.randn(128, generator=g, device=DEV)
+    u = u / u.norm()
+    t["qi"] = (t["qi"].float() + 2.0 * u).to(torch.bfloat16)
+    ki = t["ki"].float()
+    ki[:3072] += 6.0 * float(np.sqrt(128.0)) * u
+    t["ki"] = ki.to(torch.bfloat16)
+    hb = W.host_bits(t)
+    cfg = Q.default_config(budget=budget)
+    ws = torch.zeros(Q.index_topk_workspace_bytes(cfg, L), dtype=torch.uint8, device=DEV)
+    idx, _, k_rot, st = Q.index_topk(cfg, t["qi"], t["w"], t["ki"], k=t["k"], ws=ws, want_score=False)
+    torch.cuda.synchronize()
+    Q.check_status(st)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nq = (L + 63) // 64
+    kblk_bytes = -(-((L // 4) * 128 * 2 + 16) // 1024) * 1024
+    flags = ws[kblk_bytes + min(nq, sms) * 64 * 2048 * 8:][: nq * 4].cpu().numpy()
+    assert flags.sum() > 0  # some predictions failed their check
+    assert flags[: 16352 // 64 * 4].sum() == 0  # rows with few blocks never predict
+    rows = sample_rows(L, 96, seed=57, extra=[16384, 20000, 32767])
+    ref = O.prefill_rows(hb, rows, budget, want_o=False)
+    scores = O.prefill_scores(hb, rows)
+    check_selection(idx.cpu().numpy()[rows], ref["idx"], scores, rows, budget)
