@@ -14,12 +14,12 @@
 // the tensor cores.  The design therefore spends its effort on the data path:
 //   * one CTA per query (all 24 heads: each gathered row serves both KV heads'
 //     12 query heads);
-//   * a producer warp issues one 4 KiB cp.async.bulk per selected block for K
-//     and one for V (a block's 4 key rows of both KV heads are contiguous in
-//     HBM) into a ring of 64 KiB stages of 8 blocks; block slots are skewed by
-//     16 bytes so the tensor-core operand loads (ldmatrix) are free of bank
-//     conflicts.  4 KiB copies matter: with 1 KiB copies one producer warp
-//     per SM could not keep enough bytes in flight;
+//   * two producer warps (one for K, one for V) issue one 4 KiB
+//     cp.async.bulk per selected block into a ring of 64 KiB stages of 8
+//     blocks; block slots are skewed by 16 bytes so the tensor-core operand
+//     loads (ldmatrix) are free of bank conflicts.  4 KiB copies and more
+//     than one issuing warp matter: a warp issues a bulk copy only about every
+//     100 cycles, so one producer warp could not keep enough bytes in flight;
 //   * four consumer warps (KV head x key half of every stage) run QK^T and PV
 //     with the warp-level MMA (m16n8k16, bf16 in, fp32 out) and an fp32 online
 //     softmax in the log2 domain with a lazy rescale; the two halves merge at
@@ -48,7 +48,8 @@ constexpr int STAGE_BYTES = 2 * KV_BYTES;
 constexpr int QROW = kD * 2 + 16;         // 528 B per query row in smem
 constexpr int Q_BYTES = kHKV * 16 * QROW;
 constexpr int NCONS = 4;
-constexpr int THREADS = 32 * (1 + NCONS);
+constexpr int WARP_VPROD = 1 + NCONS;    // the V producer (warp 0 produces K)
+constexpr int THREADS = 32 * (2 + NCONS);
 constexpr int OFF_BAR = 0;
 constexpr int OFF_IDX = 128;
 constexpr int OFF_CS = OFF_IDX + kMaxBudget * 4;
@@ -119,7 +120,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
-            mbar_init(&full[i], 1);
+            mbar_init(&full[i], 2);  // the K and the V producer arrive
             mbar_init(&empty[i], NCONS);
         }
         fence_barrier_init();
@@ -164,7 +165,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
         st_end = min(total_st, st_begin + per);
         if (st_begin > st_end) st_begin = st_end;
     }
-    if (warp > 0) {
+    if (warp > 0 && warp <= NCONS) {
         const int ct = threadIdx.x - 32;
         constexpr int CT = NCONS * 32;
         for (int i = ct; i < kHQ * 32; i += CT) {
@@ -191,15 +192,17 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
         named_bar(1, CT);  // Q complete before any consumer reads it
     }
 
-    if (warp == 0) {
-        // ------------------------------------------------- producer --
-        // lanes 0..7: K of slot `lane`, lanes 8..15: V of slot `lane - 8`.
+    if (warp == 0 || warp == WARP_VPROD) {
+        // ------------------------------------------------ producers --
+        // warp 0 copies K, warp WARP_VPROD copies V: lanes 0..7 the block of
+        // slot `lane`.  One warp issues a bulk copy only every ~100 cycles, so
+        // two producers keep twice the copies in flight.
         // A past block (b < c, all rows <= t) is one 4 KiB copy.  The current
         // block and padding slots are copied row by row; a row that must not
         // be attended (j > t, or no block) fetches the query's own row t, so
         // every byte read is inside the tensor and finite.
         const int sl = lane & 7;
-        const int isv = (lane >> 3) & 1;
+        const int isv = warp == WARP_VPROD ? 1 : 0;
         const uint64_t pol = policy_evict_first();
         bool ok = true;
         for (int st = st_begin; st < st_end; ++st) {
@@ -209,9 +212,9 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
             if (lane == 0) ok = mbar_wait(&empty[slot], ph ^ 1);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], STAGE_BYTES - 2 * SBLK * 16);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], SBLK * kBlock * ROWB);  // this producer's half
             __syncwarp();
-            if (lane < 16) {
+            if (lane < SBLK) {
                 const int si = st * SBLK + sl;
                 const int b = si < a.budget ? sIdx[si] : -1;
                 const uint16_t *base = isv ? vbase : kbase;
