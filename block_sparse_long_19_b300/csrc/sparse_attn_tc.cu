@@ -14,19 +14,18 @@
 // 4 KiB of V) arrive as ONE 5-D TMA box each, {64 dims, 4 tokens, 2 heads,
 // 4 dim chunks, 1 sequence} with the dim-chunk outermost, so the box lands
 // as four 1 KiB 128-byte-swizzled atoms: atom c holds dims 64c..64c+63 of the
-// 8 rows (head g, token i) in the order 4g + i.  Eight blocks make a tile
-// (32 KiB of K or of V) whose 64 rows (block, head, token) are the MMA's
+// 8 rows (head g, token i) in the order 4g + i.  Sixteen blocks make a tile
+// (64 KiB of K or of V) whose 128 rows (block, head, token) are the MMA's
 // M dimension:
 //   * S^T = K Q'^T: A = the K tile, K-major (8-row groups 4 KiB apart),
-//     B = Q' (24 heads + 8 unused rows, K-major), M = 64, N = 32, K = 256,
-//     fp32 in TMEM (row r of the tile in lane (r % 16) + 32 (r / 16),
-//     column = query head);
+//     B = Q' (24 heads + 8 unused rows, K-major), M = 128, N = 32, K = 256,
+//     fp32 in TMEM (row r of the tile in lane r, column = query head);
 //   * O^T += V^T P^T: A = the V tile read MN-major (M = 128 head dims per
-//     MMA, two MMAs for the 256; K = the tile's 64 rows), B = P^T in shared
+//     MMA, two MMAs for the 256; K = the tile's 128 rows), B = P^T in shared
 //     memory, MN-major (64-byte swizzle), N = 32 query heads; O^T stays in
 //     TMEM for the whole key loop.
-// Small tiles keep more of them in flight: the ring of 6 slots holds 3 tiles'
-// K and V, and a slot is refilled as soon as its MMA has read it.
+// The ring of 3 slots of 64 KiB takes K_0, V_0, K_1, V_1, ... in turn, and a
+// slot is refilled as soon as its MMA has read it.
 // Every key row meets all 24 query heads in the MMA; the softmax gives
 // probability 0 to the 12 heads of the other KV head, so their products
 // vanish in PV (half the tensor work is spent on those zeros: the kernel is
@@ -45,9 +44,8 @@
 //   warp 4: MMA issuer (one thread): QK^T and PV of the tiles in order, each
 //     as soon as its inputs are ready;
 //   warp 5: TMEM allocation, Q' (RoPE) into shared memory;
-//   warps 6..6+NPROD-1: TMA producers.  The ring has 6 slots of 32 KiB that
-//     K and V tiles take in turn, and every producer warp issues its share
-//     of the 8 block copies of every tile: one warp issues a 4 KiB copy
+//   warps 6..6+NPROD-1: TMA producers.  Every producer warp issues its share
+//     of the 16 block copies of every tile: one warp issues a 4 KiB copy
 //     only about every 100 cycles (tensor box or plain bulk copy alike,
 //     about 39 GB/s per SM), and the next tile's load cannot start before
 //     the ring frees a slot, so a tile's copies are spread over warps.
@@ -361,10 +359,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             // first: a PV frees a ring slot for the next loads, so it must not
             // wait behind a QK^T whose K tile is still in flight.  A parity
             // test of a slot's barrier is only meaningful once the slot's
-            // previous load has landed: with 6 slots that load is K_{u-3}
-            // (read by an earlier QK^T, so always landed); with an odd ring
-            // it would be V_{u-2}, and QK^T would have to stay less than two
-            // tiles ahead of PV.
+            // previous load has landed.  With the odd ring of 3 slots, K_u
+            // goes into the slot of V_{u-2}: QK^T of tile u may only be
+            // tested once PV of tile u-2 has been issued (QK^T stays less
+            // than two tiles ahead of PV), or the test would read the parity
+            // of a phase two behind and pass too early.
             auto issue_qk = [&](int u) {
                 const int slot = (2 * u) % NSLOT;
                 tc_fence_after();
