@@ -616,7 +616,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 for (int h = 0; h < kHI; ++h) {
                     float wv = 0.f;
                     if (t < p.L) wv = __uint_as_float(static_cast<uint32_t>(p.w[(t - p.q_off) * kHI + h]) << 16);
-                    sW[(tl >> 2) * 16 + h * 4 + (tl & 3)] = wv;  // [token quad][head][token]
+                    // w / 2 (exact for every bf16 w), see the score below
+                    sW[(tl >> 2) * 16 + h * 4 + (tl & 3)] = 0.5f * wv;  // [token quad][head][token]
                 }
             }
             if (group_sync_fail(bar, false)) { ok = false; break; }
@@ -653,15 +654,25 @@ __global__ void __launch_bounds__(THREADS, 1)
                         const int tl0 = g * GTOK + ch * 4;
                         // s = sum_h w_h * max(0, x_h) for two tokens per packed FMA,
                         // heads in order 0..3, the first product added to +0 (the
-                        // sum is never -0); per component this is plain fmaf
+                        // sum is never -0); per component this is plain fmaf.
+                        // max(0, x) is taken as x + |x| = 2 max(0, x) (exact: a
+                        // doubling or x - x = +0), the 2 cancelled by the halved
+                        // weight, so the product w/2 * (x + |x|) is exactly
+                        // w * max(0, x) and each fmaf rounds as before; the add
+                        // runs on the FMA pipe, where a max would take the
+                        // integer pipe that the threshold tests and list pushes
+                        // also need.  (Exact for |x| < 2^127; a dot product of
+                        // bf16 vectors beyond that is out of range anyway.)
                         float2 s01 = make_float2(0.f, 0.f), s23 = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int h = 0; h < kHI; ++h) {
                             const float4 wv = *reinterpret_cast<const float4 *>(&sW[(tl0 >> 2) * 16 + h * 4]);
-                            const float2 x01 = make_float2(fmaxf(__uint_as_float(cur[h]), 0.f),
-                                                           fmaxf(__uint_as_float(cur[4 + h]), 0.f));
-                            const float2 x23 = make_float2(fmaxf(__uint_as_float(cur[8 + h]), 0.f),
-                                                           fmaxf(__uint_as_float(cur[12 + h]), 0.f));
+                            auto two_relu = [](uint32_t u) {
+                                const float x = __uint_as_float(u);
+                                return __fadd_rn(x, fabsf(x));
+                            };
+                            const float2 x01 = make_float2(two_relu(cur[h]), two_relu(cur[4 + h]));
+                            const float2 x23 = make_float2(two_relu(cur[8 + h]), two_relu(cur[12 + h]));
                             s01 = __ffma2_rn(make_float2(wv.x, wv.y), x01, s01);
                             s23 = __ffma2_rn(make_float2(wv.z, wv.w), x23, s23);
                         }
@@ -687,20 +698,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 m[tk] = __ballot_sync(0xFFFFFFFFu, pass[tk]);
                             }
                             // a block enters the token's list when s >= its threshold
-                            // (no branch per token: the store is predicated)
                             if ((m[0] | m[1] | m[2] | m[3]) != 0u) {
                                 uint2 *base = sub + static_cast<int64_t>(tl0) * CAP;
-                                int cnt4[4] = {c4.x, c4.y, c4.z, c4.w};
+                                const int cnt4[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
                                 for (int tk = 0; tk < 4; ++tk) {
-                                    const int pos = cnt4[tk] + __popc(m[tk] & ltmask);
+                                    if (m[tk] == 0u) continue;  // warp-uniform
+                                    int *cp = &sCnt[quarter * TQ + tl0 + tk];
+                                    const int cnt = cnt4[tk];
+                                    const int pos = cnt + __popc(m[tk] & ltmask);
                                     st_global_pred(base + tk * CAP + pos,
                                                    make_uint2(__float_as_uint(sv[tk]), static_cast<uint32_t>(b)),
                                                    pass[tk] && pos < SUB);
-                                    cnt4[tk] += __popc(m[tk]);
+                                    *cp = cnt + __popc(m[tk]);
                                 }
-                                *reinterpret_cast<int4 *>(&sCnt[quarter * TQ + tl0]) =
-                                    make_int4(cnt4[0], cnt4[1], cnt4[2], cnt4[3]);
                             }
                         }
                     }
@@ -769,14 +780,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // rp = 2 (budget-1) seen / c, is expected to keep about
                         // twice the budget of the token's c blocks above it.  It
                         // holds a later block back only if the token's final
-                        // (budget-1)-th best reaches it, which finalize checks.
+                        // (budget-1)-th best reaches it, which finalize checks
+                        // against the highest prediction the token ever had: a
+                        // later, lower prediction lowers neither (blocks below
+                        // the earlier one were already held back).
                         const int64_t ct = (t0 + tl) >> p.bshift;
                         const int64_t seen = min(static_cast<int64_t>(j + 1) * TB, ct);
                         int64_t rp = (MARGIN * static_cast<int64_t>(p.k_sel) * seen + ct - 1) / ct;
                         if (rp < R_MIN) rp = R_MIN;
                         if (rp < p.k_sel && kept >= rp) {
                             const RadixOut rq = group_radix<false, false>(it, nown, 0u, static_cast<int>(rp), 2, G);
-                            const float thp = key2f(rq.thr);  // at or below the rp-th best key
+                            // rq.thr is at or below the rp-th best key
+                            const float thp = fmaxf(sPred[tl], key2f(rq.thr));
                             if (tg == 0) {
                                 sPred[tl] = thp;
                                 sTheta[tl] = fmaxf(th, thp);
