@@ -69,7 +69,7 @@ constexpr int FLAG_AT = SUB - 32 * CHK;  // a sub-list longer than this is cut b
 constexpr int FIRST_AT = QSA_IX_FIRST_AT;  // before the first prediction: cut back a sub-list beyond this
 constexpr int R_MIN = QSA_IX_R_MIN;        // smallest rank a threshold is predicted from
 constexpr int MARGIN = QSA_IX_MARGIN;      // predicted thresholds keep MARGIN x (budget-1) blocks
-constexpr int HIST_INTS = 3 * 256;   // per group: 3 rotating histogram slots
+constexpr int HIST_INTS = 4 * 256;   // per group: 3 rotating histogram slots + one for a second rank
 constexpr int CTL_INTS = 3 * 16;     // per group: 3 rotating control slots
 
 constexpr int GCOL = GTOK * kHI;     // 64 MMA columns per group
@@ -362,6 +362,153 @@ __device__ __forceinline__ RadixOut group_radix(const uint2 (&it)[IPL], int n, u
     r.eq = eq;
     r.lo = lo;
     return r;
+}
+
+// Digit search of one radix pass (every warp does it itself from the
+// finished histogram h, no barrier): the bucket of the k-th largest value.
+__device__ __forceinline__ void radix_digit(const uint32_t *h, int lane, int krem, int &digit, uint32_t &above,
+                                            uint32_t &e) {
+    uint32_t cnt[8];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int b = 0; b < 8; ++b) {
+        cnt[b] = h[255 - (lane * 8 + b)];
+        sum += cnt[b];
+    }
+    uint32_t incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += t;
+    }
+    const uint32_t excl = incl - sum;
+    const bool mine = excl < static_cast<uint32_t>(krem) && static_cast<uint32_t>(krem) <= incl;
+    digit = 0;
+    above = 0;
+    e = 0;
+    if (mine) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            if (acc + cnt[b] >= static_cast<uint32_t>(krem)) {
+                digit = 255 - (lane * 8 + b);
+                above = acc;
+                e = cnt[b];
+                break;
+            }
+            acc += cnt[b];
+        }
+    }
+    const int src = __ffs(__ballot_sync(0xFFFFFFFFu, mine)) - 1;
+    digit = __shfl_sync(0xFFFFFFFFu, digit, src);
+    above = __shfl_sync(0xFFFFFFFFu, above, src);
+    e = __shfl_sync(0xFFFFFFFFu, e, src);
+}
+
+// group_radix<false, false>(it, n, 0, k, 2, G) for two ranks k1 and k2 at
+// once (the same two results): the max / min step and the first pass are
+// shared, and the second pass counts both ranks' buckets in one step, so the
+// pair takes 3 group steps instead of 6.
+__device__ __forceinline__ void group_radix2(const uint2 (&it)[IPL], int n, int k1, int k2, Group &G, RadixOut &r1,
+                                             RadixOut &r2) {
+    uint32_t mx = 0u, mn = 0xFFFFFFFFu;
+    int nv = 0;
+#pragma unroll
+    for (int i = 0; i < IPL; ++i) {
+        if (32 * i >= n) break;
+        if (G.lane + 32 * i < n) {
+            mx = max(mx, it[i].x);
+            mn = min(mn, it[i].x);
+            ++nv;
+        }
+    }
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    mn = __reduce_min_sync(0xFFFFFFFFu, mn);
+    nv = __reduce_add_sync(0xFFFFFFFFu, nv);
+    {
+        const int s = group_step_begin(G);
+        int *c = G.ctl + s * 16;
+        if (G.lane == 0) {
+            c[8 + G.gw] = static_cast<int>(mx);
+            c[12 + G.gw] = static_cast<int>(mn);
+            c[4 + G.gw] = nv;
+        }
+        group_step_end(G);
+        mx = 0u;
+        mn = 0xFFFFFFFFu;
+        nv = 0;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            mx = max(mx, static_cast<uint32_t>(c[8 + w]));
+            mn = min(mn, static_cast<uint32_t>(c[12 + w]));
+            nv += c[4 + w];
+        }
+    }
+    r1.krem = k1;
+    r2.krem = k2;
+    if (mx == mn) {
+        r1.thr = r2.thr = mx;
+        r1.eq = r2.eq = nv;
+        r1.lo = r2.lo = 0;
+        return;
+    }
+    const int hi = 32 - __clz(mx ^ mn);
+    const unsigned long long prefix0 = hi >= 32 ? 0ull : (static_cast<unsigned long long>(mx >> hi) << hi);
+    unsigned long long pre1 = prefix0, pre2 = prefix0;
+    int lo = hi;
+    int eq1 = nv, eq2 = nv;
+    bool go1 = true, go2 = true;  // the rank still refines its bucket
+    uint32_t *aux = G.hist + 3 * 256;
+    for (int pass = 0; pass < 2 && lo > 0 && (go1 || go2); ++pass) {
+        const int w = lo >= 8 ? 8 : lo;
+        lo -= w;
+        const uint32_t dmask = (1u << w) - 1u;
+        const unsigned long long want1 = pre1 >> (lo + w), want2 = pre2 >> (lo + w);
+        const bool split = go1 && go2 && want1 != want2;  // two buckets to count
+        const int s = group_step_begin(G);
+        if (pass == 0) {  // the second pass's extra histogram starts from zero
+            aux[G.tg] = 0u;
+            aux[G.tg + GT] = 0u;
+        }
+        uint32_t *h = G.hist + s * 256;
+        uint32_t *h2 = split ? aux : h;
+        const unsigned long long wa = go1 ? want1 : want2;
+#pragma unroll
+        for (int i = 0; i < IPL; ++i) {
+            if (32 * i >= n) break;
+            const uint32_t v = it[i].x;
+            if (G.lane + 32 * i < n) {
+                const unsigned long long top = static_cast<unsigned long long>(v) >> (lo + w);
+                if (top == wa) atomicAdd(&h[(v >> lo) & dmask], 1u);
+                else if (split && top == want2) atomicAdd(&h2[(v >> lo) & dmask], 1u);
+            }
+        }
+        group_step_end(G);
+        if (go1) {
+            int digit;
+            uint32_t above, e;
+            radix_digit(h, G.lane, r1.krem, digit, above, e);
+            r1.krem -= static_cast<int>(above);
+            eq1 = static_cast<int>(e);
+            pre1 |= static_cast<unsigned long long>(digit) << lo;
+            r1.lo = lo;
+            if (eq1 == r1.krem) go1 = false;
+        }
+        if (go2) {
+            int digit;
+            uint32_t above, e;
+            radix_digit(split ? aux : h, G.lane, r2.krem, digit, above, e);
+            r2.krem -= static_cast<int>(above);
+            eq2 = static_cast<int>(e);
+            pre2 |= static_cast<unsigned long long>(digit) << lo;
+            r2.lo = lo;
+            if (eq2 == r2.krem) go2 = false;
+        }
+    }
+    r1.thr = static_cast<uint32_t>(pre1);
+    r1.eq = eq1;
+    r2.thr = static_cast<uint32_t>(pre2);
+    r2.eq = eq2;
 }
 
 // Exact k best (key desc, block asc) of the group's items, plus the
@@ -757,8 +904,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int nown = min(sCnt[quarter * TQ + tl], SUB);  // this warp's sub-list
                     uint2 it[IPL];
                     group_load(lst + quarter * SUB, nown, it, lane);
+                    // the rank a threshold is predicted from (see below)
+                    int64_t rp = 0;
+                    if (predict_on) {
+                        const int64_t ct = (t0 + tl) >> p.bshift;
+                        const int64_t seen = min(static_cast<int64_t>(j + 1) * TB, ct);
+                        rp = (MARGIN * static_cast<int64_t>(p.k_sel) * seen + ct - 1) / ct;
+                        if (rp < R_MIN) rp = R_MIN;
+                    }
+                    const bool pred = predict_on && rp < p.k_sel;
                     // cheap pass: a bucket bound 16 bits below the shared prefix
-                    const RadixOut r = group_radix<false, false>(it, nown, 0u, p.k_sel, 2, G);
+                    // (with the predicted rank's bucket in the same steps)
+                    RadixOut r, rq;
+                    if (pred) group_radix2(it, nown, p.k_sel, static_cast<int>(rp), G, r, rq);
+                    else r = group_radix<false, false>(it, nown, 0u, p.k_sel, 2, G);
                     float th;
                     StagedRule rule{r.thr, 0u, 1};
                     if ((p.k_sel - r.krem) + r.eq <= KEEP_MAX)
@@ -775,7 +934,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         G);
                     if (tg < 4) sCnt[tg * TQ + tl] = (kept + 3 - tg) / 4;
                     if (tg == 0) sTheta[tl] = th;
-                    if (predict_on) {
+                    if (pred) {
                         // Predicted threshold: the rp-th best score seen so far,
                         // rp = 2 (budget-1) seen / c, is expected to keep about
                         // twice the budget of the token's c blocks above it.  It
@@ -784,18 +943,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // against the highest prediction the token ever had: a
                         // later, lower prediction lowers neither (blocks below
                         // the earlier one were already held back).
-                        const int64_t ct = (t0 + tl) >> p.bshift;
-                        const int64_t seen = min(static_cast<int64_t>(j + 1) * TB, ct);
-                        int64_t rp = (MARGIN * static_cast<int64_t>(p.k_sel) * seen + ct - 1) / ct;
-                        if (rp < R_MIN) rp = R_MIN;
-                        if (rp < p.k_sel && kept >= rp) {
-                            const RadixOut rq = group_radix<false, false>(it, nown, 0u, static_cast<int>(rp), 2, G);
-                            // rq.thr is at or below the rp-th best key
-                            const float thp = fmaxf(sPred[tl], key2f(rq.thr));
-                            if (tg == 0) {
-                                sPred[tl] = thp;
-                                sTheta[tl] = fmaxf(th, thp);
-                            }
+                        // rq.thr is at or below the rp-th best key (rp < budget-1
+                        // <= kept: the list holds at least rp entries)
+                        const float thp = fmaxf(sPred[tl], key2f(rq.thr));
+                        if (tg == 0) {
+                            sPred[tl] = thp;
+                            sTheta[tl] = fmaxf(th, thp);
                         }
                     }
                 }
