@@ -11,13 +11,20 @@
 //     operand registers (the contraction order inside a 32-dim slice is
 //     permuted identically on both operands, which leaves the dot products
 //     unchanged) and forms s = sum_h w_h max(0, qi_h . kblk).  The chunk's
-//     scores go to the workspace (L2-resident: 4 B per block), and a CTA
-//     radix step finds the chunk's kc-th best score with kc = ceil((budget-1)
-//     / (chunks - 1)): every full chunk holds kc blocks at or above its own
-//     value, so the smallest value over the chunks is a lower bound of the
-//     sequence's (budget-1)-th best score;
+//     scores go to the workspace (L2-resident: 4 B per block), and the
+//     chunk's kc-th best score with kc = ceil((budget-1) / (chunks - 1)) is
+//     found: every full chunk holds kc blocks at or above its own value, so
+//     the smallest value over the chunks is a lower bound of the sequence's
+//     (budget-1)-th best score.  Where kc is small (long contexts: 15 at
+//     1M tokens) each lane keeps its best keys in registers while the chunk
+//     streams and the kc-th best comes from the warps' merged lists, so no
+//     pass over the chunk's scores follows the stream; with more chunks'
+//     worth of kc each warp bounds its own blocks the same way (kw-th best),
+//     and only with few chunks does a CTA radix step run over the scores;
 //   * filter kernel: every block whose score reaches that bound becomes a
-//     candidate (on i.i.d. scores about twice the budget survive);
+//     candidate (on i.i.d. scores about twice the budget survive); at small
+//     batch the candidates' K and V rows are also prefetched into L2 for the
+//     decode attention, while HBM is otherwise idle;
 //   * merge kernel: one CTA per sequence selects the exact (budget-1) best
 //     candidates (score desc, block asc), sorts them by block and appends the
 //     current block.  If ties leave more candidates than the candidate area
@@ -34,18 +41,22 @@ namespace dx {
 constexpr int SCAN_THREADS = 256;
 constexpr int MAX_CHUNK = 16384;
 constexpr int MAX_NCHUNK = 256;  // scan CTAs per sequence
+constexpr int KW_MAX = 16;       // best scores kept per lane (and per warp) for the chunk bound
 constexpr int MERGE_THREADS = 256;
 constexpr int FILTER_THREADS = 256;
 constexpr int FILTER_PER_THREAD = 8;
 constexpr int CAND_CAP = 8192;  // filtered candidates kept per sequence
+constexpr int64_t kPrefetchL2Bytes = int64_t(72) << 20;  // L2 budget of the filter's K/V prefetch
 
 // CTA-wide radix step over n items: value(i) -> uint32, pred(i) -> bool.
 // Finds a bucket [thr, thr + 2^lo) holding the k-th largest value, looking
 // only at the bits below the prefix every valid value shares (candidate
-// scores agree on their top bits).  Same contract as the warp version in
-// qsa_select.cuh.  ctl: 8 ints of shared memory; all threads must call.
+// scores agree on their top bits), with at most max_passes 8-bit digit
+// passes (4 passes reach every bit: the bucket is then exact).  Same
+// contract as the warp version in qsa_select.cuh.  ctl: 8 ints of shared
+// memory; all threads must call.
 template <int NT, typename Val, typename Pred>
-__device__ RadixOut cta_radix(int n, int k, Val value, Pred pred, uint32_t *hist, int *ctl) {
+__device__ RadixOut cta_radix(int n, int k, Val value, Pred pred, uint32_t *hist, int *ctl, int max_passes = 4) {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint32_t mx = 0u, mn = 0xFFFFFFFFu;
     int nv = 0;
@@ -84,7 +95,7 @@ __device__ RadixOut cta_radix(int n, int k, Val value, Pred pred, uint32_t *hist
     unsigned long long prefix = hi >= 32 ? 0ull : (static_cast<unsigned long long>(mx >> hi) << hi);
     int lo = hi;
     int eq = nv;
-    while (lo > 0) {
+    for (int pass = 0; pass < max_passes && lo > 0; ++pass) {
         const int w = lo >= 8 ? 8 : lo;
         lo -= w;
         const uint32_t dmask = (1u << w) - 1u;
@@ -185,7 +196,7 @@ struct ScanParams {
     int nchunk;
     int k_sel;
     float *scores;             // [B, max_ctx/4]
-    uint32_t *lb;              // [B, nchunk] each chunk's bound key (0xFFFFFFFF: none)
+    uint32_t *lb;              // [B, nchunk, SCAN_THREADS / 32] bound keys of the chunks or their warps (0xFFFFFFFF: none)
     int32_t *ccount;           // [B] candidate counters, zeroed here for the filter
     int32_t *status;
 };
@@ -201,11 +212,12 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     const int ch = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t T = p.seq_lens[s];
-    uint32_t *lb_out = p.lb + static_cast<int64_t>(s) * p.nchunk + ch;
-    if (threadIdx.x == 0) {
-        *lb_out = 0xFFFFFFFFu;  // overwritten below if this chunk bounds the selection
-        if (ch == 0) p.ccount[s] = 0;
-    }
+    constexpr int NW = SCAN_THREADS / 32;
+    // the chunk's bound slots, one per warp: lane 0 of warp w clears slot w
+    // here and is the only thread that writes it below
+    uint32_t *lb_out = p.lb + (static_cast<int64_t>(s) * p.nchunk + ch) * NW;
+    if (lane == 0) lb_out[warp] = 0xFFFFFFFFu;
+    if (threadIdx.x == 0 && ch == 0) p.ccount[s] = 0;
     if (T < 1 || T > p.max_ctx) {
         if (threadIdx.x == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
         return;
@@ -231,10 +243,30 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
         w1 = __uint_as_float(static_cast<uint32_t>(p.w[s * kHI + 2 * qd + 1]) << 16);
     }
     const uint16_t *kb = p.kblk + static_cast<int64_t>(s) * (p.max_ctx / kBlock) * kDI;
+    // The sequence's bound is the smallest of per-chunk (or per-warp) values
+    // that each have enough scores at or above them:
+    //  * chunk (kc <= KW_MAX): the chunk's kc-th best key with kc = ceil(
+    //    (budget-1) / (chunks-1)), merged from the warps' best kc keys (each
+    //    lane keeps its best KW_MAX while the chunk streams, so no pass over
+    //    the chunk's scores follows the stream);
+    //  * warp (kw <= KW_MAX): each warp's kw-th best with kw = ceil((budget-1)
+    //    / (warps of full chunks - 1)), looser but with no merge across warps;
+    //  * otherwise the chunk's kc-th best by a CTA radix after the stream.
+    const int64_t nch_s = (c + p.chunk - 1) / p.chunk;
+    const int kc = nch_s == 1 ? p.k_sel : static_cast<int>((p.k_sel + nch_s - 2) / (nch_s - 1));
+    const int64_t wfull = (nch_s - 1) * NW;  // warps of full chunks: >= chunk / NW >= 128 scores each
+    const int kw = wfull > 1 ? static_cast<int>((p.k_sel + wfull - 2) / (wfull - 1)) : KW_MAX + 1;
+    const bool sel_needed = c > p.k_sel && nch_s > 1;
+    const bool chunk_mode = sel_needed && kc <= KW_MAX;
+    const bool warp_mode = sel_needed && !chunk_mode && kw <= KW_MAX;
+    const bool keep_top = chunk_mode || warp_mode;
+    uint32_t top[KW_MAX];  // this lane's best keys, descending (lanes with qd == 0 hold scores)
+#pragma unroll
+    for (int j = 0; j < KW_MAX; ++j) top[j] = 0u;
+    int nmine = 0;
 
     // two 16-block tiles per warp and iteration: all 16 loads of a lane in
     // flight before the first MMA
-    constexpr int NW = SCAN_THREADS / 32;
     for (int mt0 = warp; mt0 * 16 < n; mt0 += 2 * NW) {
         uint4 ua[2][4], ub[2][4];
 #pragma unroll
@@ -265,96 +297,90 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
             if (qd == 0) {
                 if (ra < b1) sc[ra - b0] = pa + 0.0f;
                 if (rb < b1) sc[rb - b0] = pb + 0.0f;
+                if (keep_top) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if ((e == 0 ? ra : rb) >= b1) continue;
+                        uint32_t v = f2key((e == 0 ? pa : pb) + 0.0f);
+                        ++nmine;
+#pragma unroll
+                        for (int j = 0; j < KW_MAX; ++j) {  // insert, keeping top[] descending
+                            const uint32_t hi = max(top[j], v);
+                            v = min(top[j], v);
+                            top[j] = hi;
+                        }
+                    }
+                }
             }
+        }
+    }
+    uint32_t *wtop = hist;  // [NW][KW_MAX] the warps' best keys, descending
+    int *wcnt = ctl;        // [NW] valid entries of each warp's list
+    if (keep_top) {
+        // the warp's best keys: the largest head of the lanes' lists, taken out
+        // one copy at a time (equal keys count separately); kc of them for the
+        // chunk bound, kw for the warp's own
+        const int want = chunk_mode ? kc : kw;
+        const int nlist = min(nmine, KW_MAX);
+        int taken = 0;  // entries this lane gave up (its list shifts up by one each time)
+        int nw = 0;     // entries of the warp's list (warp-uniform)
+        uint32_t last = 0u;
+#pragma unroll 1
+        for (int r = 0; r < want; ++r) {
+            const bool live = qd == 0 && taken < nlist;
+            if (!__any_sync(0xFFFFFFFFu, live)) break;
+            const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, live ? top[0] : 0u);
+            const unsigned who = __ballot_sync(0xFFFFFFFFu, live && top[0] == mx);
+            if (lane == __ffs(who) - 1) {
+#pragma unroll
+                for (int j = 0; j + 1 < KW_MAX; ++j) top[j] = top[j + 1];
+                ++taken;
+            }
+            if (lane == 0) wtop[warp * KW_MAX + r] = mx;
+            last = mx;
+            ++nw;
+        }
+        if (lane == 0) {
+            wcnt[warp] = nw;
+            if (warp_mode && nw == kw) lb_out[warp] = last;  // at least kw of the warp's keys are >= last
         }
     }
     __syncthreads();
 
     float *srow = p.scores + static_cast<int64_t>(s) * (p.max_ctx / kBlock);
     for (int i = threadIdx.x; i < n; i += SCAN_THREADS) srow[b0 + i] = sc[i];
-    if (c <= p.k_sel) return;  // every past block is selected
-    const int64_t nch_s = (c + p.chunk - 1) / p.chunk;
-    const int kc = nch_s == 1 ? p.k_sel : static_cast<int>((p.k_sel + nch_s - 2) / (nch_s - 1));
+    if (c <= p.k_sel || warp_mode) return;  // every past block is selected, or the warps bound
     if (n < kc) return;  // a short last chunk: the full chunks already cover the bound
+    if (chunk_mode) {
+        // the kc-th best of the warps' lists (lanes 0..NW-1 each walk one list)
+        if (warp == 0) {
+            const int nl = lane < NW ? wcnt[lane] : 0;
+            int hd = 0;
+            uint32_t kth = 0u;
+            int got = 0;
+#pragma unroll 1
+            for (int r = 0; r < kc; ++r) {
+                const bool live = hd < nl;
+                if (!__any_sync(0xFFFFFFFFu, live)) break;
+                const uint32_t head = live ? wtop[lane * KW_MAX + hd] : 0u;
+                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, head);
+                const unsigned who = __ballot_sync(0xFFFFFFFFu, live && head == mx);
+                if (lane == __ffs(who) - 1) ++hd;
+                kth = mx;
+                ++got;
+            }
+            // got < kc only if the lists hold fewer than kc keys: no bound then
+            if (lane == 0 && got == kc) lb_out[0] = kth;
+        }
+        return;
+    }
+    // two digit passes: the bucket floor is a lower bound of the kc-th best
+    // key within about 2^-8 of it (16 bits below the keys' shared prefix),
+    // and the passes that would make it exact are not spent
     const RadixOut r = cta_radix<SCAN_THREADS>(
-        n, kc, [&](int i) { return f2key(sc[i]); }, [&](int) { return true; }, hist, ctl);
+        n, kc, [&](int i) { return f2key(sc[i]); }, [&](int) { return true; }, hist, ctl, 2);
     // at least kc of this chunk's keys are >= r.thr
-    if (threadIdx.x == 0) *lb_out = r.thr;
-}
-
-struct FilterParams {
-    const int32_t *seq_lens;
-    int64_t max_ctx;
-    int k_sel;
-    const float *scores;     // [B, max_ctx/4]
-    const uint32_t *lb;      // [B, nchunk]
-    int nchunk;
-    uint2 *cand;             // [B, CAND_CAP] {score bits, block}
-    int32_t *ccount;         // [B]
-};
-
-// Candidates: the past blocks whose score key reaches the sequence's bound.
-// One global atomic per CTA reserves the CTA's range of the candidate area
-// (the sequences' counters share cache lines, so per-warp atomics from every
-// CTA would queue up at one L2 slice).
-__global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) {
-    __shared__ int s_warp[FILTER_THREADS / 32 + 1];
-    pdl_trigger();
-    pdl_wait();  // scores and bounds of the scan
-    const int s = blockIdx.y;
-    const int64_t T = p.seq_lens[s];
-    if (T < 1 || T > p.max_ctx) return;
-    const int64_t c = (T - 1) / kBlock;
-    if (c <= p.k_sel) return;
-    // the bound: the smallest chunk bound (chunks that bound nothing wrote
-    // 0xFFFFFFFF); every warp reduces the chunk slots itself, two per lane
-    const uint32_t *lbs = p.lb + static_cast<int64_t>(s) * p.nchunk;
-    const int ln = threadIdx.x & 31;
-    uint32_t bound = ln < p.nchunk ? __ldcg(lbs + ln) : 0xFFFFFFFFu;
-    for (int i = ln + 32; i < p.nchunk; i += 32) bound = min(bound, __ldcg(lbs + i));
-    bound = __reduce_min_sync(0xFFFFFFFFu, bound);
-    const float *srow = p.scores + static_cast<int64_t>(s) * (p.max_ctx / kBlock);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const unsigned ltmask = (1u << lane) - 1u;
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * FILTER_THREADS * FILTER_PER_THREAD;
-    float v[FILTER_PER_THREAD];
-    unsigned ball[FILTER_PER_THREAD];
-    int mine = 0;
-#pragma unroll
-    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
-        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
-        v[u] = b < c ? __ldcg(srow + b) : -INFINITY;
-    }
-#pragma unroll
-    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
-        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
-        ball[u] = __ballot_sync(0xFFFFFFFFu, b < c && f2key(v[u]) >= bound);
-        mine += __popc(ball[u]);
-    }
-    if (lane == 0) s_warp[warp] = mine;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int tot = 0;
-        for (int w = 0; w < FILTER_THREADS / 32; ++w) {
-            const int x = s_warp[w];
-            s_warp[w] = tot;
-            tot += x;
-        }
-        s_warp[FILTER_THREADS / 32] = tot > 0 ? atomicAdd(&p.ccount[s], tot) : 0;
-    }
-    __syncthreads();
-    int pos = s_warp[FILTER_THREADS / 32] + s_warp[warp];
-#pragma unroll
-    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
-        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
-        if ((ball[u] >> lane) & 1u) {
-            const int at = pos + __popc(ball[u] & ltmask);
-            if (at < CAND_CAP)
-                p.cand[static_cast<int64_t>(s) * CAND_CAP + at] =
-                    make_uint2(__float_as_uint(v[u]), static_cast<uint32_t>(b));
-        }
-        pos += __popc(ball[u]);
-    }
+    if (threadIdx.x == 0) lb_out[0] = r.thr;
 }
 
 struct MergeParams {
@@ -369,48 +395,38 @@ struct MergeParams {
     int32_t *status;
 };
 
-__global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    uint2 *items = reinterpret_cast<uint2 *>(smem);
-    uint32_t *sortb = reinterpret_cast<uint32_t *>(items + CAND_CAP);  // [1024]: sort input at 512..
-    uint32_t *hist = sortb + 1024;
-    int *ctl = reinterpret_cast<int *>(hist + 256);
-
-    pdl_trigger();
-    pdl_wait();  // candidates of the filter (and, through it, the scan's scores)
-    const int s = blockIdx.x;
-    const int64_t T = p.seq_lens[s];
+// The selection row of sequence s whose candidates are complete: the exact
+// (budget-1) best candidates (score desc, block asc), sorted by block, then
+// the current block.  Candidates up to items_cap are staged in shared
+// memory (`items`), more are read from the candidate area in L2, and if ties
+// flooded that area the selection runs over all of the sequence's scores.
+// sortb: 1024 words; hist: 256 words; ctl: 8 ints.  All NT threads call.
+template <int NT>
+__device__ void merge_row(const MergeParams &p, int s, int64_t c, uint2 *items, int items_cap, uint32_t *sortb,
+                          uint32_t *hist, int *ctl) {
     int32_t *row = p.idx + static_cast<int64_t>(s) * p.budget;
-    if (T < 1 || T > p.max_ctx) {
-        if (threadIdx.x == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
-        for (int i = threadIdx.x; i < p.budget; i += MERGE_THREADS) row[i] = -1;
-        return;
-    }
-    const int64_t c = (T - 1) / kBlock;
-    if (c <= p.k_sel || p.k_sel <= 0) {  // every past block (none for budget 1), then the current one
-        const int64_t np = p.k_sel <= 0 ? 0 : c;
-        for (int i = threadIdx.x; i < p.budget; i += MERGE_THREADS)
-            row[i] = i < np ? i : (i == np ? static_cast<int32_t>(c) : -1);
-        return;
-    }
     const int lane = threadIdx.x & 31;
     const unsigned ltmask = (1u << lane) - 1u;
-    const int nc = p.ccount[s];
+    const int nc = __ldcg(p.ccount + s);
     const bool direct = nc > CAND_CAP;  // ties flooded the candidate area
+    const bool staged = !direct && nc <= items_cap;
     const int n = direct ? static_cast<int>(c) : nc;
     const float *srow = p.scores + static_cast<int64_t>(s) * (p.max_ctx / kBlock);
-    if (!direct) {
-        const uint2 *src = p.cand + static_cast<int64_t>(s) * CAND_CAP;
-        for (int i = threadIdx.x; i < n; i += MERGE_THREADS) items[i] = __ldcg(src + i);
+    const uint2 *src = p.cand + static_cast<int64_t>(s) * CAND_CAP;
+    if (staged) {
+#pragma unroll 4
+        for (int i = threadIdx.x; i < n; i += NT) items[i] = __ldcg(src + i);
     }
     __syncthreads();
-    auto score = [&](int i) { return direct ? __ldcg(srow + i) : __uint_as_float(items[i].x); };
-    auto block = [&](int i) { return direct ? static_cast<uint32_t>(i) : items[i].y; };
+    auto score = [&](int i) {
+        return direct ? __ldcg(srow + i) : __uint_as_float(staged ? items[i].x : __ldcg(&src[i].x));
+    };
+    auto block = [&](int i) { return direct ? static_cast<uint32_t>(i) : (staged ? items[i].y : __ldcg(&src[i].y)); };
     SelectRule rule{0u, 0u, 1};
-    if (n > p.k_sel) rule = cta_select<MERGE_THREADS>(n, p.k_sel, score, block, hist, ctl);
+    if (n > p.k_sel) rule = cta_select<NT>(n, p.k_sel, score, block, hist, ctl);
     if (threadIdx.x == 0) ctl[3] = 0;
     __syncthreads();
-    for (int i0 = 0; i0 < n; i0 += MERGE_THREADS) {
+    for (int i0 = 0; i0 < n; i0 += NT) {
         const int i = i0 + threadIdx.x;
         float sv = 0.f;
         uint32_t bv = 0u;
@@ -452,8 +468,134 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
             if (e < m && e < p.budget) row[e] = static_cast<int32_t>(v[r]);
         }
     }
-    for (int i = m + threadIdx.x; i < p.budget; i += MERGE_THREADS)
-        row[i] = i == m ? static_cast<int32_t>(c) : -1;
+    for (int i = m + threadIdx.x; i < p.budget; i += NT) row[i] = i == m ? static_cast<int32_t>(c) : -1;
+}
+
+// A row that needs no selection: an invalid length (all -1), or every past
+// block (none for budget 1) and then the current block.  Returns true for
+// such a row, which it writes if `write` is set.
+template <int NT>
+__device__ bool trivial_row(const MergeParams &p, int s, bool write) {
+    const int64_t T = p.seq_lens[s];
+    int32_t *row = p.idx + static_cast<int64_t>(s) * p.budget;
+    if (T < 1 || T > p.max_ctx) {
+        if (write) {
+            if (threadIdx.x == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
+            for (int i = threadIdx.x; i < p.budget; i += NT) row[i] = -1;
+        }
+        return true;
+    }
+    const int64_t c = (T - 1) / kBlock;
+    if (c <= p.k_sel || p.k_sel <= 0) {
+        const int64_t np = p.k_sel <= 0 ? 0 : c;
+        if (write)
+            for (int i = threadIdx.x; i < p.budget; i += NT)
+                row[i] = i < np ? i : (i == np ? static_cast<int32_t>(c) : -1);
+        return true;
+    }
+    return false;
+}
+
+struct FilterParams {
+    MergeParams m;           // lengths, budget and scores of the sequences
+    const uint32_t *lb;      // [B, nchunk, SCAN_THREADS / 32]
+    int nchunk;
+    uint2 *cand;             // [B, CAND_CAP] {score bits, block}
+    int32_t *ccount;         // [B] candidates reserved
+    const uint16_t *kpre;    // [B, max_ctx, 2, 256] K cache to prefetch into L2 (or null)
+    const uint16_t *vpre;    // [B, max_ctx, 2, 256] V cache
+    int pre_cap;             // candidates prefetched per sequence at most
+};
+
+// Candidates: the past blocks whose score key reaches the sequence's bound.
+// One global atomic per CTA reserves the CTA's range of the candidate area
+// (the sequences' counters share cache lines, so per-warp atomics from every
+// CTA would queue up at one L2 slice).
+__global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) {
+    __shared__ int s_warp[FILTER_THREADS / 32 + 1];
+    pdl_trigger();
+    pdl_wait();  // scores and bounds of the scan
+    const int s = blockIdx.y;
+    if (trivial_row<FILTER_THREADS>(p.m, s, false)) return;  // the merge writes that row
+    const int64_t c = (p.m.seq_lens[s] - 1) / kBlock;
+    // the bound: the smallest chunk or warp bound (slots that bound nothing
+    // hold 0xFFFFFFFF); every warp reduces the slots itself
+    constexpr int SW = SCAN_THREADS / 32;  // bound slots per chunk
+    const uint32_t *lbs = p.lb + static_cast<int64_t>(s) * p.nchunk * SW;
+    const int ln = threadIdx.x & 31;
+    uint32_t bound = 0xFFFFFFFFu;
+    for (int i = ln; i < p.nchunk * SW; i += 32) bound = min(bound, __ldcg(lbs + i));
+    bound = __reduce_min_sync(0xFFFFFFFFu, bound);
+    const float *srow = p.m.scores + static_cast<int64_t>(s) * (p.m.max_ctx / kBlock);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const unsigned ltmask = (1u << lane) - 1u;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * FILTER_THREADS * FILTER_PER_THREAD;
+    float v[FILTER_PER_THREAD];
+    unsigned ball[FILTER_PER_THREAD];
+    int mine = 0;
+#pragma unroll
+    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
+        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
+        v[u] = b < c ? __ldcg(srow + b) : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
+        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
+        ball[u] = __ballot_sync(0xFFFFFFFFu, b < c && f2key(v[u]) >= bound);
+        mine += __popc(ball[u]);
+    }
+    if (lane == 0) s_warp[warp] = mine;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int tot = 0;
+        for (int w = 0; w < FILTER_THREADS / 32; ++w) {
+            const int x = s_warp[w];
+            s_warp[w] = tot;
+            tot += x;
+        }
+        s_warp[FILTER_THREADS / 32] = tot > 0 ? atomicAdd(&p.ccount[s], tot) : 0;
+    }
+    __syncthreads();
+    int pos = s_warp[FILTER_THREADS / 32] + s_warp[warp];
+#pragma unroll
+    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
+        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
+        if ((ball[u] >> lane) & 1u) {
+            const int at = pos + __popc(ball[u] & ltmask);
+            if (at < CAND_CAP)
+                p.cand[static_cast<int64_t>(s) * CAND_CAP + at] =
+                    make_uint2(__float_as_uint(v[u]), static_cast<uint32_t>(b));
+            // the decode attention gathers the selected blocks' K and V rows
+            // right after the merge; the candidates include them, so their rows
+            // are brought into L2 now, while HBM is otherwise idle
+            if (p.kpre && at < p.pre_cap) {
+                const int64_t off = (static_cast<int64_t>(s) * p.m.max_ctx + b * kBlock) * (kHKV * kD);
+                prefetch_l2_bulk(p.kpre + off, kBlock * kHKV * kD * 2);
+                prefetch_l2_bulk(p.vpre + off, kBlock * kHKV * kD * 2);
+            }
+        }
+        pos += __popc(ball[u]);
+    }
+    if (p.kpre && blockIdx.x == 0 && threadIdx.x == 0) {  // the current block is always attended
+        const int64_t off = (static_cast<int64_t>(s) * p.m.max_ctx + c * kBlock) * (kHKV * kD);
+        prefetch_l2_bulk(p.kpre + off, kBlock * kHKV * kD * 2);
+        prefetch_l2_bulk(p.vpre + off, kBlock * kHKV * kD * 2);
+    }
+}
+
+// One CTA per sequence: the selection row, from the filter's candidates
+// (staged in shared memory) or, for rows that need no selection, directly.
+__global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    uint2 *items = reinterpret_cast<uint2 *>(smem);
+    uint32_t *sortb = reinterpret_cast<uint32_t *>(items + CAND_CAP);  // [1024]: sort input at 512..
+    uint32_t *hist = sortb + 1024;
+    int *ctl = reinterpret_cast<int *>(hist + 256);
+    pdl_trigger();
+    pdl_wait();  // candidates of the filter (and, through it, the scan's scores)
+    const int s = blockIdx.x;
+    if (trivial_row<MERGE_THREADS>(p, s, true)) return;
+    merge_row<MERGE_THREADS>(p, s, (p.seq_lens[s] - 1) / kBlock, items, CAND_CAP, sortb, hist, ctl);
 }
 
 }  // namespace dx
@@ -505,7 +647,7 @@ static size_t index_ws_bytes(int batch, int64_t max_ctx) {
     b += align256(static_cast<size_t>(batch) * (max_ctx / kBlock) * sizeof(float));      // scores
     b += align256(static_cast<size_t>(batch) * dx::CAND_CAP * sizeof(uint2));            // cand
     b += align256(static_cast<size_t>(batch) * sizeof(int32_t));                         // ccount
-    b += align256(static_cast<size_t>(batch) * dx::MAX_NCHUNK * sizeof(uint32_t));       // chunk bounds
+    b += align256(static_cast<size_t>(batch) * dx::MAX_NCHUNK * (dx::SCAN_THREADS / 32) * sizeof(uint32_t));  // bounds
     return b;
 }
 
@@ -523,7 +665,8 @@ size_t decode_index_ws_bytes(int batch, int64_t max_ctx) { return index_ws_bytes
 cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &plan,
                                 const uint16_t *qi, const uint16_t *w, const uint16_t *kblk,
                                 const int32_t *seq_lens, int budget, void *ws, int32_t *idx_out,
-                                int32_t *status, cudaStream_t stream) {
+                                int32_t *status, const uint16_t *k_cache, const uint16_t *v_cache,
+                                cudaStream_t stream) {
     const int k_sel = budget - 1;
     uint8_t *base = static_cast<uint8_t *>(ws);
     float *scores = reinterpret_cast<float *>(base);
@@ -533,6 +676,16 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
     int32_t *ccount = reinterpret_cast<int32_t *>(base);
     base += align256(static_cast<size_t>(batch) * sizeof(int32_t));
     uint32_t *lb = reinterpret_cast<uint32_t *>(base);
+    dx::MergeParams mp;
+    mp.seq_lens = seq_lens;
+    mp.max_ctx = max_ctx;
+    mp.k_sel = k_sel;
+    mp.budget = budget;
+    mp.scores = scores;
+    mp.cand = cand;
+    mp.ccount = ccount;
+    mp.idx = idx_out;
+    mp.status = status;
     cudaError_t e;
     if (k_sel > 0) {
         dx::ScanParams sp;
@@ -555,14 +708,17 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         dx::FilterParams fp;
-        fp.seq_lens = seq_lens;
-        fp.max_ctx = max_ctx;
-        fp.k_sel = k_sel;
-        fp.scores = scores;
+        fp.m = mp;
         fp.lb = lb;
         fp.nchunk = plan.nchunk;
         fp.cand = cand;
         fp.ccount = ccount;
+        // prefetch while the candidates' K and V rows fit in L2 beside the
+        // scores: about twice the budget per sequence, 8 KiB per block
+        const bool pre = static_cast<int64_t>(batch) * 2 * budget * 2 * kBlock * kHKV * kD * 2 <= dx::kPrefetchL2Bytes;
+        fp.kpre = pre ? k_cache : nullptr;
+        fp.vpre = pre ? v_cache : nullptr;
+        fp.pre_cap = 2 * budget;
         const int64_t cmax = (max_ctx - 1) / kBlock;
         const int64_t per_cta = static_cast<int64_t>(dx::FILTER_THREADS) * dx::FILTER_PER_THREAD;
         const int64_t fx = cmax > 0 ? (cmax + per_cta - 1) / per_cta : 1;
@@ -570,16 +726,6 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
                        stream, fp);
         if (e != cudaSuccess) return e;
     }
-    dx::MergeParams mp;
-    mp.seq_lens = seq_lens;
-    mp.max_ctx = max_ctx;
-    mp.k_sel = k_sel;
-    mp.budget = budget;
-    mp.scores = scores;
-    mp.cand = cand;
-    mp.ccount = ccount;
-    mp.idx = idx_out;
-    mp.status = status;
     const int smem = dx::CAND_CAP * 8 + 1024 * 4 + 256 * 4 + 8 * 4;
     e = cudaFuncSetAttribute(dx::merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;

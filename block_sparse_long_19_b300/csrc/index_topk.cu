@@ -120,19 +120,28 @@ __device__ __forceinline__ bool tile_skipped(const Params &p, int q) {
     return p.redo_pass && *reinterpret_cast<const uint32_t *>(p.redo + 4 * static_cast<int64_t>(q)) == 0u;
 }
 
-// One TMEM load of 16 columns and its completion wait in a single statement:
-// the chunk's values are ordinary outputs, so nothing can read them early
-// and the compiler needs no register ties across the wait.
-__device__ __forceinline__ void tmem_load16_sync(uint32_t taddr, uint32_t (&r)[16]) {
+// A TMEM load of 16 columns (32 lanes x 32 bit), and the wait for every
+// outstanding TMEM load.  The chunk loop issues chunk ch+1's load before
+// chunk ch's arithmetic and waits after it, so the load's latency is hidden.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
           "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
+}
+// The wait names r (the registers of the load in flight) as in-out operands,
+// so no use of them can move above it.
+__device__ __forceinline__ void tmem_wait16(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                   "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                   "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
 }
 
 // Bounded wait on an mbarrier phase that gives the issue slots away while it
@@ -789,15 +798,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool masked = !(tile_all_in && (static_cast<int64_t>(j) * TB + TB <= c_min));
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        buf * NCOL + static_cast<uint32_t>(g * GCOL);
-                // 4 chunks of 4 tokens (16 columns each); the TMEM load latency is
-                // short next to a chunk's arithmetic, so each chunk loads and waits
-                uint32_t cur[16];
+                // 4 chunks of 4 tokens (16 columns each), each chunk's TMEM load
+                // in flight during the arithmetic of the chunk before it
+                uint32_t curb[2][16];
                 // MASKED: the tile holds blocks that some of the tokens may not see
                 auto score_tile = [&](auto masked_c) {
                     constexpr bool MASKED = decltype(masked_c)::value;
+                    tmem_ld16(tbase, curb[0]);
+                    tmem_wait16(curb[0]);
 #pragma unroll
                     for (int ch = 0; ch < GTOK / 4; ++ch) {
-                        tmem_load16_sync(tbase + ch * 16, cur);
+                        uint32_t (&cur)[16] = curb[ch & 1];
+                        if (ch + 1 < GTOK / 4) tmem_ld16(tbase + (ch + 1) * 16, curb[(ch + 1) & 1]);
                         const int tl0 = g * GTOK + ch * 4;
                         // s = sum_h w_h * max(0, x_h) for two tokens per packed FMA,
                         // heads in order 0..3, the first product added to +0 (the
@@ -842,10 +854,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 const int64_t t = t0 + tl0 + tk;
                                 const bool valid = !MASKED || ((t < p.L) && (b < (t >> p.bshift)));
                                 pass[tk] = valid && (sv[tk] >= thv[tk]);
-                                m[tk] = __ballot_sync(0xFFFFFFFFu, pass[tk]);
                             }
                             // a block enters the token's list when s >= its threshold
-                            if ((m[0] | m[1] | m[2] | m[3]) != 0u) {
+                            if (__any_sync(0xFFFFFFFFu, pass[0] | pass[1] | pass[2] | pass[3])) {
+#pragma unroll
+                                for (int tk = 0; tk < 4; ++tk) m[tk] = __ballot_sync(0xFFFFFFFFu, pass[tk]);
                                 uint2 *base = sub + static_cast<int64_t>(tl0) * CAP;
                                 const int cnt4[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
@@ -861,6 +874,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 }
                             }
                         }
+                        if (ch + 1 < GTOK / 4) tmem_wait16(curb[(ch + 1) & 1]);
                     }
                 };
                 if (masked) score_tile(std::true_type{});

@@ -791,7 +791,7 @@ qsa_status qsa_sparse_attn_decode(const qsa_config *cfg, int batch, const qsa_bf
     int32_t *idx = idx_out ? idx_out : idx_ws;
 
     cudaError_t e = qsa::launch_decode_index(batch, max_ctx, plan, qi, w, kblk_cache, seq_lens,
-                                             budget, cand_region, idx, dev_status, s);
+                                             budget, cand_region, idx, dev_status, k_cache, v_cache, s);
     if (e != cudaSuccess) return cuda_fail(e, "decode indexer launch");
     qsa::AttnArgs a{};
     a.q = q;

@@ -82,9 +82,12 @@ struct DecodePlan {
 DecodePlan decode_plan(int batch, int64_t max_ctx, int sms);
 size_t decode_ws_bytes(int batch, int64_t max_ctx, int budget, int sms);
 size_t decode_index_ws_bytes(int batch, int64_t max_ctx);  // leading part of the decode workspace
+// k_cache / v_cache (or null): the filter prefetches the K and V rows of its
+// candidate blocks into L2 for the decode attention that follows.
 cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &plan,
                                 const uint16_t *qi, const uint16_t *w, const uint16_t *kblk,
                                 const int32_t *seq_lens, int budget, void *ws, int32_t *idx_out,
-                                int32_t *status, cudaStream_t stream);
+                                int32_t *status, const uint16_t *k_cache, const uint16_t *v_cache,
+                                cudaStream_t stream);
 
 }  // namespace qsa

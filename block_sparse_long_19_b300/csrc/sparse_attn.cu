@@ -114,10 +114,6 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     const int64_t c = t / kBlock;
 
     // ---------------------------------------------- phase 1: idx, cos/sin --
-    if constexpr (DECODE) {
-        pdl_trigger();
-        pdl_wait();  // the selection of the decode indexer
-    }
     if (threadIdx.x == 0) {
         for (int i = 0; i < NST; ++i) {
             mbar_init(&full[i], 2);  // the K and the V producer arrive
@@ -125,47 +121,30 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
         }
         fence_barrier_init();
     }
-    for (int i = threadIdx.x; i < a.budget; i += THREADS) {
-        int b = irow[i];
-#if QSA_DEBUG_CHECKS
-        {  // a row as the indexer writes it: past blocks ascending, block c last, -1 padding
-            const int nxt = i + 1 < a.budget ? irow[i + 1] : -1;
-            bool row_ok = b >= -1 && b <= c && (i > 0 || b >= 0);
-            if (b >= 0) row_ok = row_ok && (nxt < 0 ? b == c : b < nxt);
-            else row_ok = row_ok && nxt < 0;
-            debug_check(a.status, row_ok);
-        }
-#endif
-        if (b < 0 || b > c) b = -1;  // out-of-range entries are ignored
-        sIdx[i] = b;
-    }
     if (threadIdx.x < 32) {
         float cs, sn;
         rope_cos_sin(t, f.inv_freq[threadIdx.x], cs, sn);
         sCS[threadIdx.x] = cs;
         sCS[32 + threadIdx.x] = sn;
     }
-    __syncthreads();
-
-    // ---------------------------------- phase 2: slot count, Q with RoPE --
-    // Every warp counts the used slots itself; the producer starts its copies
-    // right away while the consumer warps put Q (with RoPE) into shared
-    // memory, so the first stages are in flight during that set-up.
-    int nslot = 0;
-    for (int base = 0; base < a.budget; base += 32) {
-        const int i = base + lane;
-        const unsigned ball = __ballot_sync(0xFFFFFFFFu, i < a.budget && sIdx[i] >= 0);
-        if (ball) nslot = base + 32 - __clz(ball);
-    }
-    const int total_st = (nslot + SBLK - 1) / SBLK;
-    int st_begin = 0, st_end = total_st;
-    if constexpr (DECODE) {
-        const int per = (total_st + a.nsplit - 1) / a.nsplit;
-        st_begin = split * per;
-        st_end = min(total_st, st_begin + per);
-        if (st_begin > st_end) st_begin = st_end;
-    }
-    if (warp > 0 && warp <= NCONS) {
+    auto load_idx = [&]() {
+        for (int i = threadIdx.x; i < a.budget; i += THREADS) {
+            int b = irow[i];
+#if QSA_DEBUG_CHECKS
+            {  // a row as the indexer writes it: past blocks ascending, block c last, -1 padding
+                const int nxt = i + 1 < a.budget ? irow[i + 1] : -1;
+                bool row_ok = b >= -1 && b <= c && (i > 0 || b >= 0);
+                if (b >= 0) row_ok = row_ok && (nxt < 0 ? b == c : b < nxt);
+                else row_ok = row_ok && nxt < 0;
+                debug_check(a.status, row_ok);
+            }
+#endif
+            if (b < 0 || b > c) b = -1;  // out-of-range entries are ignored
+            sIdx[i] = b;
+        }
+    };
+    // the consumer warps put Q (with RoPE) into shared memory
+    auto q_rope = [&]() {
         const int ct = threadIdx.x - 32;
         constexpr int CT = NCONS * 32;
         for (int i = ct; i < kHQ * 32; i += CT) {
@@ -190,6 +169,41 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
             *reinterpret_cast<uint4 *>(sQ + g * 16 * QROW + r * QROW + v * 16) = make_uint4(0, 0, 0, 0);
         }
         named_bar(1, CT);  // Q complete before any consumer reads it
+    };
+    const bool consumer = warp > 0 && warp <= NCONS;
+    if constexpr (DECODE) {
+        // the query, its RoPE and the barriers do not depend on the decode
+        // indexer: they are set up while it finishes, then the selection is read
+        pdl_trigger();
+        __syncthreads();
+        if (consumer) q_rope();
+        pdl_wait();  // the selection of the decode indexer
+        load_idx();
+        __syncthreads();
+    } else {
+        load_idx();
+        __syncthreads();
+    }
+
+    // ---------------------------------- phase 2: slot count, Q with RoPE --
+    // Every warp counts the used slots itself; in prefill the producer starts
+    // its copies right away while the consumer warps put Q (with RoPE) into
+    // shared memory, so the first stages are in flight during that set-up.
+    int nslot = 0;
+    for (int base = 0; base < a.budget; base += 32) {
+        const int i = base + lane;
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, i < a.budget && sIdx[i] >= 0);
+        if (ball) nslot = base + 32 - __clz(ball);
+    }
+    const int total_st = (nslot + SBLK - 1) / SBLK;
+    int st_begin = 0, st_end = total_st;
+    if constexpr (DECODE) {
+        const int per = (total_st + a.nsplit - 1) / a.nsplit;
+        st_begin = split * per;
+        st_end = min(total_st, st_begin + per);
+        if (st_begin > st_end) st_begin = st_end;
+    } else {
+        if (consumer) q_rope();
     }
 
     if (warp == 0 || warp == WARP_VPROD) {
@@ -454,6 +468,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
 }
 
 // Merge decode splits: O = sum_i e^(lse_i - M) O_i / sum_i e^(lse_i - M).
+// All of a thread's loads are issued before their values are used (split
+// LSEs, then the partial outputs), so the merge costs two round trips to L2
+// instead of one per split.
+constexpr int kMaxSplits = 16;
 __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ part_o,
                                                       const float *__restrict__ part_lse,
                                                       int nsplit, uint16_t *__restrict__ out,
@@ -462,17 +480,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
     const int s = blockIdx.x / kHQ;
     const int h = blockIdx.x % kHQ;
     const int d = threadIdx.x;
+    float li[kMaxSplits], oi[kMaxSplits];
+#pragma unroll
+    for (int i = 0; i < kMaxSplits; ++i)
+        li[i] = i < nsplit ? __ldcg(part_lse + (static_cast<int64_t>(s) * nsplit + i) * kHQ + h) : -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxSplits; ++i)
+        oi[i] = i < nsplit ? __ldcg(part_o + ((static_cast<int64_t>(s) * nsplit + i) * kHQ + h) * kD + d) : 0.f;
     float M = -INFINITY;
-    for (int i = 0; i < nsplit; ++i)
-        M = fmaxf(M, part_lse[(static_cast<int64_t>(s) * nsplit + i) * kHQ + h]);
+#pragma unroll
+    for (int i = 0; i < kMaxSplits; ++i) M = fmaxf(M, li[i]);
     float den = 0.f, acc = 0.f;
     if (M > -INFINITY) {
-        for (int i = 0; i < nsplit; ++i) {
-            const float li = part_lse[(static_cast<int64_t>(s) * nsplit + i) * kHQ + h];
-            if (li == -INFINITY) continue;
-            const float wgt = __expf(li - M);
+#pragma unroll
+        for (int i = 0; i < kMaxSplits; ++i) {
+            if (li[i] == -INFINITY) continue;  // an empty split (or one past nsplit)
+            const float wgt = __expf(li[i] - M);
             den += wgt;
-            acc += wgt * part_o[((static_cast<int64_t>(s) * nsplit + i) * kHQ + h) * kD + d];
+            acc += wgt * oi[i];
         }
     }
     const float o = den > 0.f ? acc / den : 0.f;
