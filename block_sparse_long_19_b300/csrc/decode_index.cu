@@ -46,6 +46,7 @@ constexpr int MERGE_THREADS = 256;
 constexpr int FILTER_THREADS = 256;
 constexpr int FILTER_PER_THREAD = 8;
 constexpr int CAND_CAP = 8192;  // filtered candidates kept per sequence
+constexpr int CCOUNT_STRIDE = 32;  // ints between two sequences' candidate counters (128 B)
 constexpr int64_t kPrefetchL2Bytes = int64_t(72) << 20;  // L2 budget of the filter's K/V prefetch
 
 // CTA-wide radix step over n items: value(i) -> uint32, pred(i) -> bool.
@@ -186,6 +187,30 @@ __device__ __forceinline__ bool selected(const SelectRule &r, float s, uint32_t 
     return key > r.thr_key || (key == r.thr_key && ~b >= r.thr_nblk);
 }
 
+// How the scan bounds a sequence with c past blocks (see scan_kernel), and
+// where the bound slots that the filter reduces sit: chunk and radix modes
+// fill slot 0 of each chunk, warp mode the slots of every warp.
+constexpr int SCAN_WARPS = SCAN_THREADS / 32;
+struct BoundMode {
+    int64_t nch;     // chunks of the sequence
+    int kc, kw;      // ranks of the chunk and of the warp bounds
+    bool chunk_mode, warp_mode;
+};
+__device__ __forceinline__ BoundMode bound_mode(int64_t c, int64_t chunk, int k_sel) {
+    // 32-bit arithmetic: c < 2^20 blocks per sequence, chunk <= MAX_CHUNK
+    BoundMode m;
+    const int ci = static_cast<int>(c), chi = static_cast<int>(chunk);
+    const int nch = (ci + chi - 1) / chi;
+    m.nch = nch;
+    m.kc = nch == 1 ? k_sel : (k_sel + nch - 2) / (nch - 1);
+    const int wfull = (nch - 1) * SCAN_WARPS;  // warps of full chunks: >= chunk / 8 >= 128 scores each
+    m.kw = wfull > 1 ? (k_sel + wfull - 2) / (wfull - 1) : KW_MAX + 1;
+    const bool sel_needed = c > k_sel && m.nch > 1;
+    m.chunk_mode = sel_needed && m.kc <= KW_MAX;
+    m.warp_mode = sel_needed && !m.chunk_mode && m.kw <= KW_MAX;
+    return m;
+}
+
 struct ScanParams {
     const uint16_t *qi;        // [B, 4, 128]
     const uint16_t *w;         // [B, 4]
@@ -197,11 +222,11 @@ struct ScanParams {
     int k_sel;
     float *scores;             // [B, max_ctx/4]
     uint32_t *lb;              // [B, nchunk, SCAN_THREADS / 32] bound keys of the chunks or their warps (0xFFFFFFFF: none)
-    int32_t *ccount;           // [B] candidate counters, zeroed here for the filter
+    int32_t *ccount;           // [B x CCOUNT_STRIDE] candidate counters, zeroed here for the filter
     int32_t *status;
 };
 
-__global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
+__global__ void __launch_bounds__(SCAN_THREADS, 2) scan_kernel(ScanParams p) {
     extern __shared__ __align__(16) uint8_t smem[];
     float *sc = reinterpret_cast<float *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + p.chunk * 4);  // dynamic size: chunk*4 + 256*4 + 32
@@ -217,7 +242,7 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     // here and is the only thread that writes it below
     uint32_t *lb_out = p.lb + (static_cast<int64_t>(s) * p.nchunk + ch) * NW;
     if (lane == 0) lb_out[warp] = 0xFFFFFFFFu;
-    if (threadIdx.x == 0 && ch == 0) p.ccount[s] = 0;
+    if (threadIdx.x == 0 && ch == 0) p.ccount[static_cast<int64_t>(s) * CCOUNT_STRIDE] = 0;
     if (T < 1 || T > p.max_ctx) {
         if (threadIdx.x == 0) report(p.status, QSA_ERR_DEVICE_CHECK);
         return;
@@ -252,13 +277,9 @@ __global__ void __launch_bounds__(SCAN_THREADS) scan_kernel(ScanParams p) {
     //  * warp (kw <= KW_MAX): each warp's kw-th best with kw = ceil((budget-1)
     //    / (warps of full chunks - 1)), looser but with no merge across warps;
     //  * otherwise the chunk's kc-th best by a CTA radix after the stream.
-    const int64_t nch_s = (c + p.chunk - 1) / p.chunk;
-    const int kc = nch_s == 1 ? p.k_sel : static_cast<int>((p.k_sel + nch_s - 2) / (nch_s - 1));
-    const int64_t wfull = (nch_s - 1) * NW;  // warps of full chunks: >= chunk / NW >= 128 scores each
-    const int kw = wfull > 1 ? static_cast<int>((p.k_sel + wfull - 2) / (wfull - 1)) : KW_MAX + 1;
-    const bool sel_needed = c > p.k_sel && nch_s > 1;
-    const bool chunk_mode = sel_needed && kc <= KW_MAX;
-    const bool warp_mode = sel_needed && !chunk_mode && kw <= KW_MAX;
+    const BoundMode bm = bound_mode(c, p.chunk, p.k_sel);
+    const int kc = bm.kc, kw = bm.kw;
+    const bool chunk_mode = bm.chunk_mode, warp_mode = bm.warp_mode;
     const bool keep_top = chunk_mode || warp_mode;
     uint32_t top[KW_MAX];  // this lane's best keys, descending (lanes with qd == 0 hold scores)
 #pragma unroll
@@ -390,7 +411,7 @@ struct MergeParams {
     int budget;
     const float *scores;    // [B, max_ctx/4] (used when the candidates overflowed)
     const uint2 *cand;      // [B, CAND_CAP]
-    const int32_t *ccount;  // [B]
+    const int32_t *ccount;  // [B x CCOUNT_STRIDE]
     int32_t *idx;           // [B, budget]
     int32_t *status;
 };
@@ -407,7 +428,7 @@ __device__ void merge_row(const MergeParams &p, int s, int64_t c, uint2 *items, 
     int32_t *row = p.idx + static_cast<int64_t>(s) * p.budget;
     const int lane = threadIdx.x & 31;
     const unsigned ltmask = (1u << lane) - 1u;
-    const int nc = __ldcg(p.ccount + s);
+    const int nc = __ldcg(p.ccount + static_cast<int64_t>(s) * CCOUNT_STRIDE);
     const bool direct = nc > CAND_CAP;  // ties flooded the candidate area
     const bool staged = !direct && nc <= items_cap;
     const int n = direct ? static_cast<int>(c) : nc;
@@ -500,8 +521,9 @@ struct FilterParams {
     MergeParams m;           // lengths, budget and scores of the sequences
     const uint32_t *lb;      // [B, nchunk, SCAN_THREADS / 32]
     int nchunk;
+    int64_t chunk;           // blocks per scan chunk
     uint2 *cand;             // [B, CAND_CAP] {score bits, block}
-    int32_t *ccount;         // [B] candidates reserved
+    int32_t *ccount;         // [B x CCOUNT_STRIDE] candidates reserved
     const uint16_t *kpre;    // [B, max_ctx, 2, 256] K cache to prefetch into L2 (or null)
     const uint16_t *vpre;    // [B, max_ctx, 2, 256] V cache
     int pre_cap;             // candidates prefetched per sequence at most
@@ -509,8 +531,8 @@ struct FilterParams {
 
 // Candidates: the past blocks whose score key reaches the sequence's bound.
 // One global atomic per CTA reserves the CTA's range of the candidate area
-// (the sequences' counters share cache lines, so per-warp atomics from every
-// CTA would queue up at one L2 slice).
+// (per-warp atomics from every CTA would queue up at the counter's L2 slice);
+// the sequences' counters sit 128 bytes apart, on cache lines of their own.
 __global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) {
     __shared__ int s_warp[FILTER_THREADS / 32 + 1];
     pdl_trigger();
@@ -518,32 +540,34 @@ __global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) 
     const int s = blockIdx.y;
     if (trivial_row<FILTER_THREADS>(p.m, s, false)) return;  // the merge writes that row
     const int64_t c = (p.m.seq_lens[s] - 1) / kBlock;
-    // the bound: the smallest chunk or warp bound (slots that bound nothing
-    // hold 0xFFFFFFFF); every warp reduces the slots itself
-    constexpr int SW = SCAN_THREADS / 32;  // bound slots per chunk
-    const uint32_t *lbs = p.lb + static_cast<int64_t>(s) * p.nchunk * SW;
-    const int ln = threadIdx.x & 31;
-    uint32_t bound = 0xFFFFFFFFu;
-    for (int i = ln; i < p.nchunk * SW; i += 32) bound = min(bound, __ldcg(lbs + i));
-    bound = __reduce_min_sync(0xFFFFFFFFu, bound);
     const float *srow = p.m.scores + static_cast<int64_t>(s) * (p.m.max_ctx / kBlock);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned ltmask = (1u << lane) - 1u;
+    // this CTA's scores: all loads in flight at once, before the bound is known
     const int64_t base = static_cast<int64_t>(blockIdx.x) * FILTER_THREADS * FILTER_PER_THREAD;
     float v[FILTER_PER_THREAD];
-    unsigned ball[FILTER_PER_THREAD];
-    int mine = 0;
 #pragma unroll
     for (int u = 0; u < FILTER_PER_THREAD; ++u) {
         const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
         v[u] = b < c ? __ldcg(srow + b) : -INFINITY;
     }
+    // the bound: the smallest chunk or warp bound (slots that bound nothing
+    // hold 0xFFFFFFFF); every warp reduces the slots itself
+    const uint32_t *lbs = p.lb + static_cast<int64_t>(s) * p.nchunk * SCAN_WARPS;
+    const BoundMode bm = bound_mode(c, p.chunk, p.m.k_sel);
+    const int per = bm.warp_mode ? SCAN_WARPS : 1;  // slots read per chunk
+    const int nslot = static_cast<int>(bm.nch) * per;
+    uint32_t bound = 0xFFFFFFFFu;
+#pragma unroll 4
+    for (int i = lane; i < nslot; i += 32)
+        bound = min(bound, __ldcg(lbs + (per == 1 ? static_cast<int64_t>(i) * SCAN_WARPS : i)));
+    bound = __reduce_min_sync(0xFFFFFFFFu, bound);
+    auto keep = [&](int u) {
+        return base + u * FILTER_THREADS + threadIdx.x < c && f2key(v[u]) >= bound;
+    };
+    int mine = 0;
 #pragma unroll
-    for (int u = 0; u < FILTER_PER_THREAD; ++u) {
-        const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
-        ball[u] = __ballot_sync(0xFFFFFFFFu, b < c && f2key(v[u]) >= bound);
-        mine += __popc(ball[u]);
-    }
+    for (int u = 0; u < FILTER_PER_THREAD; ++u) mine += __popc(__ballot_sync(0xFFFFFFFFu, keep(u)));
     if (lane == 0) s_warp[warp] = mine;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -553,15 +577,18 @@ __global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) 
             s_warp[w] = tot;
             tot += x;
         }
-        s_warp[FILTER_THREADS / 32] = tot > 0 ? atomicAdd(&p.ccount[s], tot) : 0;
+        s_warp[FILTER_THREADS / 32] =
+            tot > 0 ? atomicAdd(&p.ccount[static_cast<int64_t>(s) * CCOUNT_STRIDE], tot) : 0;
     }
     __syncthreads();
     int pos = s_warp[FILTER_THREADS / 32] + s_warp[warp];
 #pragma unroll
     for (int u = 0; u < FILTER_PER_THREAD; ++u) {
         const int64_t b = base + u * FILTER_THREADS + threadIdx.x;
-        if ((ball[u] >> lane) & 1u) {
-            const int at = pos + __popc(ball[u] & ltmask);
+        const bool k = keep(u);
+        const unsigned ball = __ballot_sync(0xFFFFFFFFu, k);
+        if (k) {
+            const int at = pos + __popc(ball & ltmask);
             if (at < CAND_CAP)
                 p.cand[static_cast<int64_t>(s) * CAND_CAP + at] =
                     make_uint2(__float_as_uint(v[u]), static_cast<uint32_t>(b));
@@ -574,7 +601,7 @@ __global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) 
                 prefetch_l2_bulk(p.vpre + off, kBlock * kHKV * kD * 2);
             }
         }
-        pos += __popc(ball[u]);
+        pos += __popc(ball);
     }
     if (p.kpre && blockIdx.x == 0 && threadIdx.x == 0) {  // the current block is always attended
         const int64_t off = (static_cast<int64_t>(s) * p.m.max_ctx + c * kBlock) * (kHKV * kD);
@@ -646,7 +673,7 @@ static size_t index_ws_bytes(int batch, int64_t max_ctx) {
     size_t b = 0;
     b += align256(static_cast<size_t>(batch) * (max_ctx / kBlock) * sizeof(float));      // scores
     b += align256(static_cast<size_t>(batch) * dx::CAND_CAP * sizeof(uint2));            // cand
-    b += align256(static_cast<size_t>(batch) * sizeof(int32_t));                         // ccount
+    b += align256(static_cast<size_t>(batch) * dx::CCOUNT_STRIDE * sizeof(int32_t));     // ccount
     b += align256(static_cast<size_t>(batch) * dx::MAX_NCHUNK * (dx::SCAN_THREADS / 32) * sizeof(uint32_t));  // bounds
     return b;
 }
@@ -674,7 +701,7 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
     uint2 *cand = reinterpret_cast<uint2 *>(base);
     base += align256(static_cast<size_t>(batch) * dx::CAND_CAP * sizeof(uint2));
     int32_t *ccount = reinterpret_cast<int32_t *>(base);
-    base += align256(static_cast<size_t>(batch) * sizeof(int32_t));
+    base += align256(static_cast<size_t>(batch) * dx::CCOUNT_STRIDE * sizeof(int32_t));
     uint32_t *lb = reinterpret_cast<uint32_t *>(base);
     dx::MergeParams mp;
     mp.seq_lens = seq_lens;
@@ -711,6 +738,7 @@ cudaError_t launch_decode_index(int batch, int64_t max_ctx, const DecodePlan &pl
         fp.m = mp;
         fp.lb = lb;
         fp.nchunk = plan.nchunk;
+        fp.chunk = plan.chunk;
         fp.cand = cand;
         fp.ccount = ccount;
         // prefetch while the candidates' K and V rows fit in L2 beside the
