@@ -49,7 +49,9 @@ constexpr int QROW = kD * 2 + 16;         // 528 B per query row in smem
 constexpr int Q_BYTES = kHKV * 16 * QROW;
 constexpr int NCONS = 4;
 constexpr int WARP_VPROD = 1 + NCONS;    // the V producer (warp 0 produces K)
-constexpr int THREADS = 32 * (2 + NCONS);
+constexpr int WARP_PF = 2 + NCONS;       // brings the blocks of later stages into L2
+constexpr int PF_AHEAD = 10;             // stages the L2 prefetch runs ahead of the K producer
+constexpr int THREADS = 32 * (3 + NCONS);
 constexpr int OFF_BAR = 0;
 constexpr int OFF_IDX = 128;
 constexpr int OFF_CS = OFF_IDX + kMaxBudget * 4;
@@ -119,6 +121,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
             mbar_init(&full[i], 2);  // the K and the V producer arrive
             mbar_init(&empty[i], NCONS);
         }
+        sMisc[2] = -1;  // the last stage the K producer has issued
         fence_barrier_init();
     }
     if (threadIdx.x < 32) {
@@ -206,6 +209,36 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
         if (consumer) q_rope();
     }
 
+    if (warp == WARP_PF) {
+        // ------------------------------------------------ L2 prefetch --
+        // The ring holds NST stages, about two of them in flight: per SM
+        // that is too few bytes to cover the HBM latency at full bandwidth,
+        // so the kernel needs many SMs to reach it.  This warp brings the K
+        // and V blocks of stages up to PF_AHEAD ahead of the K producer into
+        // L2 (lanes 0-7 K, 8-15 V), so the ring's copies are served from L2
+        // and fewer SMs saturate HBM.  A hint only: it gives up (nothing else
+        // depends on it) if the producer stalls.
+        const unsigned long long t0 = globaltimer();
+        const int sl = lane & 7;
+        const bool isv = lane >= 8;
+        for (int st = st_begin + NST; st < st_end; ++st) {
+            bool go = true;
+            while (sMisc[2] < st - PF_AHEAD) {
+                if (sMisc[1] || globaltimer() - t0 > kWaitLimitNs) { go = false; break; }
+                __nanosleep(256);
+            }
+            if (!__all_sync(0xFFFFFFFFu, go)) break;
+            if (lane < 16) {
+                const int si = st * SBLK + sl;
+                const int b = si < a.budget ? sIdx[si] : -1;
+                if (b >= 0 && b < c)
+                    prefetch_l2_bulk((isv ? vbase : kbase) + static_cast<int64_t>(b) * kBlock * (kHKV * kD),
+                                     kBlock * ROWB);
+            }
+        }
+        return;
+    }
+
     if (warp == 0 || warp == WARP_VPROD) {
         // ------------------------------------------------ producers --
         // warp 0 copies K, warp WARP_VPROD copies V: lanes 0..7 the block of
@@ -226,7 +259,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
             if (lane == 0) ok = mbar_wait(&empty[slot], ph ^ 1);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&full[slot], SBLK * kBlock * ROWB);  // this producer's half
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[slot], SBLK * kBlock * ROWB);  // this producer's half
+                if (!isv) sMisc[2] = st;  // paces the L2 prefetch
+            }
             __syncwarp();
             if (lane < SBLK) {
                 const int si = st * SBLK + sl;
