@@ -232,11 +232,11 @@ void set_error_detail(const char *msg) { g_detail = msg; }
 // per chunk from per-SM costs fitted to B300 runs of both kernels, side by
 // side, at 128K and 1M tokens: the indexer takes 2.14e-10 SM-seconds per
 // (query, past block) pair plus 8.2e-6 per query row (its list start-up and
-// final selection); the attention is costed at 55 GB/s of gathered K/V per
-// SM (2 KiB per attended key), never below 6.9 TB/s for the whole GPU.  (The
-// attention's own rate per SM is higher since its L2 prefetch; a lower
-// costed rate gives it more SMs, which measured faster for the whole step
-// at 1M than the fitted 65 GB/s or anything above it.)
+// final selection); the attention consumes 65 GB/s of gathered K/V per SM
+// (2 KiB per attended key) and cannot go below 6.9 TB/s for the whole GPU.
+// (Costing the attention at 55 GB/s per SM, i.e. giving it more SMs, was 5
+// ms faster at 1M on i.i.d. inputs but 61 ms slower with topic segments,
+// where the indexer is slower than the fit.)
 // Below 256K tokens the attention's K/V mostly sits in L2 and the attention
 // is bound by its SMs rather than by HBM, so there is nothing to hand to the
 // indexer: shorter prefills run the two stages one after the other.
@@ -246,7 +246,7 @@ constexpr int64_t kOverlapMinL = 262144;
 
 constexpr double kIdxPairSm = 2.14e-10;
 constexpr double kIdxRowSm = 8.2e-6;
-constexpr double kAttnKeySm = 2048.0 / 55e9;
+constexpr double kAttnKeySm = 2048.0 / 65e9;
 constexpr double kAttnKeyFloor = 2048.0 / 6.9e12;
 
 // sum over t in [r0, r1) of floor(t/4): the pairs the indexer scores
