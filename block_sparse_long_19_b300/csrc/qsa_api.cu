@@ -243,6 +243,7 @@ void set_error_detail(const char *msg) { g_detail = msg; }
 namespace {
 
 constexpr int64_t kOverlapMinL = 262144;
+constexpr int kEdgeParts = 4;  // parts of the first and of the last chunk
 
 constexpr double kIdxPairSm = 2.14e-10;
 constexpr double kIdxRowSm = 8.2e-6;
@@ -474,7 +475,18 @@ int qsa_prefill_overlap_plan(const qsa_config *cfg, int64_t L, int sms, int max_
         index_ctas[0] = sms;
         return 1;
     }
-    for (int64_t j = 0; j < n; ++j) chunk_begin[j] = j * rows;
+    // the first and the last chunk in kEdgeParts parts each (64-row tiles):
+    // only the first part's indexer runs alone, and only the last part's
+    // attention, so the pipeline fills and drains in a quarter of a chunk
+    int64_t m = 0;
+    const bool split = n >= 2 && rows / kEdgeParts >= tq && n + 2 * (kEdgeParts - 1) <= max_chunks;
+    for (int64_t j = 0; j < n; ++j) {
+        const int64_t a = j * rows, b = j + 1 < n ? (j + 1) * rows : L;
+        const int parts = split && (j == 0 || j == n - 1) ? kEdgeParts : 1;
+        const int64_t step = ((b - a) / parts) / tq * tq;
+        for (int k = 0; k < parts; ++k) chunk_begin[m++] = a + k * step;
+    }
+    n = m;
     chunk_begin[n] = L;
     index_ctas[0] = sms;  // the first chunk's indexer runs alone
     for (int64_t j = 1; j < n; ++j) {

@@ -524,23 +524,6 @@ def prefill_overlapped(cfg: Config, q, k, v, qi, w, ki, k_rot=None, idx=None, sc
     return PrefillResult(idx, score, k_rot, out, lse, status)
 
 
-def split_edge_chunks(begin, ctas, parts: int = 4):
-    """Chunk starts and indexer grids of prefill_overlap_plan() with the first
-    and the last chunk split into `parts` parts on 64-row tiles (each part
-    keeps its chunk's indexer grid): HostPrefill's first part computes as soon
-    as it has arrived, and its last part's copy back is short.  Returns
-    (bounds, ctas) with len(bounds) == len(ctas) + 1."""
-    bounds, out = [0], []
-    for j, (a, b) in enumerate(zip(begin[:-1], begin[1:])):
-        n = parts if j in (0, len(ctas) - 1) else 1
-        step = max(64, ((b - a) // n) // 64 * 64)
-        cuts = [c for c in range(a + step, b, step)][: n - 1]
-        for c in cuts + [b]:
-            bounds.append(c)
-            out.append(ctas[j])
-    return bounds, out
-
-
 class HostPrefill:
     """Prefill of one sequence whose inputs live in pinned host memory.
 
@@ -548,18 +531,18 @@ class HostPrefill:
     calls (each chunk's rows against every earlier token), so the host->device
     copies of chunk c+1 and the device->host copy of chunk c-1's output run on
     their own streams while chunk c computes.  For long prefills the chunks
-    and indexer grid sizes are those of prefill_overlapped() (its first and
-    last chunk split into `edge_parts` parts, to shorten the pipeline's fill
-    and drain): the K-prep and indexer of a chunk run on a higher-priority
-    stream on a share of the SMs while the attention of the previous chunk
-    runs on the rest.  The results
+    and indexer grid sizes are those of prefill_overlapped() (whose first and
+    last chunk come in four parts, a short pipeline fill and drain): the
+    K-prep and indexer of a chunk run on a higher-priority stream on a share
+    of the SMs while the attention of the previous chunk runs on the rest.
+    The results
     equal those of prefill() on the whole sequence (the per-query computation
     does not depend on the chunking).  Device buffers are allocated once,
     here."""
 
     NAMES = ("q", "k", "v", "qi", "w", "ki")
 
-    def __init__(self, cfg: Config, L: int, chunk_tokens: int = 65536, device="cuda", edge_parts: int = 4):
+    def __init__(self, cfg: Config, L: int, chunk_tokens: int = 65536, device="cuda"):
         self.cfg, self.L, self.dev = cfg, L, device
         self.chunk = max(64, (chunk_tokens // 64) * 64)
         shapes = {"q": (L, 24, 256), "k": (L, 2, 256), "v": (L, 2, 256), "qi": (L, 4, 128), "w": (L, 4),
@@ -574,7 +557,7 @@ class HostPrefill:
         sms = torch.cuda.get_device_properties(device).multi_processor_count
         begin, ctas = prefill_overlap_plan(cfg, L, sms)
         if len(ctas) > 1:
-            self.bounds, self.ctas = split_edge_chunks(begin, ctas, edge_parts)
+            self.bounds, self.ctas = list(begin), list(ctas)
         else:
             self.bounds = list(range(0, L, self.chunk)) + [L]
             self.ctas = None

@@ -250,7 +250,9 @@ qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 
  * results).  The indexer's time goes to instruction issue and the
  * attention's to HBM bytes, so the query rows are cut into chunks and the
  * indexer of chunk j runs on a share of the SMs while the attention of chunk
- * j-1 runs on the rest.
+ * j-1 runs on the rest; the first and the last chunk come in four parts, so
+ * the stages run alone (the first indexer, the last attention) for a quarter
+ * of a chunk only.
  *   q [L, 24, 256], qi [L, 4, 128], w [L, 4], ki [L, 128], k [L, 2, 256]
  *   (before RoPE), k_rot [L, 2, 256] out (may equal k), v [L, 2, 256];
  *   idx [L, budget] and score [L, budget] (or NULL) as for qsa_index_topk;
@@ -273,7 +275,9 @@ qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 
  *   (chunk_begin[0] = 0, chunk_begin[n] = L; every inner start a multiple of
  *   64) and n indexer grid sizes (index_ctas[0] = sms: the first chunk's
  *   indexer runs alone), and returns n (1 <= n <= max_chunks), or 0 on
- *   invalid arguments.  chunk_begin needs max_chunks + 1 entries.
+ *   invalid arguments.  chunk_begin needs max_chunks + 1 entries.  The first
+ *   and the last four chunks are the parts of the edge chunks when max_chunks
+ *   leaves room for them (22 chunks at 1,048,576 tokens).
  * ---------------------------------------------------------------------- */
 size_t qsa_prefill_overlapped_workspace_bytes(const qsa_config *cfg, int64_t L);
 qsa_status qsa_prefill_overlapped(const qsa_config *cfg, const qsa_bf16 *q, const qsa_bf16 *qi,
@@ -297,7 +301,9 @@ int qsa_prefill_overlap_plan(const qsa_config *cfg, int64_t L, int sms, int max_
  *   out      [batch, 24, 256] bf16 out; lse [batch, 24] float out or NULL
  *   idx_out  [batch, budget] int32 out or NULL: the selection used
  *   ws       at least qsa_decode_workspace_bytes(cfg, batch, max_ctx) bytes
- * Steps: block-key scan with per-chunk exact top-(budget-1), merge, split
+ * Steps: block-key scan (scores and a lower bound of each sequence's
+ * (budget-1)-th best score), candidate filter (at small batch it also brings
+ * the candidates' K and V rows into L2), exact merge in block order, split
  * attention over the selected blocks, log-sum-exp combine.
  * Launch post, "Attention: GDN + QSA" (decode speed-up at 1M tokens is
  * quoted there); max_ctx <= 3,080,192.

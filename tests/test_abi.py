@@ -268,12 +268,17 @@ def test_overlap_plan_invariants(L, sms):
         assert n >= 4
     else:
         assert n == 1  # short prefills: nothing to overlap
-    # a later chunk's indexer has more past blocks per query: never fewer SMs
-    # (the last chunk may be longer or shorter than the others)
-    assert all(a <= b for a, b in zip(ctas[1:-2], ctas[2:-1]))
-    # no stub of a chunk at the end
     if n > 1:
-        assert begin[-1] - begin[-2] >= (begin[1] - begin[0]) // 2
+        # the first and the last chunk come in four parts on 64-row tiles
+        sizes = [b - a for a, b in zip(begin[:-1], begin[1:])]
+        assert n >= 10 and all(4 * s_ <= sizes[4] + 16 * 64 for s_ in sizes[:4])
+        assert all(4 * s_ <= 2 * sizes[4] for s_ in sizes[-4:])
+        # between them a later chunk's indexer has more past blocks per query
+        # and the attention beside it the same work: never fewer SMs
+        mid = ctas[5:-5]
+        assert all(a <= b for a, b in zip(mid[:-1], mid[1:]))
+        # no stub of a part at the end
+        assert sizes[-1] >= sizes[-2] // 2
 
 
 def test_overlap_plan_rejects_and_small_budget():
@@ -299,21 +304,3 @@ def test_debug_library_builds_and_exports_every_symbol():
         cfg = Q.default_config()
         assert L.qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 1 << 16) == \
             Q.load().qsa_index_topk_workspace_bytes(ctypes.byref(cfg), 1 << 16)
-
-
-@pytest.mark.parametrize("L", [262144, 266277, 1 << 20, 3_000_001])
-def test_host_prefill_edge_split(L):
-    """HostPrefill's chunks: the overlap plan's, with the first and last chunk
-    in parts on 64-row tiles that keep their chunk's indexer grid."""
-    cfg = Q.default_config()
-    begin, ctas = Q.prefill_overlap_plan(cfg, L, 148)
-    bounds, parts = Q.split_edge_chunks(begin, ctas, 4)
-    assert len(bounds) == len(parts) + 1
-    assert bounds[0] == 0 and bounds[-1] == L
-    assert all(a < b for a, b in zip(bounds[:-1], bounds[1:]))
-    assert all(b % 64 == 0 for b in bounds[1:-1])
-    assert set(begin) <= set(bounds)          # every chunk start is kept
-    assert len(parts) == len(ctas) + 6       # 3 extra parts at each end
-    for a, b, x in zip(bounds[:-1], bounds[1:], parts):
-        j = max(i for i in range(len(ctas)) if begin[i] <= a)
-        assert b <= begin[j + 1] and x == ctas[j]
