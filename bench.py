@@ -618,6 +618,20 @@ def run_e2e(wl: Workload, steps: int) -> dict:
 
 # ---------------------------------------------------------- CPU baseline --
 
+def oracle_sample_rows(times, n0: int, available: int, target_s: float, cap: int = 4096) -> int:
+    """Rows of the timed oracle sample, from the times of n0 and 2 n0 rows.
+    Rows differ in cost (a row's work grows with its position), so the
+    difference of the two times can come out tiny or negative: then the
+    average cost per row of the larger sample (fixed cost included, an
+    overestimate) sizes the sample instead; the sample is never larger than
+    `cap` rows."""
+    per_row_fit = (times[1] - times[0]) / n0
+    per_row_avg = times[1] / (2 * n0)
+    per_row = per_row_fit if per_row_fit > 0.25 * per_row_avg else per_row_avg
+    fixed = max(times[0] - n0 * per_row, 0.0)
+    return int(max(n0, min(available, cap, (target_s - fixed) / max(per_row, 1e-9))))
+
+
 def oracle_sample(wl_name: str, target_s: float = 12.0, host_inputs=None, gpu=None) -> dict:
     """The oracle as it stands, on the host cores, on a bounded sample of the
     workload's prefill query rows (all steps of the layer per row).  With
@@ -660,9 +674,7 @@ def oracle_sample(wl_name: str, target_s: float = 12.0, host_inputs=None, gpu=No
         t0 = time.perf_counter()
         O.prefill_rows(hb, rows0, budget)
         times.append(time.perf_counter() - t0)
-    per_row = max((times[1] - times[0]) / n0, 1e-6)
-    fixed = max(times[0] - n0 * per_row, 0.0)
-    n1 = int(max(n0, min(len(pool) - 2 * n0, (target_s - fixed) / per_row)))
+    n1 = oracle_sample_rows(times, n0, len(pool) - 2 * n0, target_s)
     rows1 = np.sort(pool[2 * n0:2 * n0 + n1])
     fill(rows1)
     t1 = time.perf_counter()

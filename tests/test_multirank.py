@@ -53,3 +53,22 @@ def test_single_rank_is_identity():
 
     assert bench.job_time_ms(42.0, None) == 42.0
     assert bench.job_tokens_per_s(10, 1, 1000.0) == 10.0
+
+
+def test_oracle_sample_stays_bounded():
+    """The CPU baseline's sample size: a per-row cost from two timed samples,
+    falling back to the larger sample's average when the difference is tiny
+    or negative (rows of unequal cost), and never above its cap."""
+    import bench
+
+    # a clean fit: 0.1 s fixed + 0.01 s per row, 12 s target
+    assert bench.oracle_sample_rows([0.1 + 16 * 0.01, 0.1 + 32 * 0.01], 16, 10 ** 6, 12.0) in (1189, 1190)
+    # the second sample came out faster than the first: bounded by the average
+    n = bench.oracle_sample_rows([0.5, 0.45], 16, 10 ** 6, 12.0)
+    assert 16 <= n <= 12.0 / (0.45 / 32) + 1
+    # a tiny positive difference: the same fallback, and the cap holds
+    assert bench.oracle_sample_rows([1.0, 1.0 + 1e-9], 16, 10 ** 6, 12.0) <= 12.0 / (1.0 / 32) + 1
+    assert bench.oracle_sample_rows([1e-6, 2e-6], 16, 10 ** 6, 12.0) == 4096
+    # never fewer than the calibration size, never more rows than there are
+    assert bench.oracle_sample_rows([50.0, 100.0], 16, 10 ** 6, 12.0) == 16
+    assert bench.oracle_sample_rows([0.01, 0.02], 16, 100, 12.0) == 100
