@@ -70,6 +70,19 @@ static_assert(kHKV * COMB_FLOATS * 4 <= STAGE_BYTES, "combine buffer must fit in
 __device__ __forceinline__ void named_bar(int id, int n) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
+// named_bar that also returns whether any of the n threads passed pred = true
+__device__ __forceinline__ bool named_bar_or(int id, int n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
 
 template <int NST, bool DECODE>
 __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs f) {
@@ -503,6 +516,528 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     }
 }
 
+// ---------------------------------------------------------------------------
+// Prefill attention, several query rows per CTA.  One query's 64 stages take
+// about 80 us of an SM at 1M tokens, and a CTA that handles a single query
+// spends several of them on its own start and end (the index row and the
+// query are read, the first stage's copies wait for memory, the key halves
+// are merged and the output written) while the SM's copies idle.  Here a CTA
+// handles up to ROWS rows and its ring of stages runs on across their
+// boundaries: the producers start the next row's copies while the consumers
+// still work through the last stages of the row before and merge its key
+// halves.
+// CTA b takes rows b*ROWS .. b*ROWS+ROWS-1 counted from the last one
+// (longest first), neighbours, whose selections overlap most: a row's
+// blocks are often still in L2 from the row before on the same SM (handing
+// out rows one at a time from a counter, so that the SMs worked on
+// neighbours at the same time instead, measured slower on topic-segment
+// inputs, 1M tokens: 419 vs 403 ms).  CTAs stay short (about 1.2 ms at 1M),
+// so SMs come free regularly for work on other streams.
+// A loader warp prepares each row in one of two query slots as soon as the
+// row two before has been released: the sanitised index row and the row's
+// position first (the producers start on those), then Q with RoPE in the
+// tensor-core layout (the consumers need that too).
+//   warp 0      K producer          warps 1-4  consumers (as in attn_kernel)
+//   warp 5      V producer          warp 6     L2 prefetch (a hint)
+//   warp 7      loader
+// Every role walks the same rows in the same order.  A slot's fills and
+// releases alternate (a row's slot is refilled only after every producer
+// and consumer lane released it), so no waiter can see a slot two fills
+// ahead; the ring stages are numbered across rows and every consumer waits
+// on every stage, as in attn_kernel.
+constexpr int MQ_NQ = 2;                                  // query slots
+constexpr int MQ_THREADS = 32 * 8;
+constexpr int MQ_WARP_VPROD = 5, MQ_WARP_PF = 6, MQ_WARP_LOAD = 7;
+constexpr int MQ_QSLOT = kHKV * kGroup * QROW;            // 12 live rows per KV head
+constexpr int MQ_OFF_BAR = 0;                              // full, empty, qidx, qrdy, qempty
+constexpr int MQ_OFF_MISC = 128;                           // [1] abort, [2] last K stage issued
+constexpr int MQ_OFF_QINFO = 192;                          // per slot {t, output row, used slots}
+constexpr int MQ_OFF_IDX = 256;
+constexpr int MQ_OFF_ZERO = MQ_OFF_IDX + MQ_NQ * kMaxBudget * 4;  // one zero query row
+constexpr int MQ_OFF_Q = ((MQ_OFF_ZERO + QROW + 127) / 128) * 128;
+constexpr int MQ_OFF_ST = ((MQ_OFF_Q + MQ_NQ * MQ_QSLOT + 127) / 128) * 128;
+constexpr int MQ_QE_COUNT = 2 * 32 + NCONS * 32;          // lanes that release a slot
+constexpr int MQ_COMB_TILES = 8;                           // O tiles merged per round
+#ifndef QSA_ATTN_MQ_PF_AHEAD
+#define QSA_ATTN_MQ_PF_AHEAD 2
+#endif
+// Stages the L2 prefetch runs ahead of the K producer.  With the ring
+// running on across rows the prefetch never pauses, and a longer lead keeps
+// so much of every SM's future data in L2 that it evicts itself (1M tokens,
+// 4 rows per CTA: 2 stages 539 ms, 4 stages 544, 8 stages 588).
+constexpr int MQ_PF_AHEAD = QSA_ATTN_MQ_PF_AHEAD;
+constexpr unsigned MQ_LOADER_SLEEP_NS = 1000;
+template <int NST>
+constexpr int mq_smem_bytes() {
+    return MQ_OFF_ST + NST * STAGE_BYTES;
+}
+static_assert(kHKV * (MQ_COMB_TILES * 32 * 4 + 32 * 4) * 4 <= MQ_QSLOT, "merge buffer must fit in a query slot");
+static_assert(mq_smem_bytes<3>() <= 227 * 1024, "shared memory");
+
+struct MqInfo {
+    int64_t t;
+    int64_t orow;
+    int nslot;  // used index slots
+    int pad;
+};
+
+template <int NST, int ROWS>
+__global__ void __launch_bounds__(MQ_THREADS, 1) attn_mq_kernel(AttnArgs a, RopeFreqs f) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + MQ_OFF_BAR);
+    uint64_t *empty = full + NST;
+    uint64_t *qidx = empty + NST;   // a slot's index row and position are in place
+    uint64_t *qrdy = qidx + MQ_NQ;  // ... and its Q with RoPE as well
+    uint64_t *qempty = qrdy + MQ_NQ;
+    volatile int *sMisc = reinterpret_cast<volatile int *>(smem + MQ_OFF_MISC);
+    MqInfo *sInfo = reinterpret_cast<MqInfo *>(smem + MQ_OFF_QINFO);
+    int32_t *sIdxAll = reinterpret_cast<int32_t *>(smem + MQ_OFF_IDX);
+    uint8_t *sZero = smem + MQ_OFF_ZERO;
+    uint8_t *sQAll = smem + MQ_OFF_Q;
+    uint8_t *sSt = smem + MQ_OFF_ST;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * ROWS;
+    const int nq = static_cast<int>(a.L - row0 < ROWS ? a.L - row0 : ROWS);  // rows of this CTA
+    const uint16_t *kbase = a.k;
+    const uint16_t *vbase = a.v;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < NST; ++i) {
+            mbar_init(&full[i], 2);  // the K and the V producer arrive
+            mbar_init(&empty[i], NCONS);
+        }
+        for (int i = 0; i < MQ_NQ; ++i) {
+            mbar_init(&qidx[i], 32);  // every loader lane
+            mbar_init(&qrdy[i], 32);
+            mbar_init(&qempty[i], MQ_QE_COUNT);
+        }
+        sMisc[1] = 0;
+        sMisc[2] = -1;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    // a bounded wait that also gives up once another role has failed
+    auto wait = [&](uint64_t *bar, uint32_t parity) -> bool {
+        if (mbar_try_wait(bar, parity)) return true;
+        const unsigned long long t0 = globaltimer();
+        while (true) {
+#pragma unroll 1
+            for (int i = 0; i < 32; ++i)
+                if (mbar_try_wait(bar, parity)) return true;
+            if (sMisc[1] || globaltimer() - t0 > kWaitLimitNs) return false;
+        }
+    };
+    // the loader's wait for a slot lasts about a row: it polls with pauses,
+    // so that it takes no issue slots from the consumer warp it shares a
+    // scheduler with
+    auto wait_slow = [&](uint64_t *bar, uint32_t parity) -> bool {
+        const unsigned long long t0 = globaltimer();
+        while (!mbar_try_wait(bar, parity)) {
+            if (sMisc[1] || globaltimer() - t0 > kWaitLimitNs) return false;
+            __nanosleep(MQ_LOADER_SLEEP_NS);
+        }
+        return true;
+    };
+    auto fail = [&]() {
+        if (lane == 0) {
+            report(a.status, QSA_ERR_TIMEOUT);
+            sMisc[1] = 1;
+        }
+    };
+
+    if (warp == MQ_WARP_LOAD) {
+        // ------------------------------------------------------ loader --
+#pragma unroll 1
+        for (int j = 0; j < nq; ++j) {
+            const int q = j % MQ_NQ;
+            if (!__all_sync(0xFFFFFFFFu, wait_slow(&qempty[q], ((j / MQ_NQ) & 1) ^ 1))) {
+                fail();
+                break;
+            }
+            const int64_t orow = a.L - 1 - (row0 + j);  // longest first
+            const int64_t t = a.q_off + orow;
+            const int64_t c = t / kBlock;
+            const int32_t *irow = a.idx + orow * a.budget;
+            int32_t *sIdx = sIdxAll + q * kMaxBudget;
+            int nslot = 0;
+#pragma unroll 4
+            for (int base = 0; base < a.budget; base += 32) {
+                const int i = base + lane;
+                int b = i < a.budget ? irow[i] : -1;
+#if QSA_DEBUG_CHECKS
+                if (i < a.budget) {
+                    const int nxt = i + 1 < a.budget ? irow[i + 1] : -1;
+                    bool row_ok = b >= -1 && b <= c && (i > 0 || b >= 0);
+                    if (b >= 0) row_ok = row_ok && (nxt < 0 ? b == c : b < nxt);
+                    else row_ok = row_ok && nxt < 0;
+                    debug_check(a.status, row_ok);
+                }
+#endif
+                if (b < 0 || b > c) b = -1;  // out-of-range entries are ignored
+                if (i < a.budget) sIdx[i] = b;
+                const unsigned ball = __ballot_sync(0xFFFFFFFFu, b >= 0);
+                if (ball) nslot = base + 32 - __clz(ball);
+            }
+            if (lane == 0) {
+                sInfo[q].t = t;
+                sInfo[q].orow = orow;
+                sInfo[q].nslot = nslot;
+            }
+            __syncwarp();
+            mbar_arrive(&qidx[q]);  // the producers can start on this row
+            // Q with RoPE: lane r rotates pair (r, r + 32) of every head; all
+            // of the row's loads are issued before any is used
+            const uint16_t *qrow = a.q + orow * (kHQ * kD);
+            uint8_t *sQ = sQAll + q * MQ_QSLOT;
+            uint16_t x1[kHQ], x2[kHQ];
+            uint4 xr[kHQ * 24 / 32];
+#pragma unroll
+            for (int h = 0; h < kHQ; ++h) {
+                x1[h] = qrow[h * kD + lane];
+                x2[h] = qrow[h * kD + lane + 32];
+            }
+#pragma unroll
+            for (int u = 0; u < kHQ * 24 / 32; ++u) {
+                const int i = u * 32 + lane, h = i / 24, v = i % 24;
+                xr[u] = *reinterpret_cast<const uint4 *>(qrow + h * kD + kRD + v * 8);
+            }
+            float cs, sn;
+            rope_cos_sin(t, f.inv_freq[lane], cs, sn);
+#pragma unroll
+            for (int h = 0; h < kHQ; ++h) {
+                const float y1 = __uint_as_float(static_cast<uint32_t>(x1[h]) << 16);
+                const float y2 = __uint_as_float(static_cast<uint32_t>(x2[h]) << 16);
+                uint8_t *qr = sQ + (h / kGroup) * kGroup * QROW + (h % kGroup) * QROW;
+                reinterpret_cast<__nv_bfloat16 *>(qr)[lane] = __float2bfloat16_rn(fmaf(y1, cs, -y2 * sn));
+                reinterpret_cast<__nv_bfloat16 *>(qr)[lane + 32] = __float2bfloat16_rn(fmaf(y2, cs, y1 * sn));
+            }
+#pragma unroll
+            for (int u = 0; u < kHQ * 24 / 32; ++u) {
+                const int i = u * 32 + lane, h = i / 24, v = i % 24;
+                uint8_t *qr = sQ + (h / kGroup) * kGroup * QROW + (h % kGroup) * QROW;
+                *reinterpret_cast<uint4 *>(qr + kRD * 2 + v * 16) = xr[u];
+            }
+            if (j == 0)
+                for (int i = lane; i < QROW / 16; i += 32)
+                    *reinterpret_cast<uint4 *>(sZero + i * 16) = make_uint4(0, 0, 0, 0);
+            __syncwarp();
+            mbar_arrive(&qrdy[q]);
+        }
+    } else if (warp == MQ_WARP_PF) {
+        // ------------------------------------------------ L2 prefetch --
+        // As in attn_kernel: the K and V blocks of the stages up to
+        // MQ_PF_AHEAD ahead of the K producer, across row boundaries.  A
+        // hint only: it stops at once if anything looks wrong (a failure, a
+        // time limit, or the producers already past the row it waits for).
+        const unsigned long long t0 = globaltimer();
+        const int sl = lane & 7;
+        const bool isv = lane >= 8;
+        int gbase = 0;  // ring stage number of the row's first stage
+        bool go = true;
+#pragma unroll 1
+        for (int j = 0; j < nq && go; ++j) {
+            const int q = j % MQ_NQ;
+            while (!mbar_try_wait(&qidx[q], (j / MQ_NQ) & 1)) {
+                if (sMisc[1] || globaltimer() - t0 > kWaitLimitNs) { go = false; break; }
+                if (sMisc[2] >= gbase) {  // the producers are into this row: ready, or this warp is behind
+                    go = mbar_try_wait(&qidx[q], (j / MQ_NQ) & 1);
+                    break;
+                }
+                __nanosleep(256);
+            }
+            go = __all_sync(0xFFFFFFFFu, go);
+            if (!go) break;
+            const int64_t c = sInfo[q].t / kBlock;
+            const int total_st = (sInfo[q].nslot + SBLK - 1) / SBLK;
+            const int32_t *sIdx = sIdxAll + q * kMaxBudget;
+#pragma unroll 1
+            for (int st = 0; st < total_st && go; ++st) {
+                const int gs = gbase + st;
+                if (gs < NST) continue;  // the producers issue these at once
+                int kst;
+                while ((kst = sMisc[2]) < gs - MQ_PF_AHEAD) {
+                    if (sMisc[1] || globaltimer() - t0 > kWaitLimitNs) { go = false; break; }
+                    __nanosleep(256);
+                }
+                go = __all_sync(0xFFFFFFFFu, go);
+                if (!go || __shfl_sync(0xFFFFFFFFu, kst, 0) >= gs) continue;  // stopped, or already issued
+                if (lane < 16) {
+                    const int si = st * SBLK + sl;
+                    const int b = si < a.budget ? sIdx[si] : -1;
+                    if (b >= 0 && b < c)
+                        prefetch_l2_bulk((isv ? vbase : kbase) + static_cast<int64_t>(b) * kBlock * (kHKV * kD),
+                                         kBlock * ROWB);
+                }
+            }
+            gbase += total_st;
+        }
+    } else if (warp == 0 || warp == MQ_WARP_VPROD) {
+        // ------------------------------------------------ producers --
+        // As in attn_kernel, with the ring's stage number running on
+        // across the rows.
+        const int sl = lane & 7;
+        const int isv = warp == MQ_WARP_VPROD ? 1 : 0;
+        const uint64_t pol = policy_evict_first();
+        bool ok = true;
+        int g = 0;  // ring stage number
+#pragma unroll 1
+        for (int j = 0; j < nq; ++j) {
+            const int q = j % MQ_NQ;
+            ok = __all_sync(0xFFFFFFFFu, wait(&qidx[q], (j / MQ_NQ) & 1));
+            if (!ok) break;
+            const int64_t t = sInfo[q].t;
+            const int64_t c = t / kBlock;
+            const int total_st = (sInfo[q].nslot + SBLK - 1) / SBLK;
+            const int32_t *sIdx = sIdxAll + q * kMaxBudget;
+#pragma unroll 1
+            for (int st = 0; st < total_st; ++st, ++g) {
+                const int slot = g % NST;
+                const uint32_t ph = (g / NST) & 1;
+                if (lane == 0) ok = wait(&empty[slot], ph ^ 1);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) break;
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[slot], SBLK * kBlock * ROWB);  // this producer's half
+                    if (!isv) sMisc[2] = g;  // paces the L2 prefetch
+                }
+                __syncwarp();
+                if (lane < SBLK) {
+                    const int si = st * SBLK + sl;
+                    const int b = si < a.budget ? sIdx[si] : -1;
+                    const uint16_t *base = isv ? vbase : kbase;
+                    uint8_t *dst = sSt + slot * STAGE_BYTES + isv * KV_BYTES + sl * SLOTB;
+                    if (b >= 0 && b < c) {
+                        bulk_g2s_hint(dst, base + static_cast<int64_t>(b) * kBlock * (kHKV * kD),
+                                      kBlock * ROWB, &full[slot], pol);
+                    } else {
+#pragma unroll
+                        for (int r = 0; r < kBlock; ++r) {
+                            const int64_t jj = static_cast<int64_t>(b) * kBlock + r;
+                            const int64_t row = (b >= 0 && jj <= t) ? jj : t;
+                            bulk_g2s_hint(dst + r * ROWB, base + row * (kHKV * kD), ROWB, &full[slot], pol);
+                        }
+                    }
+                }
+            }
+            if (!ok) break;
+            __syncwarp();
+            mbar_arrive(&qempty[q]);  // this row's indices are no longer read here
+        }
+        // the CTA must not finish while its copies can still land
+        if (lane == 0) {
+            for (int gg = max(0, g - NST); gg < g; ++gg)
+                if (!mbar_wait(&full[gg % NST], (gg / NST) & 1)) ok = false;
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) fail();
+    } else {
+        // -------------------------------------------------- consumers --
+        // The stage arithmetic of attn_kernel; between rows the two key
+        // halves are merged through the finished row's query slot (its Q is
+        // in registers by then), eight O tiles at a time.  A failed wait
+        // sets the abort flag and skips the rest of the row's work, but the
+        // warp still passes the row's named barriers, and the four consumer
+        // warps decide together (a barrier reduction) whether to go on, so
+        // none is ever left at a barrier that the others no longer reach.
+        const int cw = warp - 1;
+        const int g = cw & 1;
+        const int kh = cw >> 1;
+        const int qd = lane & 3;
+        const int r0 = lane >> 2;
+        const int qrow_lane = (lane & 7) + ((lane >> 3) & 1) * 8;  // fragment row this lane addresses
+        const uint32_t k_lane = (lane & 7) * SLOTB + (2 * kh + (lane >> 4)) * ROWB + ((lane >> 3) & 1) * 16;
+        const uint32_t v_lane = (lane & 7) * SLOTB + (2 * kh + ((lane >> 3) & 1)) * ROWB + (lane >> 4) * 16;
+        constexpr float kLn2 = 0.693147180559945309f;
+        bool ok = true;
+        int gs = 0;  // ring stage number
+#pragma unroll 1
+        for (int j = 0; j < nq; ++j) {
+            const int q = j % MQ_NQ;
+            ok = __all_sync(0xFFFFFFFFu, wait(&qrdy[q], (j / MQ_NQ) & 1));  // also covers the index row
+            if (!ok) fail();
+            // a failed wait: the four warps agree before any of them leaves
+            if (named_bar_or(1, NCONS * 32, !ok)) break;
+            // positions fit in 32 bits (at most 2^24 tokens); the stage loop
+            // runs at the register limit, so it keeps as little as it can
+            const int t = static_cast<int>(sInfo[q].t);
+            const int c = t / kBlock;
+            const int total_st = (sInfo[q].nslot + SBLK - 1) / SBLK;
+            const int32_t *sIdx = sIdxAll + q * kMaxBudget;
+            uint8_t *sQ = sQAll + q * MQ_QSLOT;
+            // rows 12..15 of the A fragments are zero (12 query heads per KV head)
+            const uint32_t q_addr = qrow_lane < kGroup
+                                        ? smem_u32(sQ) + g * kGroup * QROW + qrow_lane * QROW + (lane >> 4) * 16
+                                        : smem_u32(sZero) + (lane >> 4) * 16;
+            uint32_t qf[kD / 16][4];
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk)
+                ldsm_x4(q_addr + kk * 32, qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
+            float O[32][4];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.f;
+            float m_r[2] = {-INFINITY, -INFINITY};
+            float l_r[2] = {0.f, 0.f};
+
+#pragma unroll 1
+            for (int st = 0; st < total_st; ++st, ++gs) {
+                const int slot = gs % NST;
+                const uint32_t ph = (gs / NST) & 1;
+                if (!__all_sync(0xFFFFFFFFu, wait(&full[slot], ph))) {
+                    ok = false;
+                    fail();
+                    break;
+                }
+                const uint32_t kb = smem_u32(sSt + slot * STAGE_BYTES) + g * (kD * 2);
+                const uint32_t vb = kb + KV_BYTES;
+                float S[2][4];
+#pragma unroll
+                for (int n = 0; n < 2; ++n) S[n][0] = S[n][1] = S[n][2] = S[n][3] = 0.f;
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + k_lane + kk * 32, b0, b1, b2, b3);
+                    mma_bf16_16816(S[0], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b0, b1);
+                    mma_bf16_16816(S[1], qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3], b2, b3);
+                }
+                bool need_mask = false;
+#pragma unroll
+                for (int e = 0; e < SBLK; ++e) {
+                    const int si = st * SBLK + e;
+                    const int b = si < a.budget ? sIdx[si] : -1;
+                    need_mask |= (b < 0) || (b == c);
+                }
+#pragma unroll
+                for (int n = 0; n < 2; ++n)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) S[n][e] *= a.scale_log2;
+                if (need_mask) {
+#pragma unroll
+                    for (int n = 0; n < 2; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int si = st * SBLK + 2 * qd + (e & 1);
+                            const int b = si < a.budget ? sIdx[si] : -1;
+                            const int jj = b * kBlock + 2 * kh + n;
+                            if (b < 0 || jj > t) S[n][e] = -INFINITY;
+                        }
+                }
+                float pv[2][4];
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    float mx = fmaxf(fmaxf(S[0][2 * rr], S[0][2 * rr + 1]), fmaxf(S[1][2 * rr], S[1][2 * rr + 1]));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 1));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, 2));
+                    if (mx > m_r[rr] + 8.f) {
+                        const float sc = exp2f(m_r[rr] - mx);
+                        l_r[rr] *= sc;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            O[i][2 * rr] *= sc;
+                            O[i][2 * rr + 1] *= sc;
+                        }
+                        m_r[rr] = mx;
+                    }
+                    const bool dead = m_r[rr] == -INFINITY;
+#pragma unroll
+                    for (int n = 0; n < 2; ++n)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const float pe = dead ? 0.f : exp2f(S[n][2 * rr + e] - m_r[rr]);
+                            pv[n][2 * rr + e] = pe;
+                            l_r[rr] += pe;
+                        }
+                }
+                const uint32_t pa0 = pack_bf16(pv[0][0], pv[0][1]);
+                const uint32_t pa1 = pack_bf16(pv[0][2], pv[0][3]);
+                const uint32_t pa2 = pack_bf16(pv[1][0], pv[1][1]);
+                const uint32_t pa3 = pack_bf16(pv[1][2], pv[1][3]);
+                const uint32_t vks = vb + v_lane;
+#pragma unroll
+                for (int dt = 0; dt < 16; ++dt) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vks + dt * 32, b0, b1, b2, b3);
+                    mma_bf16_16816(O[2 * dt], pa0, pa1, pa2, pa3, b0, b1);
+                    mma_bf16_16816(O[2 * dt + 1], pa0, pa1, pa2, pa3, b2, b3);
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+            }
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                l_r[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_r[rr], 1);
+                l_r[rr] += __shfl_xor_sync(0xFFFFFFFFu, l_r[rr], 2);
+            }
+
+            // ------------------------------ merge the two key halves --
+            float *comb = reinterpret_cast<float *>(sQ) + g * (MQ_COMB_TILES * 32 * 4 + 32 * 4);
+            float *ml_buf = comb + MQ_COMB_TILES * 32 * 4;
+            named_bar(1, NCONS * 32);  // every consumer has its Q fragments and is past the ring
+            if (kh == 1)
+                *reinterpret_cast<float4 *>(&ml_buf[lane * 4]) = make_float4(m_r[0], m_r[1], l_r[0], l_r[1]);
+            float fa[2] = {0.f, 0.f}, fb[2] = {0.f, 0.f}, lt[2] = {0.f, 0.f}, mt[2] = {0.f, 0.f},
+                  inv[2] = {0.f, 0.f};
+            const int64_t orow_id = *reinterpret_cast<volatile int64_t *>(&sInfo[q].orow);
+            uint16_t *orow = a.out + orow_id * (kHQ * kD);
+            bool stop = false;
+#pragma unroll
+            for (int rd = 0; rd < 32 / MQ_COMB_TILES; ++rd) {
+                if (kh == 1) {
+#pragma unroll
+                    for (int i = 0; i < MQ_COMB_TILES; ++i) {
+                        const int ti = rd * MQ_COMB_TILES + i;
+                        *reinterpret_cast<float4 *>(&comb[(i * 32 + lane) * 4]) =
+                            make_float4(O[ti][0], O[ti][1], O[ti][2], O[ti][3]);
+                    }
+                }
+                named_bar(1, NCONS * 32);
+                if (kh == 0) {
+                    if (rd == 0) {
+                        const float4 ml = *reinterpret_cast<const float4 *>(&ml_buf[lane * 4]);
+                        const float m1[2] = {ml.x, ml.y}, l1[2] = {ml.z, ml.w};
+#pragma unroll
+                        for (int rr = 0; rr < 2; ++rr) {
+                            const float m = fmaxf(m_r[rr], m1[rr]);
+                            fa[rr] = (m == -INFINITY) ? 0.f : exp2f(m_r[rr] - m);
+                            fb[rr] = (m == -INFINITY) ? 0.f : exp2f(m1[rr] - m);
+                            lt[rr] = l_r[rr] * fa[rr] + l1[rr] * fb[rr];
+                            mt[rr] = m;
+                            inv[rr] = lt[rr] > 0.f ? 1.f / lt[rr] : 0.f;
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < MQ_COMB_TILES; ++i) {
+                        const int ti = rd * MQ_COMB_TILES + i;
+                        const float4 o1 = *reinterpret_cast<const float4 *>(&comb[(i * 32 + lane) * 4]);
+                        const float v0 = (O[ti][0] * fa[0] + o1.x * fb[0]) * inv[0];
+                        const float v1 = (O[ti][1] * fa[0] + o1.y * fb[0]) * inv[0];
+                        const float v2 = (O[ti][2] * fa[1] + o1.z * fb[1]) * inv[1];
+                        const float v3 = (O[ti][3] * fa[1] + o1.w * fb[1]) * inv[1];
+                        const int d = ti * 8 + 2 * qd;
+                        if (ok && r0 < kGroup)
+                            *reinterpret_cast<uint32_t *>(orow + (g * kGroup + r0) * kD + d) = pack_bf16(v0, v1);
+                        if (ok && r0 + 8 < kGroup)
+                            *reinterpret_cast<uint32_t *>(orow + (g * kGroup + r0 + 8) * kD + d) =
+                                pack_bf16(v2, v3);
+                    }
+                }
+                if (rd + 1 < 32 / MQ_COMB_TILES) named_bar(1, NCONS * 32);
+                else stop = named_bar_or(1, NCONS * 32, !ok || sMisc[1] != 0);
+            }
+            if (ok && kh == 0 && a.lse && qd == 0) {
+                float *lrow = a.lse + orow_id * kHQ;
+                if (r0 < kGroup) lrow[g * kGroup + r0] = lt[0] > 0.f ? (mt[0] + log2f(lt[0])) * kLn2 : -INFINITY;
+                if (r0 + 8 < kGroup)
+                    lrow[g * kGroup + r0 + 8] = lt[1] > 0.f ? (mt[1] + log2f(lt[1])) * kLn2 : -INFINITY;
+            }
+            if (stop) break;
+            mbar_arrive(&qempty[q]);  // the slot's indices, Q and merge buffer are free
+        }
+    }
+}
+
 // Merge decode splits: O = sum_i e^(lse_i - M) O_i / sum_i e^(lse_i - M).
 // All of a thread's loads are issued before their values are used (split
 // LSEs, then the partial outputs), so the merge costs two round trips to L2
@@ -547,13 +1082,30 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
 constexpr int kPrefillStages = 3;
 constexpr int kDecodeStages = 3;
 
+// Query rows per prefill CTA at most (1: attn_kernel, one row per CTA).
+#ifndef QSA_ATTN_ROWS_PER_CTA
+#define QSA_ATTN_ROWS_PER_CTA 16
+#endif
+constexpr int kPrefillRows = QSA_ATTN_ROWS_PER_CTA;
+
 cudaError_t launch_attn_prefill(const AttnArgs &a, const RopeFreqs &f, cudaStream_t stream) {
+    if (a.L <= 0) return cudaSuccess;
+    AttnArgs p = a;
+    p.nsplit = 1;
+    if constexpr (kPrefillRows > 1) {
+        constexpr int smem = at::mq_smem_bytes<kPrefillStages>();
+        auto kern = at::attn_mq_kernel<kPrefillStages, kPrefillRows>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const int64_t grid = (a.L + kPrefillRows - 1) / kPrefillRows;
+        if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+        kern<<<static_cast<unsigned>(grid), at::MQ_THREADS, smem, stream>>>(p, f);
+        return cudaGetLastError();
+    }
     constexpr int smem = at::smem_bytes<kPrefillStages>();
     cudaError_t e = cudaFuncSetAttribute(at::attn_kernel<kPrefillStages, false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    AttnArgs p = a;
-    p.nsplit = 1;
     const int64_t grid = a.L;
     if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
     at::attn_kernel<kPrefillStages, false><<<static_cast<unsigned>(grid), at::THREADS, smem, stream>>>(p, f);
