@@ -232,11 +232,16 @@ void set_error_detail(const char *msg) { g_detail = msg; }
 // per chunk from per-SM costs fitted to B300 runs of both kernels, side by
 // side, at 128K and 1M tokens: the indexer takes 2.14e-10 SM-seconds per
 // (query, past block) pair plus 8.2e-6 per query row (its list start-up and
-// final selection); the attention consumes 65 GB/s of gathered K/V per SM
-// (2 KiB per attended key) and cannot go below 6.9 TB/s for the whole GPU.
-// (Costing the attention at 55 GB/s per SM, i.e. giving it more SMs, was 5
-// ms faster at 1M on i.i.d. inputs but 61 ms slower with topic segments,
-// where the indexer is slower than the fit.)
+// final selection); the attention consumes 75 GB/s of gathered K/V per SM
+// (2 KiB per attended key) and cannot go faster than 8.3 TB/s of gathered
+// bytes for the whole GPU (its rate alone at 1M, above the HBM copy rate
+// because blocks that nearby queries share are read from L2).  Where K/V
+// sits in L2 more (topic-segment inputs) the attention runs faster than
+// that and the indexer's share of the SMs sets the time, so the costs lean
+// towards the indexer; at 1M tokens (ms, i.i.d. / topic segments): 70 GB/s
+// per SM 658-663 / 658, 75: 662-665 / 638, 80 with 9 TB/s: 668-670 / 619,
+// 90 with 10 TB/s: 675 / 592, and the earlier 65 with 6.9 TB/s 665-670 /
+// 697.
 // Below 256K tokens the attention's K/V mostly sits in L2 and the attention
 // is bound by its SMs rather than by HBM, so there is nothing to hand to the
 // indexer: shorter prefills run the two stages one after the other.
@@ -247,8 +252,8 @@ constexpr int kEdgeParts = 4;  // parts of the first and of the last chunk
 
 constexpr double kIdxPairSm = 2.14e-10;
 constexpr double kIdxRowSm = 8.2e-6;
-constexpr double kAttnKeySm = 2048.0 / 65e9;
-constexpr double kAttnKeyFloor = 2048.0 / 6.9e12;
+constexpr double kAttnKeySm = 2048.0 / 75e9;
+constexpr double kAttnKeyFloor = 2048.0 / 8.3e12;
 
 // sum over t in [r0, r1) of floor(t/4): the pairs the indexer scores
 double pairs_in(int64_t r0, int64_t r1) {
