@@ -339,6 +339,10 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
     // of slots 0-7, lanes 16-31 -> dims +8
     const uint32_t v_lane = (lane & 7) * SLOTB + (2 * kh + ((lane >> 3) & 1)) * ROWB + (lane >> 4) * 16;
     bool ok = true;
+    // positions fit in 32 bits (at most 2^24 tokens): the key loop runs at
+    // the register limit, and 64-bit copies cost it scheduling room
+    const int t32 = static_cast<int>(t);
+    const int c32 = static_cast<int>(c);
     // the query's A fragments stay in registers for the whole key loop
     uint32_t qf[kD / 16][4];
 #pragma unroll
@@ -368,7 +372,7 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
         for (int e = 0; e < SBLK; ++e) {
             const int si = st * SBLK + e;
             const int b = si < a.budget ? sIdx[si] : -1;
-            need_mask |= (b < 0) || (b == c);
+            need_mask |= (b < 0) || (b == c32);
         }
         // S[n][0..1]: row r0, S[n][2..3]: row r0+8; columns = slots 2qd, 2qd+1
 #pragma unroll
@@ -382,8 +386,8 @@ __global__ void __launch_bounds__(THREADS, 1) attn_kernel(AttnArgs a, RopeFreqs 
                 for (int e = 0; e < 4; ++e) {
                     const int si = st * SBLK + 2 * qd + (e & 1);
                     const int b = si < a.budget ? sIdx[si] : -1;
-                    const int64_t j = static_cast<int64_t>(b) * kBlock + 2 * kh + n;
-                    if (b < 0 || j > t) S[n][e] = -INFINITY;
+                    const int j = b * kBlock + 2 * kh + n;
+                    if (b < 0 || j > t32) S[n][e] = -INFINITY;
                 }
         }
         float pv[2][4];
