@@ -754,13 +754,16 @@ __global__ void __launch_bounds__(THREADS, 1)
         bool predict_on = p.predict != 0;
         for (int kk = blockIdx.x; kk < p.nq; kk += gridDim.x) {
             const int q = p.nq - 1 - kk;
-            const int64_t t0 = p.q_off + static_cast<int64_t>(q) * TQ;
+            // positions fit in 32 bits (at most 2^24 tokens): the epilogue runs
+            // at its register limit, and 64-bit copies cost it scheduling room
+            const int t0 = static_cast<int>(p.q_off) + q * TQ;
+            const int L32 = static_cast<int>(p.L);
             const int nbt = num_btiles(p, q);
             if (tile_skipped(p, q)) continue;
             if (group_sync_fail(bar, !ok || sMisc[1] != 0)) { ok = false; break; }
             if (tg < GTOK) {
                 const int tl = g * GTOK + tg;
-                const int64_t t = t0 + tl;
+                const int t = t0 + tl;
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) sCnt[qq * TQ + tl] = 0;
                 sTheta[tl] = -INFINITY;
@@ -771,15 +774,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                 for (int h = 0; h < kHI; ++h) {
                     float wv = 0.f;
-                    if (t < p.L) wv = __uint_as_float(static_cast<uint32_t>(p.w[(t - p.q_off) * kHI + h]) << 16);
+                    if (t < L32) wv = __uint_as_float(static_cast<uint32_t>(p.w[static_cast<int64_t>(t - static_cast<int>(p.q_off)) * kHI + h]) << 16);
                     // w / 2 (exact for every bf16 w), see the score below
                     sW[(tl >> 2) * 16 + h * 4 + (tl & 3)] = 0.5f * wv;  // [token quad][head][token]
                 }
             }
             if (group_sync_fail(bar, false)) { ok = false; break; }
             predict_on = sGPred[g] != 0;
-            const bool tile_all_in = (t0 + TQ <= p.L);
-            const int64_t c_min = t0 >> p.bshift;
+            const bool tile_all_in = (t0 + TQ <= L32);
+            const int c_min = t0 >> p.bshift;
             for (int j = 0; j < nbt; ++j) {
                 const uint32_t buf = acc & 1;
                 const uint32_t use = acc >> 1;
@@ -794,8 +797,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     continue;
                 }
                 tc_fence_after();
-                const int64_t b = static_cast<int64_t>(j) * TB + quarter * 32 + lane;
-                const bool masked = !(tile_all_in && (static_cast<int64_t>(j) * TB + TB <= c_min));
+                const int b = j * TB + quarter * 32 + lane;
+                const bool masked = !(tile_all_in && (j * TB + TB <= c_min));
                 const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        buf * NCOL + static_cast<uint32_t>(g * GCOL);
                 // 4 chunks of 4 tokens (16 columns each), each chunk's TMEM load
@@ -839,9 +842,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if constexpr (DENSE) {
 #pragma unroll
                             for (int tk = 0; tk < 4; ++tk) {
-                                const int64_t t = t0 + tl0 + tk;
-                                const bool valid = !MASKED || ((t < p.L) && (b < (t >> p.bshift)));
-                                if (valid) p.dense[t * p.dense_ld + b] = sv[tk];
+                                const int t = t0 + tl0 + tk;
+                                const bool valid = !MASKED || ((t < L32) && (b < (t >> p.bshift)));
+                                if (valid) p.dense[static_cast<int64_t>(t) * p.dense_ld + b] = sv[tk];
                             }
                         } else {
                             const float4 th = *reinterpret_cast<const float4 *>(&sTheta[tl0]);
@@ -851,8 +854,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             unsigned m[4];
 #pragma unroll
                             for (int tk = 0; tk < 4; ++tk) {
-                                const int64_t t = t0 + tl0 + tk;
-                                const bool valid = !MASKED || ((t < p.L) && (b < (t >> p.bshift)));
+                                const int t = t0 + tl0 + tk;
+                                const bool valid = !MASKED || ((t < L32) && (b < (t >> p.bshift)));
                                 pass[tk] = valid && (sv[tk] >= thv[tk]);
                             }
                             // a block enters the token's list when s >= its threshold
@@ -975,8 +978,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                 bool pred_failed = false;
                 for (int t16 = 0; t16 < GTOK; ++t16) {
                     const int tl = g * GTOK + t16;
-                    const int64_t t = t0 + tl;
-                    if (t >= p.L) break;
+                    const int t = t0 + tl;
+                    if (t >= L32) break;
                     const int64_t c = t >> p.bshift;
                     int n[4];
 #pragma unroll
