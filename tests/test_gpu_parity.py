@@ -129,8 +129,11 @@ def test_selection_with_many_compactions():
     assert nmis <= len(rows)
 
 
-@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 7, 9, 64, 65, 127])
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 7, 9, 15, 16, 17, 31, 33, 64, 65, 127])
 def test_tiny_and_ragged_lengths(L):
+    """Every row against the oracle; the lengths also fall on both sides of
+    the prefill attention's 16 query rows per CTA (a last CTA with 1, 15 or
+    16 rows)."""
     budget = 4
     t = W.prefill_inputs(L, 27 + L, DEV)
     hb = W.host_bits(t)
