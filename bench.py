@@ -915,7 +915,10 @@ def main():
         "stage_ms": {"prefill_overlapped": pre_ms, "decode_step": dec_ms,
                      "indexer_topk_alone": idx_ms, "sparse_attn_prefill_alone": attn_ms,
                      "decode_step_after_serial_prefill": dec_serial_ms},
-        "overlap": {"chunks": len(ctas), "index_ctas": ctas, "serial_prefill_ms": idx_ms + attn_ms,
+        "overlap": {"chunks": len(ctas), "index_ctas": ctas,
+                    "split": "index_ctas is the starting plan; from the fourth chunk on the call rescales "
+                             "the plan's costs by the measured times of the chunk pair before",
+                    "serial_prefill_ms": idx_ms + attn_ms,
                     "stage_region_launches": 9 * K,
                     "speedup_vs_serial": (idx_ms + attn_ms) / pre_ms,
                     "stage_region": "per-stage times and kernel rooflines come from a second timed region "

@@ -458,6 +458,27 @@ qsa_status qsa_sparse_attn_prefill(const qsa_config *cfg, const qsa_bf16 *q,
     return qsa_sparse_attn_prefill_cached(cfg, q, k_rot, v, idx, 0, L, out, lse, dev_status, stream);
 }
 
+// The indexer's SMs for a chunk whose indexer work is w SM-s, run beside an
+// attention chunk of a SM-s that cannot take less than fl seconds: the x
+// that minimises the later of the two to finish.
+int best_split(double w, double a, double fl, int sms) {
+    int best = 1;
+    double best_t = 1e300;
+    for (int x = 1; x < sms; ++x) {
+        const double ta = a / (sms - x) > fl ? a / (sms - x) : fl;
+        const double t = w / x > ta ? w / x : ta;
+        if (t < best_t) {
+            best_t = t;
+            best = x;
+        }
+    }
+    return best;
+}
+double chunk_index_work(const int64_t *b, int j) {
+    return pairs_in(b[j], b[j + 1]) * kIdxPairSm + static_cast<double>(b[j + 1] - b[j]) * kIdxRowSm;
+}
+double chunk_attn_keys(const int64_t *b, int j, int budget) { return keys_in(b[j], b[j + 1], budget); }
+
 int qsa_prefill_overlap_plan(const qsa_config *cfg, int64_t L, int sms, int max_chunks,
                              int64_t *chunk_begin, int *index_ctas) {
     if (check_cfg(cfg) != QSA_OK || L < 1 || L > kMaxL || sms < 2 || max_chunks < 1 || !chunk_begin ||
@@ -494,22 +515,9 @@ int qsa_prefill_overlap_plan(const qsa_config *cfg, int64_t L, int sms, int max_
     n = m;
     chunk_begin[n] = L;
     index_ctas[0] = sms;  // the first chunk's indexer runs alone
-    for (int64_t j = 1; j < n; ++j) {
-        const double w = pairs_in(chunk_begin[j], chunk_begin[j + 1]) * kIdxPairSm +
-                         static_cast<double>(chunk_begin[j + 1] - chunk_begin[j]) * kIdxRowSm;
-        const double keys = keys_in(chunk_begin[j - 1], chunk_begin[j], cfg->budget_blocks);
-        const double a = keys * kAttnKeySm, fl = keys * kAttnKeyFloor;
-        int best = 1;
-        double best_t = 1e300;
-        for (int x = 1; x < sms; ++x) {
-            const double ta = a / (sms - x) > fl ? a / (sms - x) : fl;
-            const double t = w / x > ta ? w / x : ta;
-            if (t < best_t) {
-                best_t = t;
-                best = x;
-            }
-        }
-        index_ctas[j] = best;
+    for (int j = 1; j < static_cast<int>(n); ++j) {
+        const double keys = chunk_attn_keys(chunk_begin, j - 1, cfg->budget_blocks);
+        index_ctas[j] = best_split(chunk_index_work(chunk_begin, j), keys * kAttnKeySm, keys * kAttnKeyFloor, sms);
     }
     return static_cast<int>(n);
 }
@@ -577,61 +585,118 @@ qsa_status qsa_prefill_overlapped(const qsa_config *cfg, const qsa_bf16 *q, cons
     cudaStream_t side = nullptr;
     e = cudaStreamCreateWithPriority(&side, cudaStreamNonBlocking, hi);
     if (e != cudaSuccess) return cuda_fail(e, "side stream");
-    cudaEvent_t ev[kMaxChunks + 1];
+    // per chunk: the indexer's start and end on the side stream, the
+    // attention's start and end on `stream`; then the K-prep's end
+    cudaEvent_t ev[4 * kMaxChunks + 1];
+    cudaEvent_t *ti0 = ev, *ti1 = ev + n, *ta0 = ev + 2 * n, *ta1 = ev + 3 * n, *kp = ev + 4 * n;
     int nev = 0;
     auto cleanup = [&]() {
         for (int i = 0; i < nev; ++i) cudaEventDestroy(ev[i]);
         cudaStreamDestroy(side);
     };
-    for (; nev < n + 1; ++nev) {
-        e = cudaEventCreateWithFlags(&ev[nev], cudaEventDisableTiming);
+    for (; nev < 4 * n + 1; ++nev) {
+        e = cudaEventCreate(&ev[nev]);
         if (e != cudaSuccess) {
             cleanup();
             return cuda_fail(e, "event");
         }
     }
     int *stop = qsa::index_stop_word(cand, qsa::index_cand_bytes(L, sms));
+    auto enqueue_index = [&](int j) -> qsa_status {
+        const int64_t r0 = begin[j], nr = begin[j + 1] - begin[j];
+        CUtensorMap map_q, map_k;
+        qsa_status st2 = make_map(&map_q, qi + r0 * qsa::kHI * qsa::kDI, qsa::kDI,
+                                  static_cast<uint64_t>(nr) * qsa::kHI, 256);
+        if (st2 != QSA_OK) return st2;
+        const int64_t nbk = (r0 + nr) / qsa::kBlock;
+        st2 = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
+        if (st2 != QSA_OK) return st2;
+        cudaError_t e2 = cudaEventRecord(ti0[j], side);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "event record");
+        e2 = qsa::launch_index(map_q, map_k, r0, nr, qsa::kBlock, budget, w + r0 * qsa::kHI, idx + r0 * budget,
+                               score ? score + r0 * budget : nullptr, nullptr, cand, dev_status, ctas[j], stop,
+                               side);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "indexer launch");
+        if ((e2 = cudaEventRecord(ti1[j], side)) != cudaSuccess) return cuda_fail(e2, "event record");
+        return QSA_OK;
+    };
+    auto enqueue_attn = [&](int j) -> qsa_status {
+        const int64_t r0 = begin[j], nr = begin[j + 1] - begin[j];
+        cudaError_t e2 = cudaStreamWaitEvent(s, ti1[j], 0);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "stream wait");
+        if ((e2 = cudaEventRecord(ta0[j], s)) != cudaSuccess) return cuda_fail(e2, "event record");
+        qsa::AttnArgs a{};
+        a.q = q + r0 * qsa::kHQ * qsa::kD;
+        a.k = k_rot;
+        a.v = v;
+        a.idx = idx + r0 * budget;
+        a.budget = budget;
+        a.L = nr;
+        a.q_off = r0;
+        a.out = out + r0 * qsa::kHQ * qsa::kD;
+        a.lse = lse ? lse + r0 * qsa::kHQ : nullptr;
+        a.nsplit = 1;
+        a.scale_log2 = scale_log2_of(cfg);
+        a.status = dev_status;
+        qsa_status st3 = attention_prefill(a, freqs, L, s);
+        if (st3 != QSA_OK) return st3;
+        if ((e2 = cudaEventRecord(ta1[j], s)) != cudaSuccess) return cuda_fail(e2, "event record");
+        return QSA_OK;
+    };
+    // The split adapts while the call runs.  Before chunk j's indexer is
+    // enqueued, the host waits for the pair that ran side by side before it
+    // (the indexer of chunk j-1 and the attention of chunk j-2), rescales
+    // each stage's cost halfway (in the log) towards what that pair took,
+    // and picks chunk j's split from the rescaled costs; then it enqueues
+    // chunk j's indexer and chunk j-1's attention, in that order, so the
+    // indexer (on the higher-priority stream) takes its SMs before the
+    // attention's CTAs fill the GPU, and each indexer chunk starts with the
+    // attention it is paired with, as the cost model assumes.  Where the
+    // attention's K/V sits in L2 more than the fitted costs expect
+    // (topic-segment inputs) the later chunks give the indexer more SMs.
+    // Measured at 1M tokens (ms, i.i.d. / topic segments, three boxes): 660-666
+    // / 599 against 663-672 / 633-634 with the fixed plan; letting the host
+    // run two or three chunks ahead 664 / 597 and 668-671 / 602; enqueuing
+    // the attention before the wait 673-674 / 596 (its CTAs took the SMs
+    // first).
+    constexpr int kLookahead = 1;
+    double s_idx = 1.0, s_att = 1.0;
+    auto clampd = [](double v, double lo_, double hi_) { return v < lo_ ? lo_ : (v > hi_ ? hi_ : v); };
+    auto adapt = [&](int j) -> qsa_status {
+        const int k2 = j - kLookahead;  // the newest pair that can have finished
+        if (k2 < 2) return QSA_OK;
+        cudaError_t e2 = cudaEventSynchronize(ti1[k2]);
+        if (e2 == cudaSuccess) e2 = cudaEventSynchronize(ta1[k2 - 1]);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "event wait");
+        float t_i = 0.f, t_a = 0.f;
+        if (cudaEventElapsedTime(&t_i, ti0[k2], ti1[k2]) != cudaSuccess ||
+            cudaEventElapsedTime(&t_a, ta0[k2 - 1], ta1[k2 - 1]) != cudaSuccess || t_i <= 0.f || t_a <= 0.f)
+            return QSA_OK;  // no usable times: keep the costs
+        const double keys = chunk_attn_keys(begin, k2 - 1, budget);
+        const int x = ctas[k2];
+        const double pi = s_idx * chunk_index_work(begin, k2) / x;
+        const double pa0 = s_att * keys * kAttnKeySm / (sms - x), pfl = s_att * keys * kAttnKeyFloor;
+        const double pa = pa0 > pfl ? pa0 : pfl;
+        s_idx = clampd(s_idx * std::sqrt(1e-3 * t_i / pi), 0.25, 4.0);
+        s_att = clampd(s_att * std::sqrt(1e-3 * t_a / pa), 0.25, 4.0);
+        const double kj = chunk_attn_keys(begin, j - 1, budget);
+        ctas[j] = best_split(s_idx * chunk_index_work(begin, j), s_att * kj * kAttnKeySm, s_att * kj * kAttnKeyFloor,
+                             sms);
+        return QSA_OK;
+    };
     auto run = [&]() -> qsa_status {
         cudaError_t e2 = qsa::launch_kprep(1, 0, L, L, ki, k, k_rot, kblk, freqs, sms, s);
         if (e2 != cudaSuccess) return cuda_fail(e2, "kprep launch");
         if ((e2 = cudaMemsetAsync(stop, 0, sizeof(int), s)) != cudaSuccess) return cuda_fail(e2, "memset");
-        if ((e2 = cudaEventRecord(ev[n], s)) != cudaSuccess) return cuda_fail(e2, "event record");
-        if ((e2 = cudaStreamWaitEvent(side, ev[n], 0)) != cudaSuccess) return cuda_fail(e2, "stream wait");
+        if ((e2 = cudaEventRecord(kp[0], s)) != cudaSuccess) return cuda_fail(e2, "event record");
+        if ((e2 = cudaStreamWaitEvent(side, kp[0], 0)) != cudaSuccess) return cuda_fail(e2, "stream wait");
         for (int j = 0; j < n; ++j) {
-            const int64_t r0 = begin[j], nr = begin[j + 1] - begin[j];
-            CUtensorMap map_q, map_k;
-            qsa_status st2 = make_map(&map_q, qi + r0 * qsa::kHI * qsa::kDI, qsa::kDI,
-                                      static_cast<uint64_t>(nr) * qsa::kHI, 256);
+            qsa_status st2 = adapt(j);
             if (st2 != QSA_OK) return st2;
-            const int64_t nbk = (r0 + nr) / qsa::kBlock;
-            st2 = make_map(&map_k, kblk, qsa::kDI, static_cast<uint64_t>(nbk > 0 ? nbk : 1), 128);
-            if (st2 != QSA_OK) return st2;
-            e2 = qsa::launch_index(map_q, map_k, r0, nr, qsa::kBlock, budget, w + r0 * qsa::kHI,
-                                   idx + r0 * budget, score ? score + r0 * budget : nullptr, nullptr, cand,
-                                   dev_status, ctas[j], stop, side);
-            if (e2 != cudaSuccess) return cuda_fail(e2, "indexer launch");
-            if ((e2 = cudaEventRecord(ev[j], side)) != cudaSuccess) return cuda_fail(e2, "event record");
+            if ((st2 = enqueue_index(j)) != QSA_OK) return st2;
+            if (j > 0 && (st2 = enqueue_attn(j - 1)) != QSA_OK) return st2;
         }
-        for (int j = 0; j < n; ++j) {
-            const int64_t r0 = begin[j], nr = begin[j + 1] - begin[j];
-            if ((e2 = cudaStreamWaitEvent(s, ev[j], 0)) != cudaSuccess) return cuda_fail(e2, "stream wait");
-            qsa::AttnArgs a{};
-            a.q = q + r0 * qsa::kHQ * qsa::kD;
-            a.k = k_rot;
-            a.v = v;
-            a.idx = idx + r0 * budget;
-            a.budget = budget;
-            a.L = nr;
-            a.q_off = r0;
-            a.out = out + r0 * qsa::kHQ * qsa::kD;
-            a.lse = lse ? lse + r0 * qsa::kHQ : nullptr;
-            a.nsplit = 1;
-            a.scale_log2 = scale_log2_of(cfg);
-            a.status = dev_status;
-            qsa_status st3 = attention_prefill(a, freqs, L, s);
-            if (st3 != QSA_OK) return st3;
-        }
-        return QSA_OK;
+        return enqueue_attn(n - 1);
     };
     st = run();
     cleanup();

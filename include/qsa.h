@@ -261,7 +261,12 @@ qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 
  *   16-byte aligned.
  * The call enqueues on `stream`; internally it forks a higher-priority
  * stream for the indexer and joins it back before the last attention chunk,
- * so work enqueued on `stream` afterwards sees every output.  Errors as for
+ * so work enqueued on `stream` afterwards sees every output.  The split of
+ * the SMs adapts while the call runs: before it enqueues chunk j's indexer
+ * (j >= 3) the host waits for the indexer of chunk j-1 and the attention of
+ * chunk j-2 and rescales the plan's costs by their measured times, so the
+ * call returns only when the last chunk is enqueued, about one chunk before
+ * the prefill ends.  Errors as for
  * the two calls it combines; QSA_ERR_CUDA if the helper stream or its
  * events cannot be created.
  *
@@ -274,7 +279,8 @@ qsa_status qsa_sparse_attn_prefill_cached(const qsa_config *cfg, const qsa_bf16 
  *   SMs (host only, no GPU needed).  Writes n+1 chunk starts
  *   (chunk_begin[0] = 0, chunk_begin[n] = L; every inner start a multiple of
  *   64) and n indexer grid sizes (index_ctas[0] = sms: the first chunk's
- *   indexer runs alone), and returns n (1 <= n <= max_chunks), or 0 on
+ *   indexer runs alone; the call starts from these and adapts them from the
+ *   fourth chunk on), and returns n (1 <= n <= max_chunks), or 0 on
  *   invalid arguments.  chunk_begin needs max_chunks + 1 entries.  The first
  *   and the last four chunks are the parts of the edge chunks when max_chunks
  *   leaves room for them (22 chunks at 1,048,576 tokens).
