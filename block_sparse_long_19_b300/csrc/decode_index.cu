@@ -43,9 +43,11 @@ constexpr int MAX_CHUNK = 16384;
 constexpr int MAX_NCHUNK = 256;  // scan CTAs per sequence
 constexpr int KW_MAX = 16;       // best scores kept per lane (and per warp) for the chunk bound
 constexpr int MERGE_THREADS = 256;
+constexpr int MERGE_SPEC = 8;  // candidates per merge thread loaded before their count is known
 constexpr int FILTER_THREADS = 256;
 constexpr int FILTER_PER_THREAD = 8;
 constexpr int CAND_CAP = 8192;  // filtered candidates kept per sequence
+static_assert(MERGE_SPEC * MERGE_THREADS <= CAND_CAP, "speculative loads stay in the candidate area");
 constexpr int CCOUNT_STRIDE = 32;  // ints between two sequences' candidate counters (128 B)
 constexpr int64_t kPrefetchL2Bytes = int64_t(72) << 20;  // L2 budget of the filter's K/V prefetch
 
@@ -428,15 +430,24 @@ __device__ void merge_row(const MergeParams &p, int s, int64_t c, uint2 *items, 
     int32_t *row = p.idx + static_cast<int64_t>(s) * p.budget;
     const int lane = threadIdx.x & 31;
     const unsigned ltmask = (1u << lane) - 1u;
+    // the first MERGE_SPEC * NT candidates are loaded together with their
+    // count (one round trip to L2 instead of two); entries past the count are
+    // loaded but not used (the area holds CAND_CAP entries per sequence)
+    const uint2 *src = p.cand + static_cast<int64_t>(s) * CAND_CAP;
+    uint2 pre[MERGE_SPEC];
+#pragma unroll
+    for (int k = 0; k < MERGE_SPEC; ++k) pre[k] = __ldcg(src + threadIdx.x + k * NT);
     const int nc = __ldcg(p.ccount + static_cast<int64_t>(s) * CCOUNT_STRIDE);
     const bool direct = nc > CAND_CAP;  // ties flooded the candidate area
     const bool staged = !direct && nc <= items_cap;
     const int n = direct ? static_cast<int>(c) : nc;
     const float *srow = p.scores + static_cast<int64_t>(s) * (p.max_ctx / kBlock);
-    const uint2 *src = p.cand + static_cast<int64_t>(s) * CAND_CAP;
     if (staged) {
+#pragma unroll
+        for (int k = 0; k < MERGE_SPEC; ++k)
+            if (threadIdx.x + k * NT < n) items[threadIdx.x + k * NT] = pre[k];
 #pragma unroll 4
-        for (int i = threadIdx.x; i < n; i += NT) items[i] = __ldcg(src + i);
+        for (int i = threadIdx.x + MERGE_SPEC * NT; i < n; i += NT) items[i] = __ldcg(src + i);
     }
     __syncthreads();
     auto score = [&](int i) {
@@ -536,10 +547,12 @@ struct FilterParams {
 __global__ void __launch_bounds__(FILTER_THREADS) filter_kernel(FilterParams p) {
     __shared__ int s_warp[FILTER_THREADS / 32 + 1];
     pdl_trigger();
-    pdl_wait();  // scores and bounds of the scan
+    // the sequence length is an input of the step (no earlier kernel writes
+    // it): it is read while the scan finishes
     const int s = blockIdx.y;
     if (trivial_row<FILTER_THREADS>(p.m, s, false)) return;  // the merge writes that row
     const int64_t c = (p.m.seq_lens[s] - 1) / kBlock;
+    pdl_wait();  // scores and bounds of the scan
     const float *srow = p.m.scores + static_cast<int64_t>(s) * (p.m.max_ctx / kBlock);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const unsigned ltmask = (1u << lane) - 1u;
@@ -619,10 +632,18 @@ __global__ void __launch_bounds__(MERGE_THREADS) merge_kernel(MergeParams p) {
     uint32_t *hist = sortb + 1024;
     int *ctl = reinterpret_cast<int *>(hist + 256);
     pdl_trigger();
-    pdl_wait();  // candidates of the filter (and, through it, the scan's scores)
     const int s = blockIdx.x;
-    if (trivial_row<MERGE_THREADS>(p, s, true)) return;
-    merge_row<MERGE_THREADS>(p, s, (p.seq_lens[s] - 1) / kBlock, items, CAND_CAP, sortb, hist, ctl);
+    // the length (an input of the step) is read while the filter finishes;
+    // the row is written only after the wait: before it, the previous step's
+    // attention may still be reading the index rows
+    const bool trivial = trivial_row<MERGE_THREADS>(p, s, false);
+    const int64_t c = (p.seq_lens[s] - 1) / kBlock;
+    pdl_wait();  // candidates of the filter (and, through it, the scan's scores)
+    if (trivial) {
+        trivial_row<MERGE_THREADS>(p, s, true);
+        return;
+    }
+    merge_row<MERGE_THREADS>(p, s, c, items, CAND_CAP, sortb, hist, ctl);
 }
 
 }  // namespace dx
