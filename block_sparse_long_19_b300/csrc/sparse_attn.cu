@@ -1105,15 +1105,16 @@ cudaError_t launch_attn_prefill(const AttnArgs &a, const RopeFreqs &f, cudaStrea
         if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
         kern<<<static_cast<unsigned>(grid), at::MQ_THREADS, smem, stream>>>(p, f);
         return cudaGetLastError();
+    } else {
+        constexpr int smem = at::smem_bytes<kPrefillStages>();
+        cudaError_t e = cudaFuncSetAttribute(at::attn_kernel<kPrefillStages, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        const int64_t grid = a.L;
+        if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
+        at::attn_kernel<kPrefillStages, false><<<static_cast<unsigned>(grid), at::THREADS, smem, stream>>>(p, f);
+        return cudaGetLastError();
     }
-    constexpr int smem = at::smem_bytes<kPrefillStages>();
-    cudaError_t e = cudaFuncSetAttribute(at::attn_kernel<kPrefillStages, false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    const int64_t grid = a.L;
-    if (grid > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    at::attn_kernel<kPrefillStages, false><<<static_cast<unsigned>(grid), at::THREADS, smem, stream>>>(p, f);
-    return cudaGetLastError();
 }
 
 cudaError_t launch_attn_decode(const AttnArgs &a, int batch, const RopeFreqs &f,
