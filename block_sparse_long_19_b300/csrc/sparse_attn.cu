@@ -12,8 +12,10 @@
 // for both KV heads) and on i.i.d. inputs two queries share almost none of
 // them, so the kernel is bound by the gather (about 12 flop per byte), not by
 // the tensor cores.  The design therefore spends its effort on the data path:
-//   * one CTA per query (all 24 heads: each gathered row serves both KV heads'
-//     12 query heads);
+//   * a query's 24 heads in one CTA (each gathered row serves both KV heads'
+//     12 query heads); the prefill kernel (attn_mq_kernel, below) gives a
+//     CTA 16 neighbouring queries one after the other with its copy ring
+//     running on across them, the decode splits one query's blocks;
 //   * two producer warps (one for K, one for V) issue one 4 KiB
 //     cp.async.bulk per selected block into a ring of 64 KiB stages of 8
 //     blocks; block slots are skewed by 16 bytes so the tensor-core operand
@@ -28,7 +30,7 @@
 //     V.  Every consumer waits on every stage: with an odd ring depth,
 //     consumers that skipped stages could wait on a slot two fills ahead,
 //     which a one-bit phase parity cannot tell apart.
-// Decode runs the same kernel over a slice of the selected blocks per CTA
+// Decode runs attn_kernel over a slice of the selected blocks per CTA
 // (split-KV) and a second kernel merges the slices by log-sum-exp.
 #include "qsa_common.cuh"
 #include "qsa_kernels.h"
