@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int n = 0; n < 12; ++n) sLsum[(quarter * 2 + g) * 12 + n] = l[n];
         }
         if (nt > 0 && ok && !wait_or_abort(o_full, 0, abort_flag)) ok = false;
-        ok = !softmax_bar_or(!ok);  // one verdict for the four warps (also orders sLsum)
+        ok = !softmax_bar_or(!ok);  // one decision for the four warps (also orders sLsum)
         const bool have = nt > 0 && ok;
         constexpr float kLn2 = 0.693147180559945309f;
         if (tid < 24) {
